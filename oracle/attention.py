@@ -1,0 +1,160 @@
+"""f64 oracle: scaled-dot-product attention written out from its definition.
+
+TEST INFRASTRUCTURE ONLY (tests, the smoke check and the CPU-baseline leg of the
+bench).  Plain numpy, float64 throughout, one head at a time, the full score matrix
+materialised.  No blocking, no online softmax, no split over keys: the fused kernels
+reach this same result in another order, and this file is the definition they are
+checked against.
+
+Sources (page titles and the test or function each step follows)
+-----------------------------------------------------------------
+* The formula, one head: ``softmax(scale * q k^T) v`` with the row maximum subtracted
+  before the exponential and a causal row ``i`` seeing its first ``i + Lk - Lq + 1``
+  keys -- "nuvec-core 0.5.0 tests/fast.rs", test
+  ``attention_fallback_matches_a_direct_formula``.
+* The materialised reference (scores, mask, softmax, weighted sum of V) --
+  "lattice-inference 0.4.0 src/attention/flash.rs", test helper
+  ``reference_attention_head``.
+* Masked keys carry a score of minus infinity, so their weight is exactly zero, and a
+  row with no visible key yields zeros, never NaN -- same page,
+  ``run_tiled_attention_head`` and tests ``masked_key_below_finite_sentinel_does_not_dominate``,
+  ``all_masked_row_yields_zero_output_not_nan``.
+* Grouped-query heads: query head ``h`` reads key/value head ``h / (Hq / Hkv)`` --
+  same page, ``kv_head_index``.
+* Boolean mask ``[Lq, Lk]``, true = attend, shared by every batch item and head;
+  sinks are one value per query head, in the input dtype -- "nuvec-core 0.5.0
+  tests/fast.rs", the fused-attention tests building ``bmask`` and ``sinks``.
+* No keys give zeros (also with a causal mask and with sinks) -- same page, test
+  ``window_errors_empty_inputs_and_full_windows``.
+
+Readings where the pages are silent
+-----------------------------------
+* A sink is one extra logit per query head in *score space* (it is not multiplied by
+  ``scale``) whose value row is zero: it only adds ``exp(sink - m)`` to the
+  denominator.  This is the one reading under which "no keys give zeros, with sinks
+  too" holds.
+* ``lse`` is the natural log of the full denominator, sink included, over scaled
+  scores: ``lse = m + ln Z``.  A row with no visible key and no sink has
+  ``lse = -inf``; with a sink and no visible key, ``lse = sink`` and the output is 0.
+* Causal alignment is bottom-right for any ``Lq`` and ``Lk``: row ``i`` sees key ``j``
+  iff ``j <= i + Lk - Lq``.  With ``Lq > Lk`` the first rows see no key (zeros).
+* ``scale`` is the f32 value the caller passes, widened exactly.
+"""
+from __future__ import annotations
+
+from typing import Iterable, Optional
+
+import numpy as np
+
+__all__ = ["visible_mask", "attend_rows", "sdpa", "sdpa_sampled"]
+
+
+def visible_mask(mask_kind: str, Lq: int, Lk: int, rows: np.ndarray,
+                 bool_mask: Optional[np.ndarray] = None) -> np.ndarray:
+    """Which keys each query row in ``rows`` may attend to: bool ``[len(rows), Lk]``."""
+    rows = np.asarray(rows, dtype=np.int64)
+    j = np.arange(Lk, dtype=np.int64)
+    if mask_kind == "none":
+        return np.ones((rows.size, Lk), dtype=bool)
+    if mask_kind == "causal":
+        return j[None, :] <= rows[:, None] + (Lk - Lq)
+    if mask_kind == "bool":
+        if bool_mask is None:
+            raise ValueError("bool mask kind needs a mask")
+        return np.asarray(bool_mask)[rows, :] != 0
+    raise ValueError(f"unknown mask kind {mask_kind!r}")
+
+
+def attend_rows(q_rows: np.ndarray, k_head: np.ndarray, v_head: np.ndarray,
+                vis: np.ndarray, scale: float, sink: Optional[float] = None):
+    """Attention of some query rows of one head over all keys of its KV head.
+
+    q_rows [n, d], k_head [Lk, d], v_head [Lk, dv] (f64); vis [n, Lk] bool;
+    scale, sink as f64 (sink None = no sink).  Returns (out [n, dv], lse [n]).
+    """
+    q_rows = np.asarray(q_rows, dtype=np.float64)
+    k_head = np.asarray(k_head, dtype=np.float64)
+    v_head = np.asarray(v_head, dtype=np.float64)
+    n, Lk, dv = q_rows.shape[0], k_head.shape[0], v_head.shape[1]
+    # scores s_ij = scale * <q_i, k_j>, minus infinity where key j is not visible
+    s = np.float64(scale) * (q_rows @ k_head.T) if Lk else np.zeros((n, 0))
+    s = np.where(vis, s, -np.inf)
+    # row maximum over the visible scores and the sink logit
+    m = s.max(axis=1) if Lk else np.full(n, -np.inf)
+    if sink is not None:
+        m = np.maximum(m, np.float64(sink))
+    empty = m == -np.inf
+    m_safe = np.where(empty, 0.0, m)
+    # unnormalised weights and the denominator
+    p = np.where(vis, np.exp(s - m_safe[:, None]), 0.0)
+    z = p.sum(axis=1)
+    if sink is not None:
+        z = z + np.exp(np.float64(sink) - m_safe)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        out = (p @ v_head) / z[:, None] if Lk else np.zeros((n, dv))
+        lse = m + np.log(z)
+    out = np.where(empty[:, None], 0.0, out)
+    lse = np.where(empty, -np.inf, lse)
+    return out, lse
+
+
+def _kv_head(h: int, Hq: int, Hkv: int) -> int:
+    return h // (Hq // Hkv)
+
+
+def _check(q, k, v):
+    B, Hq, Lq, d = q.shape
+    Bk, Hkv, Lk, dk = k.shape
+    if v.shape[:3] != (B, Hkv, Lk) or Bk != B or dk != d or Hkv == 0 or Hq % Hkv:
+        raise ValueError(f"bad shapes q{q.shape} k{k.shape} v{v.shape}")
+    return B, Hq, Hkv, Lq, Lk, d, v.shape[3]
+
+
+def sdpa(q, k, v, *, mask_kind: str, scale: float, bool_mask=None, sinks=None):
+    """Full attention forward in f64.
+
+    q [B,Hq,Lq,d], k [B,Hkv,Lk,d], v [B,Hkv,Lk,dv] (any real dtype, widened to f64);
+    mask_kind in {"none","causal","bool"}; bool_mask [Lq,Lk] (nonzero = attend);
+    sinks [Hq] or None.  Returns (out [B,Hq,Lq,dv] f64, lse [B,Hq,Lq] f64).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, Hq, Hkv, Lq, Lk, d, dv = _check(q, k, v)
+    out = np.zeros((B, Hq, Lq, dv))
+    lse = np.full((B, Hq, Lq), -np.inf)
+    rows = np.arange(Lq)
+    vis = visible_mask(mask_kind, Lq, Lk, rows, bool_mask)
+    for b in range(B):
+        for h in range(Hq):
+            hk = _kv_head(h, Hq, Hkv)
+            sink = None if sinks is None else float(np.asarray(sinks, dtype=np.float64)[h])
+            out[b, h], lse[b, h] = attend_rows(q[b, h], k[b, hk], v[b, hk], vis, scale, sink)
+    return out, lse
+
+
+def sdpa_sampled(q, k, v, samples: Iterable, *, mask_kind: str, scale: float,
+                 bool_mask=None, sinks=None):
+    """The same definition at selected outputs only: ``samples`` is a list of
+    (b, h, i).  Returns (out [n, dv], lse [n]) in the order of ``samples``.
+    Used where the full problem is too large for the oracle to finish in seconds."""
+    samples = list(samples)
+    B, Hq, Lq, d = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    dv = v.shape[3]
+    out = np.zeros((len(samples), dv))
+    lse = np.zeros(len(samples))
+    groups = {}
+    for n, (b, h, i) in enumerate(samples):
+        groups.setdefault((b, h), []).append((n, i))
+    for (b, h), lst in groups.items():
+        idx = np.array([n for n, _ in lst])
+        rows = np.array([i for _, i in lst])
+        hk = _kv_head(h, Hq, Hkv)
+        vis = visible_mask(mask_kind, Lq, Lk, rows, bool_mask)
+        sink = None if sinks is None else float(np.asarray(sinks, dtype=np.float64)[h])
+        o, l = attend_rows(np.asarray(q[b, h][rows], dtype=np.float64),
+                           np.asarray(k[b, hk], dtype=np.float64),
+                           np.asarray(v[b, hk], dtype=np.float64), vis, scale, sink)
+        out[idx], lse[idx] = o, l
+    return out, lse
