@@ -1,0 +1,479 @@
+#!/usr/bin/env python3
+"""Throughput of the fused attention forward on GB300, against the roofline.
+
+Headline: prefill bf16 GQA (B=2, Hq=32, Hkv=8, Lq=Lk=4096, d=dv=128, causal) in
+TFLOP/s, with algorithmic FLOPs 4*B*Hq*Lq*Lk*d halved for the causal mask.  Beside it,
+on the same JSON line: the split-KV decode (f16, B=8, Hq=32, Hkv=4, Lq=1, Lk=32769,
+d=128, sinks) in GB/s of K+V read, the end-to-end rate through the host-buffer entry
+point, each dominant kernel's roofline fraction, clocks sampled during the timed
+region, and the f64 CPU oracle timed on a bounded sample.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own copy of the workload (weak scaling,
+no collective on the data path); rank 0 prints the line with the max time over ranks.
+--impl reference times the oracle (the only reference arm there is) on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+L2_BYTES = 129 * 2 ** 20 * 1.0
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK}, "measured"
+    except Exception:
+        return dict(FALLBACK), "fallback"
+
+
+def prefill_flops(c: W.Case) -> float:
+    f = 2.0 * c.B * c.Hq * c.Lq * c.Lk * (c.d + c.dv)
+    return f / 2 if c.mask == "causal" else f
+
+
+def kv_bytes(c: W.Case) -> float:
+    return float(c.B * c.Hkv * c.Lk * (c.d + c.dv) * W.ELT_BYTES[c.dtype])
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples every 100 ms while running (read-only queries)."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.rows = []
+        self.proc = None
+        self.marks = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        rows = self.rows
+        if len(self.marks) >= 2:
+            inside = [r for t, r in rows if self.marks[0] <= t <= self.marks[-1] + 0.15]
+            rows = inside if inside else [r for _, r in rows]
+        else:
+            rows = [r for _, r in rows]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4)
+                          if len(r) > 5 + k and r[5 + k].lower() == "active"})
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+def gpu_id_for_smi(torch, dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[dev] if vis else str(dev)
+
+
+# ----------------------------------------------------------------------------- traffic
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "scaled_dot_product_nv_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel sources (profiles/traffic.txt: '<key> <source hash> <bytes>')."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    src = kernel_source_hash()
+    for line in open(p):
+        parts = line.split()
+        if len(parts) >= 3 and parts[0] == kernel_key and parts[1] == src:
+            return float(parts[2])
+    return None
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample_rate(c: W.Case, x: dict, budget_s: float, max_rows: int = None):
+    """Times the f64 oracle on evenly spread query rows of consecutive (b, h) until the
+    budget is spent.  Returns (value in the metric's unit, seconds, sample description)."""
+    import oracle
+    q, k, v = (W.widen(x[n], c.dtype) for n in ("q", "k", "v"))
+    sinks = None if x["sinks"] is None else W.widen(x["sinks"], c.dtype)
+    per_row_flops = prefill_flops(c) / (c.B * c.Hq * c.Lq)
+    per_row_bytes = kv_bytes(c) / (c.B * c.Hq * c.Lq)
+    block = max(1, min(c.Lq, 256))
+    rows_done, t0, heads = 0, time.perf_counter(), 0
+    bh = 0
+    while True:
+        b, h = divmod(bh % (c.B * c.Hq), c.Hq)
+        idx = np.linspace(0, c.Lq - 1, block).round().astype(int) if c.Lq > block else np.arange(c.Lq)
+        samples = [(b, h, int(i)) for i in idx]
+        oracle.sdpa_sampled(q, k, v, samples, mask_kind=c.mask, scale=c.scale_f32,
+                            bool_mask=x["mask"], sinks=sinks)
+        rows_done += len(samples)
+        heads += 1
+        bh += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_rows and rows_done >= max_rows):
+            break
+    sample = f"{rows_done} query rows ({len(samples)} evenly spread rows in each of {heads} (b, h) heads)"
+    if c.Lq == 1:
+        return rows_done * per_row_bytes / el / 1e9, el, sample
+    return rows_done * per_row_flops / el / 1e12, el, sample
+
+
+def host_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def time_calls(torch, call, sets, steps, warmup, stream):
+    """Warm-up, then EXACTLY `steps` calls timed with CUDA events on `stream`; the
+    inputs rotate over `sets` so that L2 cannot hold a step's inputs from the last."""
+    for w in range(warmup):
+        call(sets[w % len(sets)])
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for s in range(steps):
+        ev[s][0].record(stream)
+        call(sets[s % len(sets)])
+        ev[s][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    total_ms = start.elapsed_time(end)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    return total_ms, launch_ms
+
+
+def run_ours(args):
+    import torch
+    import scaled_dot_product_nv_gb300 as nv
+    nv.lib()  # fails loudly if the CUDA library is missing
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    stream = torch.cuda.current_stream(dev)
+    pk, pk_src = peaks()
+
+    # --------------------------------------------------------------- prefill (headline)
+    pc = W.prefill_bf16_gqa()
+    px = W.make_inputs(pc)
+
+    def to_dev(stored, dt):
+        if dt == "bf16":
+            t = torch.from_numpy(np.ascontiguousarray(stored).view(np.int16)).view(torch.bfloat16)
+        else:
+            t = torch.from_numpy(np.ascontiguousarray(stored))
+        return t.to(dev)
+
+    def device_sets(case, x, nsets):
+        base = {n: (to_dev(x[n], case.dtype) if x[n] is not None else None)
+                for n in ("q", "k", "v", "sinks")}
+        base["mask"] = to_dev(x["mask"], "u8") if x["mask"] is not None else None
+        sets = [base]
+        for _ in range(nsets - 1):
+            sets.append({n: (t.clone() if t is not None else None) for n, t in base.items()})
+        for s in sets:
+            s["out"] = torch.empty((case.B, case.Hq, case.Lq, case.dv), dtype=s["q"].dtype, device=dev)
+            s["lse"] = torch.empty((case.B, case.Hq, case.Lq), dtype=torch.float32, device=dev)
+        return sets
+
+    def caller(case):
+        dims = (case.B, case.Hq, case.Hkv, case.Lq, case.Lk, case.d, case.dv)
+        mk, dt = W.MASK_CODES[case.mask], W.DTYPE_CODES[case.dtype]
+        cs = stream.cuda_stream
+
+        def call(s):
+            st = nv.nv_sdpa(s["q"].data_ptr(), s["k"].data_ptr(), s["v"].data_ptr(), dims, mk,
+                            s["mask"].data_ptr() if s["mask"] is not None else 0,
+                            s["sinks"].data_ptr() if s["sinks"] is not None else 0,
+                            case.scale_f32, s["out"].data_ptr(), s["lse"].data_ptr(), dt, cs)
+            if st != 0:
+                raise nv.NvSdpaError(st)
+        return call
+
+    def set_bytes(case):
+        n = case.numel()
+        e = W.ELT_BYTES[case.dtype]
+        return (n["q"] + n["k"] + n["v"] + n["out"]) * e + n["lse"] * 4
+
+    psets = device_sets(pc, px, max(2, math.ceil(2 * L2_BYTES / set_bytes(pc)) + 1))
+    st_, pplan = nv.nv_sdpa_plan((pc.B, pc.Hq, pc.Hkv, pc.Lq, pc.Lk, pc.d, pc.dv),
+                                 W.MASK_CODES[pc.mask], 0, W.DTYPE_CODES[pc.dtype])
+    pcall = caller(pc)
+    gpu_name = torch.cuda.get_device_name(dev)
+    sampler = ClockSampler(gpu_id_for_smi(torch, local))
+    # untimed warm-up that also lets the clocks settle before the timed region
+    for w in range(args.warmup):
+        pcall(psets[w % len(psets)])
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    sampler.mark()
+    total_ms, launch_ms = time_calls(torch, pcall, psets, args.steps, 0, stream)
+    sampler.mark()
+    if pg:
+        pg.barrier()
+    clocks = sampler.stop()
+    t = torch.tensor([total_ms], device=dev)
+    if pg:
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    total_ms_max = float(t.item())
+    flops_step = prefill_flops(pc)
+    value = ws * flops_step * args.steps / (total_ms_max / 1e3) / 1e12
+    launch_avg = statistics.mean(launch_ms)
+    peak_t = pk["bf16_tflops"]
+    p_achieved = flops_step / (launch_avg / 1e3) / 1e12
+    pkernel = pplan["kernel"]
+
+    # --------------------------------------------------------------- decode (secondary)
+    dc = W.decode_f16_long_kv()
+    dx = W.make_inputs(dc)
+    dsets = device_sets(dc, dx, 2)
+    _, dplan = nv.nv_sdpa_plan((dc.B, dc.Hq, dc.Hkv, dc.Lq, dc.Lk, dc.d, dc.dv),
+                               W.MASK_CODES[dc.mask], 1, W.DTYPE_CODES[dc.dtype])
+    dsteps = max(args.steps, 50)
+    d_total, d_launch = time_calls(torch, caller(dc), dsets, dsteps, max(args.warmup, 3), stream)
+    dbytes = kv_bytes(dc)
+    d_call_avg = statistics.mean(d_launch)
+    d_gbs = dbytes / (d_call_avg / 1e3) / 1e9
+    decode = {
+        "workload": dc.name, "metric": "decode KV GB/s", "value": round(d_gbs, 1), "unit": "GB/s",
+        "ms_per_call": round(d_call_avg, 5), "steps": dsteps, "kernel": dplan["kernel"],
+        "nblk": dplan["nblk"], "launches_per_call": dplan["launches"],
+        "roofline": {"bound": "hbm", "achieved": round(d_gbs, 1), "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(d_gbs / pk["hbm_gbs"], 4),
+                     "peak_source": pk_src + " hbm_gbs (copy)",
+                     "timed": "whole call (pass 1 + merge) per CUDA-event pair",
+                     "traffic": recorded_traffic("decode:" + dc.name)},
+        "algorithmic_bytes_per_call": dbytes,
+    }
+
+    # --------------------------------------------------------------- end to end (host buffers)
+    e2e_steps = min(args.steps, 10)
+    pin = {n: torch.from_numpy(np.ascontiguousarray(px[n]).view(np.int16)).pin_memory()
+           for n in ("q", "k", "v")}
+    hout = torch.empty((pc.B, pc.Hq, pc.Lq, pc.dv), dtype=torch.int16).pin_memory()
+    hlse = torch.empty((pc.B, pc.Hq, pc.Lq), dtype=torch.float32).pin_memory()
+    dims = (pc.B, pc.Hq, pc.Hkv, pc.Lq, pc.Lk, pc.d, pc.dv)
+
+    def host_call(_):
+        st = nv.nv_sdpa_host(pin["q"].data_ptr(), pin["k"].data_ptr(), pin["v"].data_ptr(), dims,
+                             W.MASK_CODES[pc.mask], 0, 0, pc.scale_f32, hout.data_ptr(),
+                             hlse.data_ptr(), W.DTYPE_CODES[pc.dtype], stream.cuda_stream)
+        if st != 0:
+            raise nv.NvSdpaError(st, "nv_sdpa_host")
+    host_call(None)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        host_call(None)
+    e2e_s = time.perf_counter() - t0
+    te = torch.tensor([e2e_s], device=dev)
+    if pg:
+        pg.all_reduce(te, op=pg.ReduceOp.MAX)
+    e2e_value = ws * flops_step * e2e_steps / float(te.item()) / 1e12
+    h2d = sum(int(pin[n].numel()) * 2 for n in pin)
+    d2h = int(hout.numel()) * 2 + int(hlse.numel()) * 4
+
+    # --------------------------------------------------------------- CPU oracle baseline
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        val, secs, sample = oracle_sample_rate(pc, px, args.cpu_budget)
+        cpu = {"value": round(val, 6), "unit": "TFLOP/s", "cores": host_threads(), "kind": "oracle",
+               "sample": f"{pc.name}: {sample}, {secs:.1f} s of f64 numpy on the host",
+               "seconds": round(secs, 2)}
+
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return 0
+    launches = args.steps * int(pplan["launches"])
+    line = {
+        "metric": "prefill attention TFLOP/s & decode KV GB/s (1 GB300) vs roofline",
+        "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms_max / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded LCG; 0.5*N(0,1) values)",
+        "config": {"workload": pc.name, "B": pc.B, "Hq": pc.Hq, "Hkv": pc.Hkv, "Lq": pc.Lq,
+                   "Lk": pc.Lk, "d": pc.d, "dv": pc.dv, "mask": pc.mask,
+                   "flops_per_step": flops_step, "kernel": pkernel,
+                   "l2": f"inputs rotate over {len(psets)} device copies "
+                         f"({len(psets) * set_bytes(pc) / 2**20:.0f} MiB > 2x the 129 MB L2)",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU"},
+        "roofline": {"bound": "tensor", "achieved": round(p_achieved, 2), "peak": peak_t,
+                     "unit": "TFLOP/s", "frac": round(p_achieved / peak_t, 4),
+                     "peak_source": pk_src + " bf16_tflops (burst, cuBLAS)",
+                     "kernel_ms": round(launch_avg, 5),
+                     "traffic": recorded_traffic("prefill:" + pc.name)},
+        "decode": decode,
+        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "api": "nv_sdpa_host (pinned host buffers; copies, device alloc, sync inside)"},
+        "cpu_baseline": cpu,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "gpu": gpu_name,
+    }
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The reference arm: the f64 oracle on the host cores, each step a bounded sample
+    of the prefill workload (evenly spread query rows), sized so that warm-up plus
+    steps end within a few minutes."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    pc = W.prefill_bf16_gqa()
+    px = W.make_inputs(pc)
+    q, k, v = (W.widen(px[n], pc.dtype) for n in ("q", "k", "v"))
+    per_row = prefill_flops(pc) / (pc.B * pc.Hq * pc.Lq)
+
+    def step(nrows, s):
+        b, h = divmod(s % (pc.B * pc.Hq), pc.Hq)
+        idx = np.linspace(0, pc.Lq - 1, nrows).round().astype(int)
+        oracle.sdpa_sampled(q, k, v, [(b, h, int(i)) for i in idx], mask_kind=pc.mask,
+                            scale=pc.scale_f32)
+    t0 = time.perf_counter()
+    step(64, 0)
+    t_row = (time.perf_counter() - t0) / 64
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    nrows = int(max(16, min(pc.Lq, budget / max(t_row, 1e-6))))
+    for w in range(args.warmup):
+        step(nrows, w)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        step(nrows, s)
+    el = time.perf_counter() - t0
+    val = nrows * args.steps * per_row / el / 1e12
+    sample = (f"{pc.name}: {nrows} evenly spread query rows of one (b, h) head per step, "
+              f"f64 numpy on the host")
+    line = {
+        "impl": "reference", "metric": "prefill attention TFLOP/s & decode KV GB/s (1 GB300) vs roofline",
+        "value": round(val, 6), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded LCG; 0.5*N(0,1) values)",
+        "config": {"workload": pc.name, "B": pc.B, "Hq": pc.Hq, "Hkv": pc.Hkv, "Lq": pc.Lq,
+                   "Lk": pc.Lk, "d": pc.d, "dv": pc.dv, "mask": pc.mask},
+        "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": host_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps, always
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,158 @@
+/*
+ * nv_sdpa -- fused scaled-dot-product attention forward for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (one head; "nuvec-core 0.5.0 tests/fast.rs", test
+ * attention_fallback_matches_a_direct_formula, and the fused-attention tests there):
+ *
+ *     out[b,h,i,:] = sum_j softmax_j(scale * <q[b,h,i,:], k[b,hk,j,:]> (+ mask)) * v[b,hk,j,:]
+ *
+ * with hk = h / (Hq / Hkv) (grouped-query heads; "lattice-inference 0.4.0
+ * src/attention/flash.rs", kv_head_index), masked keys at a score of minus infinity,
+ * rows with no visible key giving zeros ("lattice-inference 0.4.0
+ * src/attention/flash.rs", tests all_masked_row_yields_zero_output_not_nan and
+ * masked_key_below_finite_sentinel_does_not_dominate), and an optional per-head sink
+ * logit that adds exp(sink - m) to the softmax denominator only (a sink is passed
+ * per query head in the input dtype in the nuvec fused-attention tests; this library
+ * reads it as a logit in score space, not multiplied by scale, with a zero value row).
+ *
+ * All entry points are plain C.  Device pointers are CUDA device addresses of the
+ * current device; `stream` is a cudaStream_t (NULL = the legacy default stream).
+ * Every call is asynchronous with respect to the host, like a kernel launch, unless
+ * stated otherwise.  No entry point ever falls back to the CPU.
+ *
+ * Layouts (all contiguous, row-major, element type = `dtype`):
+ *   q    [B, Hq,  Lq, d ]        k [B, Hkv, Lk, d]        v [B, Hkv, Lk, dv]
+ *   out  [B, Hq,  Lq, dv]        lse [B, Hq, Lq] float32 (natural log; may be NULL)
+ *   bool_mask [Lq, Lk] uint8, nonzero = attend, shared by every batch item and head
+ *   sinks [Hq] in `dtype`, or NULL
+ *
+ * Error behaviour: every argument check runs on the host before anything is launched;
+ * a failed check returns its status and launches nothing.  Errors are returned, never
+ * raised or printed.  Device-side waits are bounded: a wait that runs out records
+ * NV_SDPA_ERR_DEVICE_TIMEOUT in a per-device status word that nv_sdpa_device_status()
+ * reads, and the kernel returns instead of hanging.
+ */
+#ifndef NV_SDPA_H
+#define NV_SDPA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define NV_SDPA_ABI_VERSION 1
+
+/* Element types of q, k, v, sinks and out. */
+typedef enum { NV_SDPA_F32 = 0, NV_SDPA_F16 = 1, NV_SDPA_BF16 = 2 } nv_sdpa_dtype;
+
+/* Mask kinds.  CAUSAL is aligned bottom-right: query row i sees key j iff
+ * j <= i + (Lk - Lq) ("nuvec-core 0.5.0 tests/fast.rs", the direct-formula test's
+ * visible count i + lk - lq + 1).  With Lq > Lk the first Lq - Lk rows see no key.
+ * BOOL reads bool_mask[i * Lk + j] ("nuvec-core 0.5.0 tests/fast.rs", the boolean
+ * mask of shape [lq, lk] in the fused-attention tests). */
+typedef enum { NV_SDPA_MASK_NONE = 0, NV_SDPA_MASK_CAUSAL = 1, NV_SDPA_MASK_BOOL = 2 } nv_sdpa_mask;
+
+typedef enum {
+  NV_SDPA_OK = 0,
+  NV_SDPA_ERR_INVALID = 1,        /* bad argument: shape, pointer, kind, overflow   */
+  NV_SDPA_ERR_UNSUPPORTED = 2,    /* valid, but (d, dv) or alignment not built here  */
+  NV_SDPA_ERR_CUDA = 3,           /* a CUDA runtime call failed (launch, allocation) */
+  NV_SDPA_ERR_DEVICE_TIMEOUT = 4  /* a bounded device-side wait ran out              */
+} nv_sdpa_status;
+
+/* Problem sizes.  B, Hq, Lq, Lk >= 0; Hkv >= 1 with Hq % Hkv == 0; 8 <= d, dv <= 256,
+ * both multiples of 8 (this covers every head size 64..256 and (96,64), (192,128)). */
+typedef struct {
+  int64_t B, Hq, Hkv, Lq, Lk, d, dv;
+} nv_sdpa_dims;
+
+typedef enum {
+  NV_SDPA_PATH_NOOP = 0,     /* B*Hq*Lq == 0: nothing to write                         */
+  NV_SDPA_PATH_NO_KEYS = 1,  /* Lk == 0: out = 0, lse = sink or -inf                   */
+  NV_SDPA_PATH_PREFILL = 2,  /* Lq > 8: tiled online softmax                           */
+  NV_SDPA_PATH_DECODE = 3    /* Lq <= 8: split-KV pass 1 + log-sum-exp merge pass 2    */
+} nv_sdpa_path;
+
+typedef enum {
+  NV_SDPA_KERNEL_NONE = 0,
+  NV_SDPA_KERNEL_FILL = 1,          /* Lk == 0 rows                                     */
+  NV_SDPA_KERNEL_PREFILL_TC = 2,    /* tcgen05 + TMEM + TMA prefill, f16/bf16           */
+  NV_SDPA_KERNEL_TILED_SIMT = 3,    /* FP32-FMA tiled online softmax (f32; any path)    */
+  NV_SDPA_KERNEL_DECODE_MMA = 4     /* TMA-staged tensor-core decode pass 1, f16/bf16   */
+} nv_sdpa_kernel;
+
+/* What nv_sdpa() will launch for a problem.  Pure: a function of its arguments only
+ * (same answer on every call, thread and device), like the pure attention planner of
+ * "nuvec-core 0.6.1 tests/attention_plan.rs" (plans_are_pure). */
+typedef struct {
+  int32_t path;          /* nv_sdpa_path                                                */
+  int32_t kernel;        /* nv_sdpa_kernel of the main (first) launch                   */
+  int64_t nblk;          /* decode/SIMT: key blocks per KV head; >1 adds the merge pass */
+  int64_t keys_per_blk;  /* keys each block covers                                      */
+  int64_t rows_per_cta;  /* query rows of one KV head handled by one CTA                */
+  int64_t grid;          /* CTAs of the main launch                                     */
+  int64_t launches;      /* kernels launched by one nv_sdpa() call                      */
+  int64_t scratch_bytes; /* device scratch nv_sdpa() allocates on `stream` (partials)   */
+} nv_sdpa_plan_t;
+
+/* nv_sdpa: the fused attention forward.
+ *   q, k, v   device, dtype, layouts above; must be 16-byte aligned.
+ *   dims      host pointer, read during the call only.
+ *   mask_kind nv_sdpa_mask.  bool_mask: device [Lq, Lk] uint8 when mask_kind is BOOL,
+ *             ignored otherwise.
+ *   sinks     device [Hq] of dtype, or NULL for no sinks.
+ *   scale     any finite float (0 and negative allowed); multiplies q.k, not the sink.
+ *   out       device [B, Hq, Lq, dv] dtype, written once, rounded to nearest even from
+ *             the f32 accumulator ("nuvec-core 0.5.0 tests/fast.rs",
+ *             half_precision_softmax_is_precise: one rounding at the end).
+ *   lse       device [B, Hq, Lq] float32 or NULL: m + ln(sum of weights incl. sink).
+ *   dtype     nv_sdpa_dtype.   stream: cudaStream_t.
+ * Ownership: the caller owns every buffer.  When the plan has nblk > 1, the call takes
+ * plan.scratch_bytes of device memory with cudaMallocAsync on `stream` and frees it with
+ * cudaFreeAsync on the same stream; nothing else is allocated, nothing synchronises.
+ * Returns NV_SDPA_OK or an nv_sdpa_status; on error nothing was launched (INVALID,
+ * UNSUPPORTED) or a launch failed (CUDA). */
+int nv_sdpa(const void* q, const void* k, const void* v, const nv_sdpa_dims* dims,
+            int mask_kind, const uint8_t* bool_mask, const void* sinks, float scale,
+            void* out, float* lse, int dtype, void* stream);
+
+/* nv_sdpa_plan: the plan nv_sdpa() follows for these arguments, without launching
+ * anything or touching a device.  Applies exactly the checks of nv_sdpa() that do not
+ * need pointers (shapes, kinds, dtype, head sizes, size overflow) and returns the same
+ * status for them.  `plan` is a host pointer, written on success. */
+int nv_sdpa_plan(const nv_sdpa_dims* dims, int mask_kind, int has_sinks, int dtype,
+                 nv_sdpa_plan_t* plan);
+
+/* nv_sdpa_host: the same operation on HOST buffers (same layouts), for callers without
+ * device memory of their own.  Allocates device buffers with cudaMallocAsync on `stream`,
+ * copies the inputs in, runs nv_sdpa, copies out (and lse, if not NULL) back, frees, and
+ * synchronises `stream` before returning.  Pinned host memory makes the copies fastest.
+ * `bool_mask` and `sinks` are host pointers here too. */
+int nv_sdpa_host(const void* q, const void* k, const void* v, const nv_sdpa_dims* dims,
+                 int mask_kind, const uint8_t* bool_mask, const void* sinks, float scale,
+                 void* out, float* lse, int dtype, void* stream);
+
+/* nv_sdpa_device_status: synchronises `stream`, then reads and clears the current
+ * device's status word.  Returns NV_SDPA_OK, NV_SDPA_ERR_DEVICE_TIMEOUT (a bounded wait
+ * in a kernel ran out; that launch's outputs are not valid), or NV_SDPA_ERR_CUDA.
+ * If `detail` is not NULL it receives the raw status word (which wait gave up). */
+int nv_sdpa_device_status(void* stream, uint32_t* detail);
+
+/* Test hook for the bounded waits: sets the iteration limit of every device-side wait
+ * of later launches on this process (0 = the built-in default).  A tiny limit makes
+ * the waits run out so that the timeout path can be checked without hanging anything. */
+int nv_sdpa_set_wait_limit(uint64_t spins);
+
+/* A short, static, human-readable name of a status code. */
+const char* nv_sdpa_status_string(int status);
+
+/* NV_SDPA_ABI_VERSION of the loaded library. */
+int nv_sdpa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NV_SDPA_H */

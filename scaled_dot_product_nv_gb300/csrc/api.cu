@@ -1,0 +1,282 @@
+// The C ABI of nv_sdpa: argument checks, the pure planner/router, launches on the
+// caller's stream, the per-device status word and the host-buffer entry point.
+//
+// Checks follow "nuvec-core 0.6.1 tests/attention_plan.rs"
+// (invalid_options_are_rejected_by_plan_and_op: the plan and the op reject the same
+// inputs) and "nuvec-core 0.5.0 tests/fast.rs" (attention_fallback_matches_a_direct_formula:
+// a head count that does not group is an error).  Size products are checked for
+// overflow before anything is allocated, like the guards of "lattice-inference 0.4.0
+// src/attention/flash.rs" (assert_tiled_scratch_no_overflow).
+#include <atomic>
+#include <cmath>
+#include <cstring>
+
+#include "../../include/nv_sdpa.h"
+#include "common.cuh"
+#include "kernels.h"
+
+#define NV_SDPA_API extern "C" __attribute__((visibility("default")))
+
+namespace nvsdpa {
+namespace {
+
+__device__ uint32_t g_status;  // per-device status word (bounded waits record here)
+
+constexpr int kMaxDevices = 64;
+uint32_t* g_status_ptr[kMaxDevices];
+std::atomic<uint64_t> g_wait_limit{0};
+constexpr uint64_t kDefaultWaitLimit = 1ull << 22;  // spins, each with a short back-off
+
+int elt_bytes(int dtype) { return dtype == NV_SDPA_F32 ? 4 : 2; }
+
+bool mul_ok(int64_t a, int64_t b, int64_t* r) {
+  if (__builtin_mul_overflow(a, b, r)) return false;
+  return *r <= (int64_t(1) << 62);
+}
+
+// Checks that need no pointer.  Returns NV_SDPA_OK or the status.
+int check_dims(const nv_sdpa_dims* dm, int mask_kind, int dtype) {
+  if (!dm) return NV_SDPA_ERR_INVALID;
+  const nv_sdpa_dims& x = *dm;
+  if (dtype != NV_SDPA_F32 && dtype != NV_SDPA_F16 && dtype != NV_SDPA_BF16) return NV_SDPA_ERR_INVALID;
+  if (mask_kind != NV_SDPA_MASK_NONE && mask_kind != NV_SDPA_MASK_CAUSAL && mask_kind != NV_SDPA_MASK_BOOL)
+    return NV_SDPA_ERR_INVALID;
+  if (x.B < 0 || x.Hq < 0 || x.Lq < 0 || x.Lk < 0 || x.Hkv < 1 || x.d < 1 || x.dv < 1)
+    return NV_SDPA_ERR_INVALID;
+  if (x.Hq % x.Hkv != 0) return NV_SDPA_ERR_INVALID;
+  const int64_t e = elt_bytes(dtype);
+  int64_t t;
+  // every tensor's byte size must be representable
+  if (!mul_ok(x.B, x.Hq, &t) || !mul_ok(t, x.Lq, &t) || !mul_ok(t, std::max(x.d, x.dv), &t) || !mul_ok(t, e, &t))
+    return NV_SDPA_ERR_INVALID;
+  if (!mul_ok(x.B, x.Hkv, &t) || !mul_ok(t, x.Lk, &t) || !mul_ok(t, std::max(x.d, x.dv), &t) || !mul_ok(t, e, &t))
+    return NV_SDPA_ERR_INVALID;
+  if (!mul_ok(x.Lq, x.Lk, &t)) return NV_SDPA_ERR_INVALID;
+  // head sizes this build has kernels for
+  if (x.d > 256 || x.dv > 256 || x.d % 8 || x.dv % 8) return NV_SDPA_ERR_UNSUPPORTED;
+  return NV_SDPA_OK;
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// The router.  Pure: depends on its arguments only.  The key-block count depends on
+// Lk and the per-batch-item work (Hkv x row tiles), never on B, so that a batch item
+// gets the bits of the same item run alone.
+int make_plan(const nv_sdpa_dims& x, int mask_kind, int has_sinks, int dtype, nv_sdpa_plan_t* pl) {
+  (void)mask_kind;
+  (void)has_sinks;
+  std::memset(pl, 0, sizeof(*pl));
+  pl->nblk = 1;
+  if (x.B == 0 || x.Hq == 0 || x.Lq == 0) {
+    pl->path = NV_SDPA_PATH_NOOP;
+    pl->kernel = NV_SDPA_KERNEL_NONE;
+    return NV_SDPA_OK;
+  }
+  const int64_t g = x.Hq / x.Hkv, G = g * x.Lq;
+  if (x.Lk == 0) {
+    pl->path = NV_SDPA_PATH_NO_KEYS;
+    pl->kernel = NV_SDPA_KERNEL_FILL;
+    pl->grid = 1;
+    pl->launches = 1;
+    return NV_SDPA_OK;
+  }
+  pl->path = x.Lq > 8 ? NV_SDPA_PATH_PREFILL : NV_SDPA_PATH_DECODE;
+  (void)dtype;
+  // FP32-FMA tiled kernel, split over key blocks when one CTA per row tile would leave
+  // most SMs idle.
+  pl->kernel = NV_SDPA_KERNEL_TILED_SIMT;
+  pl->rows_per_cta = tiled_simt_rows_per_cta();
+  const int64_t row_tiles = cdiv(G, pl->rows_per_cta);
+  const int64_t units = x.Hkv * row_tiles;     // CTAs per batch item with one block
+  const int64_t kMinKeys = 256;                  // keys per block, at least
+  const int64_t kTargetCtas = 2 * 152;           // per batch item
+  int64_t nblk = cdiv(kTargetCtas, units);
+  nblk = std::min(nblk, cdiv(x.Lk, kMinKeys));
+  nblk = std::max<int64_t>(1, std::min(nblk, merge_max_blocks()));
+  int64_t kpb = cdiv(cdiv(x.Lk, nblk), 128) * 128;  // multiple of every key tile
+  nblk = cdiv(x.Lk, kpb);
+  pl->nblk = nblk;
+  pl->keys_per_blk = kpb;
+  int64_t grid;
+  if (!mul_ok(x.B * x.Hkv, row_tiles, &grid) || !mul_ok(grid, nblk, &grid) || grid > 0x7fffffff)
+    return NV_SDPA_ERR_UNSUPPORTED;
+  pl->grid = grid;
+  pl->launches = nblk > 1 ? 2 : 1;
+  if (nblk > 1) {
+    const int64_t rows = x.B * x.Hq * x.Lq;
+    const int64_t o_bytes = cdiv(rows * nblk * x.dv * 4, 256) * 256;
+    pl->scratch_bytes = o_bytes + rows * nblk * 2 * 4;
+  }
+  return NV_SDPA_OK;
+}
+
+uint32_t* status_ptr_for_current_device(cudaError_t* err) {
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!g_status_ptr[dev]) {
+    void* ptr = nullptr;
+    *err = cudaGetSymbolAddress(&ptr, g_status);
+    if (*err != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<uint32_t*>(ptr);
+  }
+  return g_status_ptr[dev];
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+}  // namespace nvsdpa
+
+using namespace nvsdpa;
+
+NV_SDPA_API int nv_sdpa_abi_version(void) { return NV_SDPA_ABI_VERSION; }
+
+NV_SDPA_API const char* nv_sdpa_status_string(int s) {
+  switch (s) {
+    case NV_SDPA_OK: return "ok";
+    case NV_SDPA_ERR_INVALID: return "invalid argument";
+    case NV_SDPA_ERR_UNSUPPORTED: return "unsupported head size, alignment or launch size";
+    case NV_SDPA_ERR_CUDA: return "CUDA runtime error";
+    case NV_SDPA_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
+    default: return "unknown status";
+  }
+}
+
+NV_SDPA_API int nv_sdpa_plan(const nv_sdpa_dims* dims, int mask_kind, int has_sinks, int dtype,
+                             nv_sdpa_plan_t* plan) {
+  if (!plan) return NV_SDPA_ERR_INVALID;
+  int st = check_dims(dims, mask_kind, dtype);
+  if (st != NV_SDPA_OK) return st;
+  return make_plan(*dims, mask_kind, has_sinks, dtype, plan);
+}
+
+NV_SDPA_API int nv_sdpa_set_wait_limit(uint64_t spins) {
+  g_wait_limit.store(spins);
+  return NV_SDPA_OK;
+}
+
+NV_SDPA_API int nv_sdpa(const void* q, const void* k, const void* v, const nv_sdpa_dims* dims,
+                        int mask_kind, const uint8_t* bool_mask, const void* sinks, float scale,
+                        void* out, float* lse, int dtype, void* stream) {
+  int st = check_dims(dims, mask_kind, dtype);
+  if (st != NV_SDPA_OK) return st;
+  if (!std::isfinite(scale)) return NV_SDPA_ERR_INVALID;
+  const nv_sdpa_dims& x = *dims;
+  nv_sdpa_plan_t pl;
+  st = make_plan(x, mask_kind, sinks != nullptr, dtype, &pl);
+  if (st != NV_SDPA_OK) return st;
+  if (pl.path == NV_SDPA_PATH_NOOP) return NV_SDPA_OK;
+  // pointers: required ones present and aligned
+  const int64_t e = elt_bytes(dtype);
+  if (!out || !aligned(out, 16)) return NV_SDPA_ERR_INVALID;
+  if (lse && !aligned(lse, 4)) return NV_SDPA_ERR_INVALID;
+  if (sinks && !aligned(sinks, (uintptr_t)e)) return NV_SDPA_ERR_INVALID;
+  if (pl.path != NV_SDPA_PATH_NO_KEYS) {
+    if (!q || !k || !v || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16)) return NV_SDPA_ERR_INVALID;
+    if (mask_kind == NV_SDPA_MASK_BOOL && !bool_mask) return NV_SDPA_ERR_INVALID;
+  }
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t ce;
+  Params p{};
+  p.q = q; p.k = k; p.v = v;
+  p.mask = mask_kind == NV_SDPA_MASK_BOOL ? bool_mask : nullptr;
+  p.sinks = sinks; p.out = out; p.lse = lse;
+  p.status = status_ptr_for_current_device(&ce);
+  if (!p.status) return NV_SDPA_ERR_CUDA;
+  p.B = x.B; p.Hq = x.Hq; p.Hkv = x.Hkv; p.Lq = x.Lq; p.Lk = x.Lk; p.d = x.d; p.dv = x.dv;
+  p.g = x.Hq / x.Hkv; p.G = p.g * x.Lq;
+  p.nblk = pl.nblk; p.keys_per_blk = pl.keys_per_blk;
+  p.row_tiles = pl.rows_per_cta ? (p.G + pl.rows_per_cta - 1) / pl.rows_per_cta : 1;
+  p.mask_kind = mask_kind;
+  p.has_sinks = sinks != nullptr;
+  p.scale = scale;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  const uint64_t wl = g_wait_limit.load();
+  p.wait_limit = wl ? wl : kDefaultWaitLimit;
+
+  if (pl.path == NV_SDPA_PATH_NO_KEYS) {
+    ce = launch_fill_no_keys(dtype, p, cs);
+    return ce == cudaSuccess ? NV_SDPA_OK : NV_SDPA_ERR_CUDA;
+  }
+  void* scratch = nullptr;
+  if (pl.scratch_bytes) {
+    ce = cudaMallocAsync(&scratch, (size_t)pl.scratch_bytes, cs);
+    if (ce != cudaSuccess) return NV_SDPA_ERR_CUDA;
+    const int64_t rows = x.B * x.Hq * x.Lq;
+    const int64_t o_bytes = (rows * pl.nblk * x.dv * 4 + 255) / 256 * 256;
+    p.part_o = static_cast<float*>(scratch);
+    p.part_ml = reinterpret_cast<float*>(static_cast<char*>(scratch) + o_bytes);
+  }
+  ce = launch_tiled_simt(dtype, p, cs);
+  if (ce == cudaSuccess && pl.nblk > 1) ce = launch_merge(dtype, p, cs);
+  if (scratch) {
+    cudaError_t fe = cudaFreeAsync(scratch, cs);
+    if (ce == cudaSuccess) ce = fe;
+  }
+  return ce == cudaSuccess ? NV_SDPA_OK : NV_SDPA_ERR_CUDA;
+}
+
+NV_SDPA_API int nv_sdpa_device_status(void* stream, uint32_t* detail) {
+  cudaError_t ce = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (ce != cudaSuccess) return NV_SDPA_ERR_CUDA;
+  uint32_t w = 0;
+  ce = cudaMemcpyFromSymbol(&w, g_status, sizeof(w));
+  if (ce != cudaSuccess) return NV_SDPA_ERR_CUDA;
+  if (w) {
+    const uint32_t zero = 0;
+    ce = cudaMemcpyToSymbol(g_status, &zero, sizeof(zero));
+    if (ce != cudaSuccess) return NV_SDPA_ERR_CUDA;
+  }
+  if (detail) *detail = w;
+  if (!w) return NV_SDPA_OK;
+  if (w & kStatBadConfig) return NV_SDPA_ERR_UNSUPPORTED;
+  return NV_SDPA_ERR_DEVICE_TIMEOUT;
+}
+
+NV_SDPA_API int nv_sdpa_host(const void* q, const void* k, const void* v, const nv_sdpa_dims* dims,
+                             int mask_kind, const uint8_t* bool_mask, const void* sinks, float scale,
+                             void* out, float* lse, int dtype, void* stream) {
+  int st = check_dims(dims, mask_kind, dtype);
+  if (st != NV_SDPA_OK) return st;
+  if (!std::isfinite(scale)) return NV_SDPA_ERR_INVALID;
+  const nv_sdpa_dims& x = *dims;
+  const int64_t e = elt_bytes(dtype);
+  const size_t nq = (size_t)(x.B * x.Hq * x.Lq * x.d * e), nk = (size_t)(x.B * x.Hkv * x.Lk * x.d * e),
+               nv = (size_t)(x.B * x.Hkv * x.Lk * x.dv * e), no = (size_t)(x.B * x.Hq * x.Lq * x.dv * e),
+               nl = (size_t)(x.B * x.Hq * x.Lq * 4), nm = (size_t)(x.Lq * x.Lk), ns = (size_t)(x.Hq * e);
+  if ((nq && !q) || (nk && !k) || (nv && !v) || (no && !out)) return NV_SDPA_ERR_INVALID;
+  if (mask_kind == NV_SDPA_MASK_BOOL && nm && !bool_mask) return NV_SDPA_ERR_INVALID;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const bool use_mask = mask_kind == NV_SDPA_MASK_BOOL && nm;
+  const bool use_lse = lse && nl;
+  const bool use_sinks = sinks != nullptr;
+  // one device block holds every buffer, each piece 256-byte aligned
+  auto up = [](size_t n) { return (n + 255) / 256 * 256; };
+  const size_t oq = 0, ok = oq + up(nq), ov = ok + up(nk), oo = ov + up(nv), ol = oo + up(no),
+               om = ol + up(use_lse ? nl : 0), os = om + up(use_mask ? nm : 0), total = os + up(use_sinks ? ns : 0);
+  char* dbuf = nullptr;
+  cudaError_t ce = cudaMallocAsync(reinterpret_cast<void**>(&dbuf), total ? total : 256, cs);
+  if (ce != cudaSuccess) return NV_SDPA_ERR_CUDA;
+  if (nq) ce = cudaMemcpyAsync(dbuf + oq, q, nq, cudaMemcpyHostToDevice, cs);
+  if (ce == cudaSuccess && nk) ce = cudaMemcpyAsync(dbuf + ok, k, nk, cudaMemcpyHostToDevice, cs);
+  if (ce == cudaSuccess && nv) ce = cudaMemcpyAsync(dbuf + ov, v, nv, cudaMemcpyHostToDevice, cs);
+  if (ce == cudaSuccess && use_mask) ce = cudaMemcpyAsync(dbuf + om, bool_mask, nm, cudaMemcpyHostToDevice, cs);
+  if (ce == cudaSuccess && use_sinks) ce = cudaMemcpyAsync(dbuf + os, sinks, ns, cudaMemcpyHostToDevice, cs);
+  if (ce == cudaSuccess) {
+    st = nv_sdpa(dbuf + oq, dbuf + ok, dbuf + ov, dims, mask_kind,
+                 use_mask ? reinterpret_cast<const uint8_t*>(dbuf + om) : nullptr,
+                 use_sinks ? dbuf + os : nullptr, scale, dbuf + oo,
+                 use_lse ? reinterpret_cast<float*>(dbuf + ol) : nullptr, dtype, stream);
+  } else {
+    st = NV_SDPA_ERR_CUDA;
+  }
+  if (st == NV_SDPA_OK && no) ce = cudaMemcpyAsync(out, dbuf + oo, no, cudaMemcpyDeviceToHost, cs);
+  if (st == NV_SDPA_OK && ce == cudaSuccess && use_lse)
+    ce = cudaMemcpyAsync(lse, dbuf + ol, nl, cudaMemcpyDeviceToHost, cs);
+  if (st == NV_SDPA_OK && ce != cudaSuccess) st = NV_SDPA_ERR_CUDA;
+  cudaError_t fe = cudaFreeAsync(dbuf, cs);
+  cudaError_t se = cudaStreamSynchronize(cs);
+  if (st == NV_SDPA_OK && (fe != cudaSuccess || se != cudaSuccess)) st = NV_SDPA_ERR_CUDA;
+  return st;
+}

@@ -1,0 +1,87 @@
+// Shared device-side definitions of the nv_sdpa kernels: element conversions, the
+// launch parameters, the per-device status word and the bounded-wait budget.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nvsdpa {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kMaskNone = 0, kMaskCausal = 1, kMaskBool = 2;
+
+// Bits of the device status word (OR-ed in by a kernel whose bounded wait ran out).
+enum : uint32_t {
+  kStatTimeoutTmaFull = 1u << 0,   // a consumer waited too long for a TMA load
+  kStatTimeoutSlotFree = 1u << 1,  // a producer waited too long for a free stage
+  kStatTimeoutMma = 1u << 2,       // a waiter on an MMA commit gave up
+  kStatTimeoutTmem = 1u << 3,      // waiting on the TMEM handoff gave up
+  kStatBadConfig = 1u << 8,        // the kernel found a launch configuration it cannot run
+};
+
+// Everything a kernel needs to know about one call.
+struct Params {
+  const void* q;
+  const void* k;
+  const void* v;
+  const uint8_t* mask;  // [Lq, Lk] or null
+  const void* sinks;    // [Hq] or null
+  void* out;            // [B, Hq, Lq, dv]
+  float* lse;           // [B, Hq, Lq] or null
+  float* part_o;        // split-KV partials [B*Hq*Lq][nblk][dv] (unnormalised)
+  float* part_ml;       // [B*Hq*Lq][nblk][2]: running max (log2 units) and sum
+  uint32_t* status;     // per-device status word
+  int64_t B, Hq, Hkv, Lq, Lk, d, dv;
+  int64_t g;            // Hq / Hkv
+  int64_t G;            // g * Lq: query rows that share one KV head
+  int64_t nblk;         // key blocks per KV head (1 = final output written directly)
+  int64_t keys_per_blk; // keys per block (a multiple of every kernel's key tile)
+  int64_t row_tiles;    // ceil(G / rows per CTA)
+  int mask_kind;
+  int has_sinks;
+  float scale;          // as passed
+  float scale_log2;     // scale * log2(e): scores are kept in log2 units
+  uint64_t wait_limit;  // spin budget of every bounded wait
+};
+
+template <typename T> __device__ __forceinline__ float to_f32(T x);
+template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f32<__half>(__half x) { return __half2float(x); }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// 2^x on the SFU; exact 0 for x = -inf.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Sink logit of query head h in log2 units, or -inf.
+template <typename T>
+__device__ __forceinline__ float sink_log2(const Params& p, int64_t h) {
+  if (!p.has_sinks) return -INFINITY;
+  return to_f32<T>(reinterpret_cast<const T*>(p.sinks)[h]) * kLog2e;
+}
+
+// Last key index query row i may see under the causal mask (bottom-right aligned).
+__device__ __forceinline__ int64_t causal_last_key(const Params& p, int64_t i) {
+  return i + (p.Lk - p.Lq);
+}
+
+__device__ __forceinline__ void record_status(const Params& p, uint32_t bits) {
+  if (p.status) atomicOr(p.status, bits);
+}
+
+}  // namespace nvsdpa

@@ -1,0 +1,335 @@
+// FP32-FMA tiled online-softmax attention (all dtypes), the split-KV merge pass and
+// the no-key fill.
+//
+// The tiled kernel follows the online softmax of "lattice-inference 0.4.0
+// src/attention/flash.rs" (run_tiled_attention_head): per key tile, scores, the row
+// maximum, the rescale alpha = exp(m_old - m_new) of the running sum and output, and a
+// final division by the sum -- with masked keys at minus infinity and an all-masked
+// row giving zeros.  Here the scores are kept in log2 units (scale * log2 e folded into
+// one multiplier) and exponentials are 2^x.
+//
+// Work split: one CTA takes 32 query rows that share one KV head -- the g = Hq/Hkv
+// query heads of that KV head times their Lq rows, head-major -- and the keys of one
+// key block.  With one block it writes the normalised output; with several it writes
+// (m, l, o) partials that sdpa_merge_partials combines (the split-KV two-pass scheme
+// of the vector kernels named in "nuvec-core 0.6.1 tests/attention_plan.rs").
+#include "common.cuh"
+#include "kernels.h"
+
+namespace nvsdpa {
+
+namespace {
+
+constexpr int kRows = 32;      // query rows per CTA (one per lane)
+constexpr int kKeys = 32;      // keys per tile (8 per warp)
+constexpr int kThreads = 128;  // 4 warps
+constexpr int kMaxDvPerThread = 64;  // dv <= 256 over 4 warps
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+sdpa_tiled_simt(const Params p) {
+  extern __shared__ float smem[];
+  const int d = (int)p.d, dv = (int)p.dv;
+  const int ldq = d + 1;  // odd row stride: lane-per-row reads hit distinct banks
+  float* Qs = smem;                         // [kRows][d+1]
+  float* Ks = Qs + kRows * ldq;             // [kKeys][d+1]
+  float* Vs = Ks + kKeys * ldq;             // [kKeys][dv]
+  float* Ps = Vs + kKeys * dv;              // [kRows][kKeys+1]
+  float* red_max = Ps + kRows * (kKeys + 1);  // [4][32]
+  float* red_sum = red_max + 4 * 32;          // [4][32]
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int64_t x = blockIdx.x;
+  const int64_t rt = x % p.row_tiles; x /= p.row_tiles;
+  const int64_t blk = x % p.nblk;
+  const int64_t bh = x / p.nblk;  // b * Hkv + hkv
+  const int64_t b = bh / p.Hkv, hkv = bh % p.Hkv;
+
+  const T* Kg = reinterpret_cast<const T*>(p.k) + bh * p.Lk * p.d;
+  const T* Vg = reinterpret_cast<const T*>(p.v) + bh * p.Lk * p.dv;
+
+  // This lane's query row.
+  const int64_t rho = rt * kRows + lane;
+  const bool row_ok = rho < p.G;
+  const int64_t hh = row_ok ? rho / p.Lq : 0, i = row_ok ? rho % p.Lq : 0;
+  const int64_t h = hkv * p.g + hh;
+  const int64_t row_global = (b * p.Hq + h) * p.Lq + i;
+
+  // Stage the 32 query rows (zeros past the last row).
+  for (int idx = tid; idx < kRows * d; idx += kThreads) {
+    const int r = idx / d, c = idx % d;
+    const int64_t rr = rt * kRows + r;
+    float val = 0.f;
+    if (rr < p.G) {
+      const int64_t qh = hkv * p.g + rr / p.Lq, qi = rr % p.Lq;
+      val = to_f32<T>(reinterpret_cast<const T*>(p.q)[((b * p.Hq + qh) * p.Lq + qi) * p.d + c]);
+    }
+    Qs[r * ldq + c] = val;
+  }
+
+  // Keys of this block, cut at the last key any row of the tile may see.
+  const int64_t j_begin = blk * p.keys_per_blk;
+  int64_t j_end = j_begin + p.keys_per_blk;
+  if (j_end > p.Lk) j_end = p.Lk;
+  if (p.mask_kind == kMaskCausal) {
+    // the largest i among this tile's rows (rows wrap at Lq when a tile spans heads)
+    const int64_t r0 = rt * kRows;
+    int64_t r1 = r0 + kRows - 1;
+    if (r1 > p.G - 1) r1 = p.G - 1;
+    int64_t imax = (r0 / p.Lq == r1 / p.Lq) ? r1 % p.Lq : p.Lq - 1;
+    const int64_t lim = causal_last_key(p, imax) + 1;
+    if (j_end > lim) j_end = lim;
+  }
+  const int64_t my_last = causal_last_key(p, i);
+  const uint8_t* mrow = (p.mask_kind == kMaskBool) ? p.mask + i * p.Lk : nullptr;
+
+  float m = -INFINITY, l = 0.f;
+  float o[kMaxDvPerThread];
+#pragma unroll
+  for (int kk = 0; kk < kMaxDvPerThread; ++kk) o[kk] = 0.f;
+
+  for (int64_t j0 = j_begin; j0 < j_end; j0 += kKeys) {
+    __syncthreads();  // previous tile fully consumed (and Qs staged on the first pass)
+    for (int idx = tid; idx < kKeys * d; idx += kThreads) {
+      const int r = idx / d, c = idx % d;
+      const int64_t j = j0 + r;
+      Ks[r * ldq + c] = j < j_end ? to_f32<T>(Kg[j * p.d + c]) : 0.f;
+    }
+    for (int idx = tid; idx < kKeys * dv; idx += kThreads) {
+      const int r = idx / dv, c = idx % dv;
+      const int64_t j = j0 + r;
+      Vs[r * dv + c] = j < j_end ? to_f32<T>(Vg[j * p.dv + c]) : 0.f;
+    }
+    __syncthreads();
+
+    // Scores of this lane's row against the warp's 8 keys.
+    float s[8];
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) s[jj] = 0.f;
+    const float* qrow = Qs + lane * ldq;
+    const float* kbase = Ks + (warp * 8) * ldq;
+    for (int c = 0; c < d; ++c) {
+      const float qc = qrow[c];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) s[jj] = fmaf(qc, kbase[jj * ldq + c], s[jj]);
+    }
+    float tmax = -INFINITY;
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      const int64_t j = j0 + warp * 8 + jj;
+      bool vis = row_ok && j < j_end;
+      if (p.mask_kind == kMaskCausal) vis = vis && j <= my_last;
+      else if (p.mask_kind == kMaskBool) vis = vis && mrow[j] != 0;
+      s[jj] = vis ? s[jj] * p.scale_log2 : -INFINITY;
+      tmax = fmaxf(tmax, s[jj]);
+    }
+    red_max[warp * 32 + lane] = tmax;
+    __syncthreads();
+    tmax = fmaxf(fmaxf(red_max[lane], red_max[32 + lane]), fmaxf(red_max[64 + lane], red_max[96 + lane]));
+    const float m_new = fmaxf(m, tmax);
+    float alpha, tsum = 0.f;
+    if (m_new == -INFINITY) {  // nothing visible yet: keep zeros, no NaN
+      alpha = 1.f;
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) Ps[lane * (kKeys + 1) + warp * 8 + jj] = 0.f;
+    } else {
+      alpha = ex2(m - m_new);
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const float pj = ex2(s[jj] - m_new);
+        Ps[lane * (kKeys + 1) + warp * 8 + jj] = pj;
+        tsum += pj;
+      }
+    }
+    red_sum[warp * 32 + lane] = tsum;
+    __syncthreads();
+    tsum = (red_sum[lane] + red_sum[32 + lane]) + (red_sum[64 + lane] + red_sum[96 + lane]);
+    l = l * alpha + tsum;
+    m = m_new;
+    const float* prow = Ps + lane * (kKeys + 1);
+#pragma unroll
+    for (int kk = 0; kk < kMaxDvPerThread; ++kk) {
+      const int c = warp + 4 * kk;
+      if (c < dv) {
+        float acc = o[kk] * alpha;
+#pragma unroll 8
+        for (int j = 0; j < kKeys; ++j) acc = fmaf(prow[j], Vs[j * dv + c], acc);
+        o[kk] = acc;
+      }
+    }
+  }
+  if (!row_ok) return;
+
+  if (p.nblk == 1) {
+    const float sk = sink_log2<T>(p, h);
+    const float M = fmaxf(m, sk);
+    T* orow = reinterpret_cast<T*>(p.out) + row_global * p.dv;
+    if (M == -INFINITY) {
+#pragma unroll
+      for (int kk = 0; kk < kMaxDvPerThread; ++kk) {
+        const int c = warp + 4 * kk;
+        if (c < dv) orow[c] = from_f32<T>(0.f);
+      }
+      if (warp == 0 && p.lse) p.lse[row_global] = -INFINITY;
+      return;
+    }
+    const float a = ex2(m - M);
+    const float L = l * a + ex2(sk - M);
+    const float f = a / L;
+#pragma unroll
+    for (int kk = 0; kk < kMaxDvPerThread; ++kk) {
+      const int c = warp + 4 * kk;
+      if (c < dv) orow[c] = from_f32<T>(o[kk] * f);
+    }
+    if (warp == 0 && p.lse) p.lse[row_global] = (M + log2f(L)) * kLn2;
+  } else {
+    float* po = p.part_o + (row_global * p.nblk + blk) * p.dv;
+#pragma unroll
+    for (int kk = 0; kk < kMaxDvPerThread; ++kk) {
+      const int c = warp + 4 * kk;
+      if (c < dv) po[c] = o[kk];
+    }
+    if (warp == 0) {
+      p.part_ml[(row_global * p.nblk + blk) * 2 + 0] = m;
+      p.part_ml[(row_global * p.nblk + blk) * 2 + 1] = l;
+    }
+  }
+}
+
+// Pass 2 of split-KV: one warp per query row merges its nblk partials,
+//   M = max(max_blk m_blk, sink),  L = sum_blk l_blk 2^(m_blk - M) + 2^(sink - M),
+//   out = sum_blk o_blk 2^(m_blk - M) / L,  lse = (M + log2 L) ln 2.
+constexpr int kMergeWarps = 4;
+constexpr int kMaxBlk = 1024;
+
+template <typename T>
+__global__ void __launch_bounds__(kMergeWarps * 32)
+sdpa_merge_partials(const Params p) {
+  __shared__ float w_s[kMergeWarps][kMaxBlk];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t rows = p.B * p.Hq * p.Lq;
+  const int64_t row = (int64_t)blockIdx.x * kMergeWarps + warp;
+  if (row >= rows) return;
+  const int64_t h = (row / p.Lq) % p.Hq;
+  const int nb = (int)p.nblk;
+  const float* ml = p.part_ml + row * p.nblk * 2;
+  const float sk = sink_log2<T>(p, h);
+  float M = sk;
+  for (int k = lane; k < nb; k += 32) M = fmaxf(M, ml[2 * k]);
+#pragma unroll
+  for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  T* orow = reinterpret_cast<T*>(p.out) + row * p.dv;
+  if (M == -INFINITY) {
+    for (int c = lane; c < p.dv; c += 32) orow[c] = from_f32<T>(0.f);
+    if (lane == 0 && p.lse) p.lse[row] = -INFINITY;
+    return;
+  }
+  float L = 0.f;
+  for (int k = lane; k < nb; k += 32) {
+    const float mk = ml[2 * k];
+    const float w = (mk == -INFINITY) ? 0.f : ex2(mk - M);
+    w_s[warp][k] = w;
+    L += ml[2 * k + 1] * w;
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  L += ex2(sk - M);
+  __syncwarp();
+  const float inv = 1.f / L;
+  const float* po = p.part_o + row * p.nblk * p.dv;
+  for (int c = lane; c < p.dv; c += 32) {
+    float acc = 0.f;
+    for (int k = 0; k < nb; ++k) acc = fmaf(po[(int64_t)k * p.dv + c], w_s[warp][k], acc);
+    orow[c] = from_f32<T>(acc * inv);
+  }
+  if (lane == 0 && p.lse) p.lse[row] = (M + log2f(L)) * kLn2;
+}
+
+// Lk == 0: every row sees no key.  out = 0; lse = the sink, or -inf without sinks.
+template <typename T>
+__global__ void sdpa_fill_no_keys(const Params p) {
+  const int64_t rows = p.B * p.Hq * p.Lq;
+  const int64_t n = rows * p.dv;
+  T* out = reinterpret_cast<T*>(p.out);
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    out[e] = from_f32<T>(0.f);
+    if (p.lse && e % p.dv == 0) {
+      const int64_t row = e / p.dv, h = (row / p.Lq) % p.Hq;
+      p.lse[row] = p.has_sinks ? to_f32<T>(reinterpret_cast<const T*>(p.sinks)[h]) : -INFINITY;
+    }
+  }
+}
+
+template <typename T>
+cudaError_t launch_simt_t(const Params& p, cudaStream_t st) {
+  const size_t smem = tiled_simt_smem_bytes(p.d, p.dv);
+  static unsigned long long configured = 0;  // one bit per device ordinal < 64
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !(configured >> dev & 1ull)) {
+    e = cudaFuncSetAttribute(sdpa_tiled_simt<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)tiled_simt_smem_bytes(256, 256));
+    if (e != cudaSuccess) return e;
+    if (dev < 64) configured |= 1ull << dev;
+  }
+  const int64_t grid = p.B * p.Hkv * p.nblk * p.row_tiles;
+  sdpa_tiled_simt<T><<<(unsigned)grid, kThreads, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_merge_t(const Params& p, cudaStream_t st) {
+  const int64_t rows = p.B * p.Hq * p.Lq;
+  const int64_t grid = (rows + kMergeWarps - 1) / kMergeWarps;
+  sdpa_merge_partials<T><<<(unsigned)grid, kMergeWarps * 32, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_fill_t(const Params& p, cudaStream_t st) {
+  const int64_t n = p.B * p.Hq * p.Lq * p.dv;
+  int64_t grid = (n + 255) / 256;
+  if (grid > 152 * 16) grid = 152 * 16;
+  if (grid < 1) grid = 1;
+  sdpa_fill_no_keys<T><<<(unsigned)grid, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t tiled_simt_smem_bytes(int64_t d, int64_t dv) {
+  return sizeof(float) * (size_t)(kRows * (d + 1) + kKeys * (d + 1) + kKeys * dv +
+                                  kRows * (kKeys + 1) + 2 * 4 * 32);
+}
+
+int64_t tiled_simt_rows_per_cta() { return kRows; }
+int64_t tiled_simt_keys_per_tile() { return kKeys; }
+int64_t merge_max_blocks() { return kMaxBlk; }
+
+cudaError_t launch_tiled_simt(int dtype, const Params& p, cudaStream_t st) {
+  switch (dtype) {
+    case 0: return launch_simt_t<float>(p, st);
+    case 1: return launch_simt_t<__half>(p, st);
+    default: return launch_simt_t<__nv_bfloat16>(p, st);
+  }
+}
+
+cudaError_t launch_merge(int dtype, const Params& p, cudaStream_t st) {
+  switch (dtype) {
+    case 0: return launch_merge_t<float>(p, st);
+    case 1: return launch_merge_t<__half>(p, st);
+    default: return launch_merge_t<__nv_bfloat16>(p, st);
+  }
+}
+
+cudaError_t launch_fill_no_keys(int dtype, const Params& p, cudaStream_t st) {
+  switch (dtype) {
+    case 0: return launch_fill_t<float>(p, st);
+    case 1: return launch_fill_t<__half>(p, st);
+    default: return launch_fill_t<__nv_bfloat16>(p, st);
+  }
+}
+
+}  // namespace nvsdpa

@@ -1,0 +1,186 @@
+"""Parity of the CUDA path with the f64 oracle, through the C ABI, on seeded inputs.
+
+Element by element wherever the oracle finishes in seconds (sizes that still span
+several tiles and ragged tails), on sampled rows at the full sizes of the workloads.
+Tolerance per dtype: f32 2e-5, f16 4e-3, bf16 2e-2 of max(|want|, 1), the same for
+the log-sum-exp."""
+import itertools
+
+import numpy as np
+import pytest
+
+import workloads as W
+from helpers import TOL, assert_close, check_case, ensure_built, oracle_full, run_gpu, upload
+
+pytestmark = pytest.mark.gpu
+
+
+def _small_cases():
+    shapes = [(64, 64), (96, 64), (128, 128), (192, 128), (256, 256), (72, 72), (80, 80)]
+    heads = [(4, 2), (8, 1), (6, 6), (32, 4), (2, 1)]
+    lens = [(1, 1), (1, 300), (3, 129), (8, 1000), (9, 9), (77, 141), (200, 200), (130, 2049),
+            (333, 64), (64, 333)]
+    out = []
+    n = 0
+    for dt, mk, sk in itertools.product(["f32", "f16", "bf16"], ["none", "causal", "bool"],
+                                        [False, True]):
+        for t in range(3):
+            d, dv = shapes[n % len(shapes)]
+            hq, hkv = heads[n % len(heads)]
+            lq, lk = lens[n % len(lens)]
+            out.append(W.Case(1 + n % 2, hq, hkv, lq, lk, d, dv, dt, mk, sk, None,
+                              ["u0.25", "u2", "n0.5"][n % 3], seed=100 + n,
+                              name=f"small{n:02d}_{dt}_{mk}_s{int(sk)}_d{d}x{dv}_h{hq}x{hkv}_{lq}x{lk}"))
+            n += 1
+    return out
+
+
+SMALL = _small_cases()
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[c.name for c in SMALL])
+def test_small_cases(case):
+    check_case(case)
+
+
+def test_tiny_f32_causal():
+    check_case(W.tiny_f32_causal())
+
+
+def test_decode_f16_long_kv_full():
+    check_case(W.decode_f16_long_kv(), max_oracle_flops=1e12)
+
+
+def test_prefill_f16_boolmask_sinks_full():
+    check_case(W.prefill_f16_boolmask_sinks(), max_oracle_flops=1e12)
+
+
+def test_prefill_bf16_gqa_sampled():
+    check_case(W.prefill_bf16_gqa())
+
+
+SWEEP = W.sweep_bf16()
+
+
+@pytest.mark.parametrize("case", SWEEP, ids=[c.name for c in SWEEP])
+def test_sweep_bf16(case):
+    check_case(case, max_oracle_flops=3e9)
+
+
+# ----------------------------------------------------------------------------- edge cases
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+def test_no_keys_gives_zeros(dt):
+    for mk, sk in [("none", False), ("causal", False), ("causal", True)]:
+        c = W.Case(1, 2, 2, 3, 0, 64, 64, dt, mk, sk, 0.125, seed=7)
+        x = W.make_inputs(c)
+        got, lse = run_gpu(c, x)
+        assert got.shape == (1, 2, 3, 64) and np.all(got == 0.0)
+        if sk:
+            np.testing.assert_allclose(lse[0], np.broadcast_to(W.widen(x["sinks"], dt)[:, None], (2, 3)))
+        else:
+            assert np.all(lse == -np.inf)
+
+
+def test_no_queries_is_a_noop():
+    c = W.Case(1, 2, 2, 0, 9, 64, 64, "bf16", "causal", False, seed=8)
+    got, lse = run_gpu(c, W.make_inputs(c))
+    assert got.shape == (1, 2, 0, 64)
+
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("lq,lk", [(20, 5), (6, 2), (300, 129)])
+def test_causal_with_more_queries_than_keys(dt, lq, lk):
+    for sk in [False, True]:
+        c = W.Case(2, 4, 2, lq, lk, 64, 64, dt, "causal", sk, None, "n0.5", seed=9)
+        got, lse = check_case(c)
+        assert np.all(got[:, :, : lq - lk] == 0.0)
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("lq", [1, 5, 40, 200])
+def test_all_masked_rows_are_zero(dt, lq):
+    c = W.Case(1, 4, 2, lq, 300, 128, 128, dt, "bool", False, None, "n0.5", seed=10)
+    x = W.make_inputs(c)
+    x["mask"][::3] = 0  # every third row sees nothing
+    got, lse = check_case(c, x)
+    assert np.all(got[:, :, ::3] == 0.0) and np.all(lse[:, :, ::3] == -np.inf)
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+def test_large_group_decode(dt):
+    # 32 query heads on one KV head with 8 queries each: 256 rows per KV head
+    check_case(W.Case(1, 32, 1, 8, 5000, 128, 128, dt, "causal", True, None, "u2", seed=11))
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+def test_extreme_scores_stay_finite(dt):
+    # scores of +-100s: the online max must keep every exponent <= 0
+    c = W.Case(1, 4, 2, 70, 900, 64, 64, dt, "none", True, 4.0, "n1", seed=12)
+    check_case(c)
+
+
+# ----------------------------------------------------------------------------- invariants
+
+@pytest.mark.parametrize("lq,lk", [(300, 300), (1, 8193), (9, 777)])
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+def test_batch_items_equal_each_item_alone(lq, lk, dt):
+    """"nuvec-core 0.5.0 tests/fast.rs", attention_batch_items_equal_each_item_alone:
+    each batch item gets the bits of that item alone."""
+    import torch
+    nv = ensure_built()
+    c = W.Case(3, 8, 2, lq, lk, 128, 128, dt, "causal", True, None, "u0.25", seed=13)
+    x = W.make_inputs(c)
+    dev = upload(c, x)
+    allb, _ = nv.sdpa(dev["q"], dev["k"], dev["v"], mask_kind="causal", scale=c.scale_f32,
+                      sinks=dev["sinks"])
+    for b in range(3):
+        one, _ = nv.sdpa(dev["q"][b:b + 1].contiguous(), dev["k"][b:b + 1].contiguous(),
+                         dev["v"][b:b + 1].contiguous(), mask_kind="causal", scale=c.scale_f32,
+                         sinks=dev["sinks"])
+        assert torch.equal(allb[b:b + 1].view(torch.int16), one.view(torch.int16)), b
+
+
+def test_run_to_run_deterministic():
+    import torch
+    nv = ensure_built()
+    for c in [W.decode_f16_long_kv(), W.prefill_f16_boolmask_sinks()]:
+        x = W.make_inputs(c)
+        dev = upload(c, x)
+        outs = [nv.sdpa(dev["q"], dev["k"], dev["v"], mask_kind=c.mask, scale=c.scale_f32,
+                        bool_mask=dev["mask"], sinks=dev["sinks"]) for _ in range(3)]
+        for o, l in outs[1:]:
+            assert torch.equal(o.view(torch.int16), outs[0][0].view(torch.int16))
+            assert torch.equal(l, outs[0][1])
+
+
+def test_host_buffer_entry_point_matches_device_entry_point():
+    import torch
+    nv = ensure_built()
+    c = W.prefill_f16_boolmask_sinks().with_(Lq=200, Lk=333)
+    x = W.make_inputs(c)
+    dev = upload(c, x)
+    o_dev, l_dev = nv.sdpa(dev["q"], dev["k"], dev["v"], mask_kind=c.mask, scale=c.scale_f32,
+                           bool_mask=dev["mask"], sinks=dev["sinks"])
+    torch.cuda.synchronize()
+    out = np.empty((c.B, c.Hq, c.Lq, c.dv), dtype=np.float16)
+    lse = np.empty((c.B, c.Hq, c.Lq), dtype=np.float32)
+    st = nv.nv_sdpa_host(x["q"].ctypes.data, x["k"].ctypes.data, x["v"].ctypes.data,
+                         (c.B, c.Hq, c.Hkv, c.Lq, c.Lk, c.d, c.dv), 2, x["mask"].ctypes.data,
+                         x["sinks"].ctypes.data, c.scale_f32, out.ctypes.data, lse.ctypes.data,
+                         1, 0)
+    assert st == 0
+    np.testing.assert_array_equal(out, o_dev.cpu().numpy())
+    np.testing.assert_array_equal(lse, l_dev.cpu().numpy())
+
+
+def test_lse_only_optional_and_status_clean():
+    import torch
+    nv = ensure_built()
+    c = W.Case(1, 4, 2, 33, 100, 64, 64, "bf16", "causal", False, seed=14)
+    dev = upload(c, W.make_inputs(c))
+    o1, _ = nv.sdpa(dev["q"], dev["k"], dev["v"], mask_kind="causal", scale=c.scale_f32)
+    o2, none = nv.sdpa(dev["q"], dev["k"], dev["v"], mask_kind="causal", scale=c.scale_f32,
+                       want_lse=False)
+    assert none is None and torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert nv.nv_sdpa_device_status(0) == (0, 0)
