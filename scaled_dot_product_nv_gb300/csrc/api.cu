@@ -23,6 +23,7 @@ namespace {
 __device__ uint32_t g_status;  // per-device status word (bounded waits record here)
 
 constexpr int kMaxDevices = 64;
+constexpr int64_t kNumSms = 152;  // GB300: 2 dies x 76 SMs
 uint32_t* g_status_ptr[kMaxDevices];
 std::atomic<uint64_t> g_wait_limit{0};
 constexpr uint64_t kDefaultWaitLimit = 1ull << 22;  // spins, each with a short back-off
@@ -63,7 +64,6 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // Lk and the per-batch-item work (Hkv x row tiles), never on B, so that a batch item
 // gets the bits of the same item run alone.
 int make_plan(const nv_sdpa_dims& x, int mask_kind, int has_sinks, int dtype, nv_sdpa_plan_t* pl) {
-  (void)mask_kind;
   (void)has_sinks;
   std::memset(pl, 0, sizeof(*pl));
   pl->nblk = 1;
@@ -81,7 +81,48 @@ int make_plan(const nv_sdpa_dims& x, int mask_kind, int has_sinks, int dtype, nv
     return NV_SDPA_OK;
   }
   pl->path = x.Lq > 8 ? NV_SDPA_PATH_PREFILL : NV_SDPA_PATH_DECODE;
-  (void)dtype;
+  if (pl->path == NV_SDPA_PATH_PREFILL && prefill_tc_supported(dtype, x.d, x.dv)) {
+    // tcgen05 kernel: one CTA per 128 rows of one KV head, all keys (no split)
+    pl->kernel = NV_SDPA_KERNEL_PREFILL_TC;
+    pl->rows_per_cta = prefill_tc_rows_per_cta();
+    pl->keys_per_blk = x.Lk;
+    int64_t grid;
+    if (!mul_ok(x.B * x.Hkv, cdiv(G, pl->rows_per_cta), &grid) || grid > 0x7fffffff)
+      return NV_SDPA_ERR_UNSUPPORTED;
+    pl->grid = grid;
+    pl->launches = 1;
+    if (mask_kind == NV_SDPA_MASK_BOOL) {  // bit-packed copy of the mask
+      pl->launches = 2;
+      pl->scratch_bytes = x.Lq * (int64_t)prefill_tc_mask_words(x.Lk) * 4;
+    }
+    return NV_SDPA_OK;
+  }
+  if (pl->path == NV_SDPA_PATH_DECODE && decode_mma_supported(dtype, x.d, x.dv)) {
+    // tensor-core decode: one CTA per (b, KV head, key block, 16 query rows); enough
+    // key blocks that one batch item alone fills every CTA slot of the GPU
+    pl->kernel = NV_SDPA_KERNEL_DECODE_MMA;
+    pl->rows_per_cta = decode_mma_rows_per_cta();
+    const int64_t rc = cdiv(G, pl->rows_per_cta);
+    const int64_t slots = kNumSms * decode_mma_ctas_per_sm(x.d, x.dv);
+    const int64_t kt = decode_mma_key_tile();
+    int64_t nblk = cdiv(slots, x.Hkv * rc);
+    nblk = std::min(nblk, cdiv(x.Lk, 4 * kt));
+    nblk = std::max<int64_t>(1, std::min(nblk, merge_max_blocks()));
+    const int64_t kpb = cdiv(cdiv(x.Lk, nblk), kt) * kt;
+    nblk = cdiv(x.Lk, kpb);
+    pl->nblk = nblk;
+    pl->keys_per_blk = kpb;
+    int64_t grid;
+    if (!mul_ok(x.B * x.Hkv, rc, &grid) || !mul_ok(grid, nblk, &grid) || grid > 0x7fffffff)
+      return NV_SDPA_ERR_UNSUPPORTED;
+    pl->grid = grid;
+    pl->launches = nblk > 1 ? 2 : 1;
+    if (nblk > 1) {
+      const int64_t rows = x.B * x.Hq * x.Lq;
+      pl->scratch_bytes = cdiv(rows * nblk * x.dv * 4, 256) * 256 + rows * nblk * 2 * 4;
+    }
+    return NV_SDPA_OK;
+  }
   // FP32-FMA tiled kernel, split over key blocks when one CTA per row tile would leave
   // most SMs idle.
   pl->kernel = NV_SDPA_KERNEL_TILED_SIMT;
@@ -89,7 +130,7 @@ int make_plan(const nv_sdpa_dims& x, int mask_kind, int has_sinks, int dtype, nv
   const int64_t row_tiles = cdiv(G, pl->rows_per_cta);
   const int64_t units = x.Hkv * row_tiles;     // CTAs per batch item with one block
   const int64_t kMinKeys = 256;                  // keys per block, at least
-  const int64_t kTargetCtas = 2 * 152;           // per batch item
+  const int64_t kTargetCtas = 2 * kNumSms;       // per batch item
   int64_t nblk = cdiv(kTargetCtas, units);
   nblk = std::min(nblk, cdiv(x.Lk, kMinKeys));
   nblk = std::max<int64_t>(1, std::min(nblk, merge_max_blocks()));
@@ -208,8 +249,15 @@ NV_SDPA_API int nv_sdpa(const void* q, const void* k, const void* v, const nv_sd
     p.part_o = static_cast<float*>(scratch);
     p.part_ml = reinterpret_cast<float*>(static_cast<char*>(scratch) + o_bytes);
   }
-  ce = launch_tiled_simt(dtype, p, cs);
-  if (ce == cudaSuccess && pl.nblk > 1) ce = launch_merge(dtype, p, cs);
+  if (pl.kernel == NV_SDPA_KERNEL_PREFILL_TC) {
+    ce = launch_prefill_tc(dtype, p, static_cast<uint32_t*>(scratch), cs);
+  } else if (pl.kernel == NV_SDPA_KERNEL_DECODE_MMA) {
+    ce = launch_decode_mma(dtype, p, cs);
+    if (ce == cudaSuccess && pl.nblk > 1) ce = launch_merge(dtype, p, cs);
+  } else {
+    ce = launch_tiled_simt(dtype, p, cs);
+    if (ce == cudaSuccess && pl.nblk > 1) ce = launch_merge(dtype, p, cs);
+  }
   if (scratch) {
     cudaError_t fe = cudaFreeAsync(scratch, cs);
     if (ce == cudaSuccess) ce = fe;

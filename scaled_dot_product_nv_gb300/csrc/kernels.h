@@ -19,4 +19,20 @@ cudaError_t launch_tiled_simt(int dtype, const Params& p, cudaStream_t st);
 cudaError_t launch_merge(int dtype, const Params& p, cudaStream_t st);
 cudaError_t launch_fill_no_keys(int dtype, const Params& p, cudaStream_t st);
 
+// prefill_tc.cu
+bool prefill_tc_supported(int dtype, int64_t d, int64_t dv);
+int prefill_tc_bn(int64_t d, int64_t dv);
+size_t prefill_tc_smem_bytes(int64_t d, int64_t dv, int bn);
+int64_t prefill_tc_rows_per_cta();
+size_t prefill_tc_mask_words(int64_t Lk);
+cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, cudaStream_t st);
+
+// decode_mma.cu
+bool decode_mma_supported(int dtype, int64_t d, int64_t dv);
+int64_t decode_mma_rows_per_cta();
+int64_t decode_mma_key_tile();
+size_t decode_mma_smem_bytes(int64_t d, int64_t dv);
+int decode_mma_ctas_per_sm(int64_t d, int64_t dv);
+cudaError_t launch_decode_mma(int dtype, const Params& p, cudaStream_t st);
+
 }  // namespace nvsdpa

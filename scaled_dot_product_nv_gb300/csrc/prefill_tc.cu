@@ -1,0 +1,512 @@
+// Prefill attention on the 5th-generation tensor cores (tcgen05) for f16/bf16.
+//
+// The algorithm is the tiled online softmax of "lattice-inference 0.4.0
+// src/attention/flash.rs" (run_tiled_attention_head): per key tile, S = Q K^T, the row
+// maximum, rescale of the running sum and output, P V accumulated, one division at the
+// end; masked keys at minus infinity and all-masked rows giving zeros.  The blocking,
+// the memory movement and the exponent bookkeeping are this kernel's own:
+//
+// * One CTA owns 128 query rows of one KV head (rows of the g query heads sharing it,
+//   head-major -- contiguous in memory) and walks the key tiles of BN keys.
+// * Warp 0 (one lane) streams Q once and K/V tiles through a 2-stage ring with TMA
+//   (128-byte swizzle), completion on mbarriers.
+// * Warp 1 allocates 512 TMEM columns; one lane issues tcgen05.mma:
+//     S_t = Q K_t^T      (A, B from shared memory, f32 accumulator in TMEM, 2 buffers)
+//     O  += P_t V_t      (A = P from TMEM, B = V from shared memory, MN-major)
+//   and signals completions with tcgen05.commit.
+// * Warps 2-5 (one query row per thread = one TMEM lane): read S_t, mask, keep the
+//   running max in log2 units, write P_t = 2^(s - m) as 16-bit values back into the
+//   TMEM columns of S_t, and rescale O only when the max grew by more than 2^8
+//   (otherwise the stale max is kept: exact after the final division, and every
+//   weight stays <= 2^8).  The epilogue folds in the sink logit, divides once, rounds
+//   once to the output type and writes the log-sum-exp.
+// * Causal: key tiles wholly above the (bottom-right aligned) diagonal are skipped.
+//   Boolean masks arrive as a bit-packed copy made by sdpa_pack_mask_bits.
+// * Every mbarrier wait is bounded; a wait that runs out records a status bit, raises
+//   a shared abort flag that the other roles also watch, and the CTA drains its
+//   in-flight copies and MMAs before freeing TMEM and exiting.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "sm100_ptx.cuh"
+
+namespace nvsdpa {
+namespace {
+
+using namespace sm100;
+
+constexpr int kBM = 128;
+constexpr int kTcThreads = 192;
+constexpr int kStages = 2;
+constexpr int kTmemCols = 512;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr uint64_t kDrainLimit = 1ull << 22;
+constexpr int64_t kTcMaxSmem = 227 * 1024;  // opt-in dynamic shared memory per CTA
+
+struct TcArgs {
+  CUtensorMap tmq, tmk, tmv;  // 64-byte aligned by type
+  Params p;
+  const uint32_t* mask_bits;  // [Lq][mask_words], bit j%32 of word j/32 = key j visible
+  int64_t mask_words;
+  int n_rt;          // row tiles per (b, kv head)
+  int dpanels;       // 64-element panels of d
+  int dvpanels;      // 64-element panels of dv
+  int ksteps_qk;     // ceil(d / 16)
+  int n_pv;          // dv rounded up to 16 (MMA N of P V)
+  int itile_order;   // Lq % 128 == 0: launch the late (heavier, causal) row tiles first
+};
+
+enum { kBarQ = 0, kBarKvFull = 1, kBarKvEmpty = 1 + kStages, kBarSFull = 1 + 2 * kStages,
+       kBarPFull = 3 + 2 * kStages, kBarPvDone = 5 + 2 * kStages, kBarDrain = 6 + 2 * kStages,
+       kNumBars = 7 + 2 * kStages };
+
+__device__ __forceinline__ void fail(const Params& p, volatile int* abort, uint32_t bit) {
+  *abort = 1;
+  record_status(p, bit);
+}
+
+template <typename T> struct TypeCode;
+template <> struct TypeCode<__half> { static constexpr uint32_t v = 0; };
+template <> struct TypeCode<__nv_bfloat16> { static constexpr uint32_t v = 1; };
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <> __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) { return pack_f16(lo, hi); }
+template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+  return pack_bf16(lo, hi);
+}
+
+template <typename T, int BN>
+__global__ void __launch_bounds__(kTcThreads, 1) sdpa_prefill_tc(const __grid_constant__ TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const Params& p = a.p;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const uint32_t q_bytes = a.dpanels * kBM * 128;
+  const uint32_t k_bytes = a.dpanels * BN * 128;
+  const uint32_t v_bytes = a.dvpanels * BN * 128;
+  const uint32_t sQ = smem_addr(base);
+  const uint32_t sK = sQ + q_bytes;
+  const uint32_t sV = sK + kStages * k_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + q_bytes + kStages * (k_bytes + v_bytes));
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  auto bar = [&](int i) { return smem_addr(bars + i); };
+
+  // ---- which rows and keys this CTA owns
+  const int64_t BH = p.B * p.Hkv;
+  int64_t rt, bh;
+  if (a.itile_order) {
+    const int64_t ipt = p.Lq / kBM;  // row tiles per head
+    int64_t x = blockIdx.x;
+    const int64_t hh = x % p.g; x /= p.g;
+    bh = x % BH;
+    const int64_t it = ipt - 1 - x / BH;
+    rt = hh * ipt + it;
+  } else {
+    rt = blockIdx.x % a.n_rt;
+    bh = blockIdx.x / a.n_rt;
+  }
+  const int64_t hkv = bh % p.Hkv;
+  int64_t kend = p.Lk;
+  if (p.mask_kind == kMaskCausal) {
+    const int64_t r0 = rt * kBM;
+    const int64_t r1 = (r0 + kBM < p.G ? r0 + kBM : p.G) - 1;
+    const int64_t imax = (r0 / p.Lq == r1 / p.Lq) ? r1 % p.Lq : p.Lq - 1;
+    const int64_t lim = causal_last_key(p, imax) + 1;
+    if (lim < kend) kend = lim;
+  }
+  const int n_tiles = kend > 0 ? (int)((kend + BN - 1) / BN) : 0;
+
+  // ---- set-up: barriers, TMEM
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kBarQ), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(kBarKvFull + s), 1);
+      mbar_init(bar(kBarKvEmpty + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(kBarSFull + b), 1);
+      mbar_init(bar(kBarPFull + b), 128);
+    }
+    mbar_init(bar(kBarPvDone), 1);
+    mbar_init(bar(kBarDrain), 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_holder), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
+  const uint64_t limit = p.wait_limit;
+
+  if (warp == 0) {
+    // ================================================================ TMA producer
+    if (lane == 0 && n_tiles > 0) {
+      tma_prefetch_desc(&a.tmq);
+      tma_prefetch_desc(&a.tmk);
+      tma_prefetch_desc(&a.tmv);
+      mbar_arrive_expect_tx(bar(kBarQ), q_bytes);
+      for (int pn = 0; pn < a.dpanels; ++pn)
+        tma_load_3d(sQ + pn * kBM * 128, &a.tmq, bar(kBarQ), pn * 64, (int)(rt * kBM), (int)bh);
+      int issued = 0;
+      for (int t = 0; t < n_tiles; ++t) {
+        const int s = t % kStages;
+        if (!mbar_wait(bar(kBarKvEmpty + s), ((t / kStages) & 1) ^ 1, limit, abort)) {
+          fail(p, abort, kStatTimeoutSlotFree);
+          break;
+        }
+        mbar_arrive_expect_tx(bar(kBarKvFull + s), k_bytes + v_bytes);
+        for (int pn = 0; pn < a.dpanels; ++pn)
+          tma_load_3d(sK + s * k_bytes + pn * BN * 128, &a.tmk, bar(kBarKvFull + s), pn * 64, t * BN, (int)bh);
+        for (int pn = 0; pn < a.dvpanels; ++pn)
+          tma_load_3d(sV + s * v_bytes + pn * BN * 128, &a.tmv, bar(kBarKvFull + s), pn * 64, t * BN, (int)bh);
+        issued = t + 1;
+      }
+      // Every copy issued must land before the CTA may exit (a no-op when all were consumed).
+      mbar_wait(bar(kBarQ), 0, kDrainLimit, nullptr);
+      for (int t = issued > kStages ? issued - kStages : 0; t < issued; ++t)
+        mbar_wait(bar(kBarKvFull + t % kStages), (t / kStages) & 1, kDrainLimit, nullptr);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    if (lane == 0 && n_tiles > 0) {
+      const uint32_t idesc_s = idesc_f16(TypeCode<T>::v, 0, 0, kBM, BN);
+      const uint32_t idesc_o = idesc_f16(TypeCode<T>::v, 0, 1, kBM, a.n_pv);
+      const uint32_t tO = tmem + 2 * BN;
+      bool ok = mbar_wait(bar(kBarQ), 0, limit, abort);
+      if (!ok) fail(p, abort, kStatTimeoutTmaFull);
+      auto issue_s = [&](int t) {
+        const int s = t % kStages;
+        const uint32_t tS = tmem + (t & 1) * BN;
+        for (int k = 0; k < a.ksteps_qk; ++k) {
+          const uint32_t off = (uint32_t)(k & 3) * 32;  // 16 elements inside the 128-byte row
+          const uint64_t ad = smem_desc_sw128(sQ + (k >> 2) * kBM * 128 + off, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(sK + s * k_bytes + (k >> 2) * BN * 128 + off, 16, 1024);
+          mma_ss(tS, ad, bd, idesc_s, k > 0);
+        }
+        mma_commit(bar(kBarSFull + (t & 1)));
+      };
+      if (ok) {
+        ok = mbar_wait(bar(kBarKvFull), 0, limit, abort);
+        if (!ok) fail(p, abort, kStatTimeoutTmaFull);
+      }
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+      }
+      for (int t = 0; ok && t < n_tiles; ++t) {
+        if (t + 1 < n_tiles) {
+          const int s1 = (t + 1) % kStages;
+          if (!mbar_wait(bar(kBarKvFull + s1), ((t + 1) / kStages) & 1, limit, abort)) {
+            fail(p, abort, kStatTimeoutTmaFull);
+            break;
+          }
+          tc_fence_after();
+          issue_s(t + 1);
+        }
+        if (!mbar_wait(bar(kBarPFull + (t & 1)), (t >> 1) & 1, limit, abort)) {
+          fail(p, abort, kStatTimeoutMma);
+          break;
+        }
+        tc_fence_after();
+        const int s = t % kStages;
+        const uint32_t tP = tmem + (t & 1) * BN;
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t bd = smem_desc_sw128(sV + s * v_bytes + kk * 16 * 128, BN * 128, 1024);
+          mma_ts(tO, tP + kk * 8, bd, idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(kBarKvEmpty + s));
+        mma_commit(bar(kBarPvDone));
+      }
+      // all MMAs issued by this thread complete before TMEM can be freed
+      mma_commit(bar(kBarDrain));
+      mbar_wait(bar(kBarDrain), 0, kDrainLimit, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // ================================================================ softmax / epilogue
+    const int q4 = warp & 3;
+    const int row = q4 * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    const int64_t rho = rt * kBM + row;
+    const bool row_ok = rho < p.G;
+    const int64_t i = row_ok ? rho % p.Lq : 0;
+    const int64_t h = hkv * p.g + (row_ok ? rho / p.Lq : 0);
+    const int64_t last_key = (p.mask_kind == kMaskCausal) ? causal_last_key(p, i) : p.Lk - 1;
+    const uint32_t* mrow = a.mask_bits ? a.mask_bits + i * a.mask_words : nullptr;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int t = 0; t < n_tiles; ++t) {
+      const int buf = t & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull + buf), (t >> 1) & 1, limit, abort));
+      if (!ok) {
+        fail(p, abort, kStatTimeoutMma);
+        break;
+      }
+      tc_fence_after();
+      // scores of this row: raw dot products from TMEM, then scaled (log2 units) and masked
+      uint32_t sr_flat[BN];
+      if constexpr (BN == 128) tmem_ld128_sync(tmem + lane_base + buf * BN, sr_flat);
+      else tmem_ld64_sync(tmem + lane_base + buf * BN, sr_flat);
+      uint32_t (&sr)[BN / 32][32] = *reinterpret_cast<uint32_t (*)[BN / 32][32]>(sr_flat);
+      const int64_t j0 = (int64_t)t * BN;
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t bits = 0xffffffffu;
+        if (mrow) bits = row_ok ? __ldg(mrow + j0 / 32 + c) : 0u;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int64_t j = j0 + c * 32 + e;
+          const bool vis = row_ok && j <= last_key && ((bits >> e) & 1u);
+          const float x = vis ? __uint_as_float(sr[c][e]) * p.scale_log2 : -INFINITY;
+          sr[c][e] = __float_as_uint(x);
+          mt = fmaxf(mt, x);
+        }
+      }
+      const float m_new = fmaxf(m_run, mt);
+      const bool need = m_new > m_run + kRescaleLog2;
+      float alpha = 1.f;
+      if (need) {
+        alpha = ex2(m_run - m_new);
+        m_run = m_new;
+      }
+      // P = 2^(s - m) as 16-bit pairs into the TMEM columns of S (its A operand of P V)
+      const bool none = (m_run == -INFINITY);
+      float tsum = 0.f;
+#pragma unroll
+      for (int c2 = 0; c2 < BN / 64; ++c2) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int idx = c2 * 64 + 2 * e;
+          const float p0 = none ? 0.f : ex2(__uint_as_float(sr[idx / 32][idx % 32]) - m_run);
+          const float p1 = none ? 0.f : ex2(__uint_as_float(sr[(idx + 1) / 32][(idx + 1) % 32]) - m_run);
+          tsum += p0 + p1;
+          pk[e] = pack2<T>(p0, p1);
+        }
+        tmem_st32(tmem + lane_base + buf * BN + c2 * 32, pk);
+      }
+      l_run = l_run * alpha + tsum;
+      tmem_st_wait();
+      if (t > 0) {
+        // O must hold P_{t-1} V_{t-1} before it is rescaled for this tile's max
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarPvDone), (t - 1) & 1, limit, abort));
+        if (!ok) {
+          fail(p, abort, kStatTimeoutMma);
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, need)) {
+          for (int c = 0; c < (a.n_pv + 31) / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32_sync(tmem + lane_base + 2 * BN + c * 32, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tmem + lane_base + 2 * BN + c * 32, o);
+          }
+          tmem_st_wait();
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(kBarPFull + buf));
+    }
+    // ---- epilogue
+    if (ok && n_tiles > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarPvDone), (n_tiles - 1) & 1, limit, abort));
+      if (!ok) fail(p, abort, kStatTimeoutMma);
+      tc_fence_after();
+    }
+    ok = __all_sync(0xffffffffu, ok && !*abort);
+    if (ok) {
+      const float sk = sink_log2<T>(p, h);
+      const float M = fmaxf(m_run, sk);
+      float f = 0.f, L = 0.f;
+      if (M != -INFINITY) {
+        const float am = ex2(m_run - M);
+        L = l_run * am + ex2(sk - M);
+        f = am / L;
+      }
+      T* orow = reinterpret_cast<T*>(p.out) + (bh * p.G + rho) * p.dv;
+      const int dv = (int)p.dv;
+      for (int c = 0; c < (dv + 31) / 32; ++c) {
+        uint32_t o[32];
+        if (n_tiles > 0) {
+          tmem_ld32_sync(tmem + lane_base + 2 * BN + c * 32, o);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0u;
+        }
+        if (row_ok) {
+#pragma unroll
+          for (int e8 = 0; e8 < 4; ++e8) {
+            const int col = c * 32 + e8 * 8;
+            if (col < dv) {
+              uint4 v;
+              v.x = pack2<T>(__uint_as_float(o[e8 * 8 + 0]) * f, __uint_as_float(o[e8 * 8 + 1]) * f);
+              v.y = pack2<T>(__uint_as_float(o[e8 * 8 + 2]) * f, __uint_as_float(o[e8 * 8 + 3]) * f);
+              v.z = pack2<T>(__uint_as_float(o[e8 * 8 + 4]) * f, __uint_as_float(o[e8 * 8 + 5]) * f);
+              v.w = pack2<T>(__uint_as_float(o[e8 * 8 + 6]) * f, __uint_as_float(o[e8 * 8 + 7]) * f);
+              *reinterpret_cast<uint4*>(orow + col) = v;
+            }
+          }
+        }
+      }
+      if (row_ok && p.lse) p.lse[bh * p.G + rho] = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
+    }
+  }
+
+  // ---- tear-down
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Bool mask [Lq, Lk] bytes -> bits [Lq, words]: bit e of word w = mask[i, 32 w + e] != 0,
+// zero past Lk (the key tiles' padding).
+__global__ void sdpa_pack_mask_bits(const uint8_t* __restrict__ mask, int64_t Lq, int64_t Lk,
+                                    int64_t words, uint32_t* __restrict__ bits) {
+  const int64_t n = Lq * words;
+  for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < n;
+       w += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = w / words, j0 = (w % words) * 32;
+    uint32_t v = 0;
+    const uint8_t* row = mask + i * Lk;
+    for (int e = 0; e < 32; ++e) {
+      const int64_t j = j0 + e;
+      if (j < Lk && row[j]) v |= 1u << e;
+    }
+    bits[w] = v;
+  }
+}
+
+// ------------------------------------------------------------------------- host side
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                 CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                 CUtensorMapFloatOOBfill);
+
+EncodeTiled get_encode() {
+  static EncodeTiled fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(ptr);
+  }
+  return fn;
+}
+
+// [outer][rows][inner] 16-bit tensor, boxes of 64 x box_rows x 1 with 128-byte swizzle,
+// out-of-range elements read as zero.
+bool encode_3d(CUtensorMap* m, int dtype, const void* ptr, int64_t inner, int64_t rows, int64_t outer,
+               int box_rows) {
+  EncodeTiled enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)outer};
+  cuuint64_t strides[2] = {(cuuint64_t)(inner * 2), (cuuint64_t)(inner * rows * 2)};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                   const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <typename T, int BN>
+cudaError_t launch_tc_t(const TcArgs& a, size_t smem, int64_t grid, cudaStream_t st) {
+  static unsigned long long configured = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !(configured >> dev & 1ull)) {
+    e = cudaFuncSetAttribute(sdpa_prefill_tc<T, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kTcMaxSmem);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) configured |= 1ull << dev;
+  }
+  sdpa_prefill_tc<T, BN><<<(unsigned)grid, kTcThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int prefill_tc_bn(int64_t d, int64_t dv) {
+  // largest key tile whose 2-stage K/V ring plus the Q tile fit in shared memory and
+  // whose two S buffers plus O fit in the 512 TMEM columns
+  const int64_t dp = (d + 63) / 64, dvp = (dv + 63) / 64, npv = (dv + 15) / 16 * 16;
+  for (int bn : {128, 64}) {
+    const int64_t smem = dp * kBM * 128 + kStages * (dp + dvp) * bn * 128 + 1024 + 256;
+    if (smem <= kTcMaxSmem && 2 * bn + npv <= kTmemCols) return bn;
+  }
+  return 0;
+}
+
+size_t prefill_tc_smem_bytes(int64_t d, int64_t dv, int bn) {
+  const int64_t dp = (d + 63) / 64, dvp = (dv + 63) / 64;
+  size_t s = (size_t)(dp * kBM * 128 + kStages * (dp + dvp) * bn * 128) + 1024 /*align*/ + 256 /*bars*/;
+  // at least 120 KB so that one CTA (with its 512 TMEM columns) owns the SM
+  return s < 120 * 1024 ? 120 * 1024 : s;
+}
+
+int64_t prefill_tc_rows_per_cta() { return kBM; }
+
+bool prefill_tc_supported(int dtype, int64_t d, int64_t dv) {
+  return (dtype == 1 || dtype == 2) && d % 8 == 0 && dv % 8 == 0 && d <= 256 && dv <= 256 &&
+         prefill_tc_bn(d, dv) != 0;
+}
+
+size_t prefill_tc_mask_words(int64_t Lk) {
+  // words per mask row: every key tile of up to 128 keys reads whole words
+  return (size_t)((Lk + 127) / 128 * 4);
+}
+
+cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, cudaStream_t st) {
+  TcArgs a;
+  memset(&a, 0, sizeof(a));
+  a.p = p;
+  const int bn = prefill_tc_bn(p.d, p.dv);
+  if (!bn) return cudaErrorInvalidValue;
+  const int64_t BH = p.B * p.Hkv;
+  if (!encode_3d(&a.tmq, dtype, p.q, p.d, p.G, BH, kBM) || !encode_3d(&a.tmk, dtype, p.k, p.d, p.Lk, BH, bn) ||
+      !encode_3d(&a.tmv, dtype, p.v, p.dv, p.Lk, BH, bn))
+    return cudaErrorInvalidValue;
+  a.n_rt = (int)((p.G + kBM - 1) / kBM);
+  a.dpanels = (int)((p.d + 63) / 64);
+  a.dvpanels = (int)((p.dv + 63) / 64);
+  a.ksteps_qk = (int)((p.d + 15) / 16);
+  a.n_pv = (int)((p.dv + 15) / 16 * 16);
+  a.itile_order = (p.Lq % kBM == 0) ? 1 : 0;
+  if (p.mask_kind == kMaskBool) {
+    a.mask_words = (int64_t)prefill_tc_mask_words(p.Lk);
+    a.mask_bits = mask_bits;
+    const int64_t n = p.Lq * a.mask_words;
+    int64_t g = (n + 255) / 256;
+    if (g > 152 * 8) g = 152 * 8;
+    sdpa_pack_mask_bits<<<(unsigned)(g > 0 ? g : 1), 256, 0, st>>>(p.mask, p.Lq, p.Lk, a.mask_words, mask_bits);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t grid = BH * a.n_rt;
+  const size_t smem = prefill_tc_smem_bytes(p.d, p.dv, bn);
+  if (dtype == 1) return bn == 128 ? launch_tc_t<__half, 128>(a, smem, grid, st) : launch_tc_t<__half, 64>(a, smem, grid, st);
+  return bn == 128 ? launch_tc_t<__nv_bfloat16, 128>(a, smem, grid, st)
+                   : launch_tc_t<__nv_bfloat16, 64>(a, smem, grid, st);
+}
+
+}  // namespace nvsdpa
