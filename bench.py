@@ -460,6 +460,32 @@ def run_reference(args):
     return 0
 
 
+def run_profile_case(args):
+    """Launches one workload `args.steps` times with no timing or JSON: the program an
+    ncu capture runs (small enough to profile: the workloads' own sizes, < 1 GB)."""
+    import torch
+    import scaled_dot_product_nv_gb300 as nv
+    case = {"prefill": W.prefill_bf16_gqa(), "decode": W.decode_f16_long_kv(),
+            "mask": W.prefill_f16_boolmask_sinks(), "tiny": W.tiny_f32_causal()}[args.profile_case]
+    x = W.make_inputs(case)
+    dev = torch.device("cuda", 0)
+
+    def up(a, dt):
+        if a is None:
+            return None
+        if dt == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    q, k, v, s = (up(x[n], case.dtype) for n in ("q", "k", "v", "sinks"))
+    m = up(x["mask"], "u8")
+    for _ in range(args.steps):
+        nv.sdpa(q, k, v, mask_kind=case.mask, scale=case.scale_f32, bool_mask=m, sinks=s)
+    torch.cuda.synchronize()
+    st, detail = nv.nv_sdpa_device_status(0)
+    print(f"profile case {case.name}: {args.steps} calls, device status {st}")
+    return 0 if st == 0 else 1
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -468,7 +494,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", choices=["prefill", "decode", "mask", "tiny"],
+                    help="only launch this workload --steps times (for ncu); prints no JSON")
     args = ap.parse_args()
+    if args.profile_case:
+        return run_profile_case(args)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps, always
     if args.impl == "reference":
         return run_reference(args)
