@@ -134,6 +134,28 @@ int nv_sdpa_host(const void* q, const void* k, const void* v, const nv_sdpa_dims
                  int mask_kind, const uint8_t* bool_mask, const void* sinks, float scale,
                  void* out, float* lse, int dtype, void* stream);
 
+/* nv_sdpa_noalloc: nv_sdpa() for callers that cannot allocate device memory -- e.g. a
+ * host program whose GPU memory is owned by another allocator (a serving runtime or
+ * framework that reserves the device up front and forbids allocations outside its
+ * pool), or a loop that cannot afford an allocation call.  No counterpart on the source
+ * pages: this is a deployment variant of the same operation.
+ * Same arguments, layouts, results and checks as nv_sdpa().  It calls no cudaMalloc,
+ * cudaMallocAsync, cudaFree or other allocating routine: the scratch a plan needs
+ * (plan.scratch_bytes: split-KV partials, the bit-packed boolean mask) comes from one
+ * fixed device array of NV_SDPA_STATIC_SCRATCH_BYTES that the library defines and that
+ * every GPU loading the library holds until the process exits.  A call whose plan needs
+ * more returns NV_SDPA_ERR_UNSUPPORTED and launches nothing (nv_sdpa_plan() tells in
+ * advance).  The first call on a device looks the array's device address up
+ * (cudaGetSymbolAddress) with that device current: make that first call before any
+ * stream capture.  Every call on a device shares the one array, which keeps the last
+ * call's contents (nothing in it needs to start at zero); calls whose kernels overlap
+ * on the GPU -- on different streams, or from different host threads -- race on it and
+ * must be serialised by the caller. */
+#define NV_SDPA_STATIC_SCRATCH_BYTES (32u << 20)
+int nv_sdpa_noalloc(const void* q, const void* k, const void* v, const nv_sdpa_dims* dims,
+                    int mask_kind, const uint8_t* bool_mask, const void* sinks, float scale,
+                    void* out, float* lse, int dtype, void* stream);
+
 /* nv_sdpa_device_status: synchronises `stream`, then reads and clears the current
  * device's status word.  Returns NV_SDPA_OK, NV_SDPA_ERR_DEVICE_TIMEOUT (a bounded wait
  * in a kernel ran out; that launch's outputs are not valid), or NV_SDPA_ERR_CUDA.

@@ -5,7 +5,7 @@ module converts Python arguments to C ones and raises on a non-OK status.  There
 no CPU path: if the library is missing, loading it raises.
 
 Raw entry points (same names as the C functions, pointers as ints):
-    nv_sdpa, nv_sdpa_plan, nv_sdpa_host, nv_sdpa_device_status,
+    nv_sdpa, nv_sdpa_plan, nv_sdpa_host, nv_sdpa_noalloc, nv_sdpa_device_status,
     nv_sdpa_set_wait_limit, nv_sdpa_status_string, nv_sdpa_abi_version
 Torch convenience (torch tensors for device memory and the current stream):
     sdpa(q, k, v, mask_kind=..., scale=..., bool_mask=None, sinks=None)
@@ -67,6 +67,8 @@ def lib() -> ctypes.CDLL:
         L.nv_sdpa.restype = ctypes.c_int
         L.nv_sdpa_host.argtypes = sig
         L.nv_sdpa_host.restype = ctypes.c_int
+        L.nv_sdpa_noalloc.argtypes = sig
+        L.nv_sdpa_noalloc.restype = ctypes.c_int
         L.nv_sdpa_plan.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                    ctypes.POINTER(Plan)]
         L.nv_sdpa_plan.restype = ctypes.c_int
@@ -101,6 +103,20 @@ def nv_sdpa_host(q, k, v, dims, mask_kind, bool_mask, sinks, scale, out, lse, dt
     return lib().nv_sdpa_host(q, k, v, ctypes.byref(dims), int(mask_kind), bool_mask or None,
                               sinks or None, ctypes.c_float(scale), out, lse or None, int(dtype),
                               stream or None)
+
+
+def nv_sdpa_noalloc(q, k, v, dims, mask_kind, bool_mask, sinks, scale, out, lse, dtype, stream) -> int:
+    """nv_sdpa for callers that cannot allocate device memory: scratch comes from the
+    library's fixed device array (STATIC_SCRATCH_BYTES); calls that overlap on the GPU
+    share it and must be serialised by the caller."""
+    if not isinstance(dims, Dims):
+        dims = _dims(*dims)
+    return lib().nv_sdpa_noalloc(q, k, v, ctypes.byref(dims), int(mask_kind), bool_mask or None,
+                                 sinks or None, ctypes.c_float(scale), out, lse or None, int(dtype),
+                                 stream or None)
+
+
+STATIC_SCRATCH_BYTES = 32 << 20
 
 
 def nv_sdpa_plan(dims, mask_kind, has_sinks, dtype):

@@ -328,3 +328,109 @@ NV_SDPA_API int nv_sdpa_host(const void* q, const void* k, const void* v, const 
   if (st == NV_SDPA_OK && (fe != cudaSuccess || se != cudaSuccess)) st = NV_SDPA_ERR_CUDA;
   return st;
 }
+
+// ------------------------------------------------------------------------------------
+// nv_sdpa_noalloc: the same attention call for callers that cannot allocate device
+// memory.  Some callers run inside a host program whose device memory belongs to
+// another allocator -- a serving runtime or framework that reserves the GPU's memory up
+// front and forbids allocations outside its own pool -- or in a loop that cannot
+// afford an allocation call at all.  nv_sdpa() takes its scratch (split-KV partials,
+// the bit-packed boolean mask) with cudaMallocAsync; this entry point takes it from the
+// fixed array below instead and allocates nothing.
+//
+// The array is a file-scope device variable: every GPU that loads this library holds
+// NV_SDPA_STATIC_SCRATCH_BYTES of it until the process exits.  In host code its name
+// is only a host-side stand-in, so its device address is looked up once per device
+// (cudaGetSymbolAddress, with that device current) by the first call on that device,
+// and that address is what the kernels receive.
+static __device__ __align__(256) unsigned char g_nv_sdpa_static_scratch[NV_SDPA_STATIC_SCRATCH_BYTES];
+
+namespace nvsdpa {
+namespace {
+std::atomic<void*> g_static_scratch_ptr[kMaxDevices];
+
+// Device address of the static scratch on the current device (set up on first use).
+void* static_scratch_for_current_device(cudaError_t* err) {
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    if (*err == cudaSuccess) *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  void* ptr = g_static_scratch_ptr[dev].load();
+  if (!ptr) {
+    *err = cudaGetSymbolAddress(&ptr, g_nv_sdpa_static_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    g_static_scratch_ptr[dev].store(ptr);
+  }
+  return ptr;
+}
+}  // namespace
+}  // namespace nvsdpa
+
+NV_SDPA_API int nv_sdpa_noalloc(const void* q, const void* k, const void* v, const nv_sdpa_dims* dims,
+                                int mask_kind, const uint8_t* bool_mask, const void* sinks, float scale,
+                                void* out, float* lse, int dtype, void* stream) {
+  int st = check_dims(dims, mask_kind, dtype);
+  if (st != NV_SDPA_OK) return st;
+  if (!std::isfinite(scale)) return NV_SDPA_ERR_INVALID;
+  const nv_sdpa_dims& x = *dims;
+  nv_sdpa_plan_t pl;
+  st = make_plan(x, mask_kind, sinks != nullptr, dtype, &pl);
+  if (st != NV_SDPA_OK) return st;
+  if (pl.path == NV_SDPA_PATH_NOOP) return NV_SDPA_OK;
+  if (pl.scratch_bytes > (int64_t)NV_SDPA_STATIC_SCRATCH_BYTES) return NV_SDPA_ERR_UNSUPPORTED;
+  const int64_t e = elt_bytes(dtype);
+  if (!out || !aligned(out, 16)) return NV_SDPA_ERR_INVALID;
+  if (lse && !aligned(lse, 4)) return NV_SDPA_ERR_INVALID;
+  if (sinks && !aligned(sinks, (uintptr_t)e)) return NV_SDPA_ERR_INVALID;
+  if (pl.path != NV_SDPA_PATH_NO_KEYS) {
+    if (!q || !k || !v || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16)) return NV_SDPA_ERR_INVALID;
+    if (mask_kind == NV_SDPA_MASK_BOOL && !bool_mask) return NV_SDPA_ERR_INVALID;
+  }
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t ce;
+  Params p{};
+  p.q = q; p.k = k; p.v = v;
+  p.mask = mask_kind == NV_SDPA_MASK_BOOL ? bool_mask : nullptr;
+  p.sinks = sinks; p.out = out; p.lse = lse;
+  p.status = status_ptr_for_current_device(&ce);
+  if (!p.status) return NV_SDPA_ERR_CUDA;
+  void* scratch = nullptr;
+  if (pl.scratch_bytes) {
+    scratch = static_scratch_for_current_device(&ce);
+    if (!scratch) return NV_SDPA_ERR_CUDA;
+  }
+  p.B = x.B; p.Hq = x.Hq; p.Hkv = x.Hkv; p.Lq = x.Lq; p.Lk = x.Lk; p.d = x.d; p.dv = x.dv;
+  p.g = x.Hq / x.Hkv; p.G = p.g * x.Lq;
+  p.nblk = pl.nblk; p.keys_per_blk = pl.keys_per_blk;
+  p.row_tiles = pl.rows_per_cta ? (p.G + pl.rows_per_cta - 1) / pl.rows_per_cta : 1;
+  p.mask_kind = mask_kind;
+  p.has_sinks = sinks != nullptr;
+  p.scale = scale;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  const uint64_t wl = g_wait_limit.load();
+  p.wait_limit = wl ? wl : kDefaultWaitLimit;
+  if (pl.path == NV_SDPA_PATH_NO_KEYS) {
+    ce = launch_fill_no_keys(dtype, p, cs);
+    return ce == cudaSuccess ? NV_SDPA_OK : NV_SDPA_ERR_CUDA;
+  }
+  if (scratch) {
+    // every partial (and mask word) the merge pass reads is written by this call's first
+    // kernel, so the array's previous contents never need clearing
+    const int64_t rows = x.B * x.Hq * x.Lq;
+    const int64_t o_bytes = (rows * pl.nblk * x.dv * 4 + 255) / 256 * 256;
+    p.part_o = static_cast<float*>(scratch);
+    p.part_ml = reinterpret_cast<float*>(static_cast<char*>(scratch) + o_bytes);
+  }
+  if (pl.kernel == NV_SDPA_KERNEL_PREFILL_TC) {
+    ce = launch_prefill_tc(dtype, p, static_cast<uint32_t*>(scratch), cs);
+  } else if (pl.kernel == NV_SDPA_KERNEL_DECODE_MMA) {
+    ce = launch_decode_mma(dtype, p, cs);
+    if (ce == cudaSuccess && pl.nblk > 1) ce = launch_merge(dtype, p, cs);
+  } else {
+    ce = launch_tiled_simt(dtype, p, cs);
+    if (ce == cudaSuccess && pl.nblk > 1) ce = launch_merge(dtype, p, cs);
+  }
+  return ce == cudaSuccess ? NV_SDPA_OK : NV_SDPA_ERR_CUDA;
+}
