@@ -113,6 +113,62 @@ class ClockSampler:
                 "samples": len(rows), "power_w_max": max(pw) if pw else None}
 
 
+class NvmlSampler:
+    """Polls the SM clock, clock-event reasons and power through NVML (read-only) every
+    ~2 ms on a thread, so that even a timed region of a few tens of ms has samples."""
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid: str):
+        import ctypes
+        self.samples, self.marks, self.stop_flag = [], [], False
+        L = ctypes.CDLL("libnvidia-ml.so.1")
+        if L.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if L.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle for " + uuid)
+        self.L, self.ct = L, ctypes
+        mx = ctypes.c_uint()
+        L.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+        self.max_mhz = mx.value
+        self.t = threading.Thread(target=self._poll, daemon=True)
+        self.t.start()
+
+    def _poll(self):
+        ct, L = self.ct, self.L
+        c, r, pw = ct.c_uint(), ct.c_ulonglong(), ct.c_uint()
+        while not self.stop_flag:
+            L.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(c))
+            L.nvmlDeviceGetCurrentClocksEventReasons(self.h, ct.byref(r))
+            L.nvmlDeviceGetPowerUsage(self.h, ct.byref(pw))
+            self.samples.append((time.time(), c.value, r.value, pw.value / 1000.0))
+            time.sleep(0.002)
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        self.stop_flag = True
+        self.t.join(timeout=1)
+        t0, t1 = (self.marks[0], self.marks[-1]) if len(self.marks) >= 2 else (0, 1e30)
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no samples"], "samples": 0}
+        reasons = sorted({name for s in inside for bit, name in self.REASONS.items() if s[2] & bit})
+        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(inside),
+                "power_w_max": round(max(s[3] for s in inside), 1), "source": "nvml"}
+
+
+def clock_sampler(torch, dev):
+    uuid = gpu_id_for_smi(torch, dev)
+    try:
+        return NvmlSampler(uuid)
+    except Exception:
+        return ClockSampler(uuid)
+
+
 def gpu_id_for_smi(torch, dev):
     try:
         u = str(torch.cuda.get_device_properties(dev).uuid)
@@ -288,7 +344,7 @@ def run_ours(args):
                                  W.MASK_CODES[pc.mask], 0, W.DTYPE_CODES[pc.dtype])
     pcall = caller(pc)
     gpu_name = torch.cuda.get_device_name(dev)
-    sampler = ClockSampler(gpu_id_for_smi(torch, local))
+    sampler = clock_sampler(torch, local)
     # untimed warm-up that also lets the clocks settle before the timed region
     for w in range(args.warmup):
         pcall(psets[w % len(psets)])

@@ -252,25 +252,40 @@ __global__ void __launch_bounds__(kTcThreads, 1) sdpa_prefill_tc(const __grid_co
         break;
       }
       tc_fence_after();
-      // scores of this row: raw dot products from TMEM, then scaled (log2 units) and masked
-      uint32_t sr_flat[BN];
-      if constexpr (BN == 128) tmem_ld128_sync(tmem + lane_base + buf * BN, sr_flat);
-      else tmem_ld64_sync(tmem + lane_base + buf * BN, sr_flat);
-      uint32_t (&sr)[BN / 32][32] = *reinterpret_cast<uint32_t (*)[BN / 32][32]>(sr_flat);
+      // scores of this row: raw dot products from TMEM
+      uint32_t sr[BN];
+      if constexpr (BN == 128) tmem_ld128_sync(tmem + lane_base + buf * BN, sr);
+      else tmem_ld64_sync(tmem + lane_base + buf * BN, sr);
       const int64_t j0 = (int64_t)t * BN;
-      float mt = -INFINITY;
+      // columns [0, vis_cols) pass the causal / key-count bound for this row
+      int64_t vc = last_key - j0 + 1;
+      const int vis_cols = vc < 0 ? 0 : (vc > BN ? BN : (int)vc);
+      const bool masked = !row_ok || mrow != nullptr || vis_cols < BN;
+      // warp-uniform fast path: nothing masked in the tile and scale >= 0, so the row
+      // maximum of the raw scores gives the scaled maximum and 2^(s*c - m) is one FFMA
+      const bool fast = !__any_sync(0xffffffffu, masked) && p.scale_log2 >= 0.f;
+      float mt;
+      if (fast) {
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t bits = 0xffffffffu;
-        if (mrow) bits = row_ok ? __ldg(mrow + j0 / 32 + c) : 0u;
+        for (int e = 0; e < BN; ++e) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(sr[e]));
+        mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
+      } else {
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int64_t j = j0 + c * 32 + e;
-          const bool vis = row_ok && j <= last_key && ((bits >> e) & 1u);
-          const float x = vis ? __uint_as_float(sr[c][e]) * p.scale_log2 : -INFINITY;
-          sr[c][e] = __float_as_uint(x);
-          mt = fmaxf(mt, x);
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t bits = 0xffffffffu;
+          if (mrow) bits = row_ok ? __ldg(mrow + j0 / 32 + c) : 0u;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int col = c * 32 + e;
+            const bool vis = row_ok && col < vis_cols && ((bits >> e) & 1u);
+            const float x = vis ? __uint_as_float(sr[col]) * p.scale_log2 : -INFINITY;
+            sr[col] = __float_as_uint(x);
+            m4[e & 3] = fmaxf(m4[e & 3], x);
+          }
         }
+        mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       }
       const float m_new = fmaxf(m_run, mt);
       const bool need = m_new > m_run + kRescaleLog2;
@@ -281,40 +296,46 @@ __global__ void __launch_bounds__(kTcThreads, 1) sdpa_prefill_tc(const __grid_co
       }
       // P = 2^(s - m) as 16-bit pairs into the TMEM columns of S (its A operand of P V)
       const bool none = (m_run == -INFINITY);
-      float tsum = 0.f;
+      const float neg_m = -m_run;
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c2 = 0; c2 < BN / 64; ++c2) {
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int idx = c2 * 64 + 2 * e;
-          const float p0 = none ? 0.f : ex2(__uint_as_float(sr[idx / 32][idx % 32]) - m_run);
-          const float p1 = none ? 0.f : ex2(__uint_as_float(sr[(idx + 1) / 32][(idx + 1) % 32]) - m_run);
-          tsum += p0 + p1;
+          float p0, p1;
+          if (fast) {
+            p0 = ex2(fmaf(__uint_as_float(sr[idx]), p.scale_log2, neg_m));
+            p1 = ex2(fmaf(__uint_as_float(sr[idx + 1]), p.scale_log2, neg_m));
+          } else {
+            p0 = none ? 0.f : ex2(__uint_as_float(sr[idx]) + neg_m);
+            p1 = none ? 0.f : ex2(__uint_as_float(sr[idx + 1]) + neg_m);
+          }
+          s4[e & 3] += p0 + p1;
           pk[e] = pack2<T>(p0, p1);
         }
         tmem_st32(tmem + lane_base + buf * BN + c2 * 32, pk);
       }
-      l_run = l_run * alpha + tsum;
+      l_run = l_run * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
       tmem_st_wait();
-      if (t > 0) {
-        // O must hold P_{t-1} V_{t-1} before it is rescaled for this tile's max
+      if (t > 0 && __any_sync(0xffffffffu, need)) {
+        // O must hold P_{t-1} V_{t-1} before it is rescaled for this tile's max (the
+        // newest phase pv_done can have completed here is t-1: P_t is not released yet)
         ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarPvDone), (t - 1) & 1, limit, abort));
         if (!ok) {
           fail(p, abort, kStatTimeoutMma);
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, need)) {
-          for (int c = 0; c < (a.n_pv + 31) / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32_sync(tmem + lane_base + 2 * BN + c * 32, o);
+        for (int c = 0; c < (a.n_pv + 31) / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32_sync(tmem + lane_base + 2 * BN + c * 32, o);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(tmem + lane_base + 2 * BN + c * 32, o);
-          }
-          tmem_st_wait();
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(tmem + lane_base + 2 * BN + c * 32, o);
         }
+        tmem_st_wait();
       }
       tc_fence_before();
       mbar_arrive(bar(kBarPFull + buf));

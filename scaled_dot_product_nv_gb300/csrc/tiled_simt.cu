@@ -196,53 +196,70 @@ sdpa_tiled_simt(const Params p) {
   }
 }
 
-// Pass 2 of split-KV: one warp per query row merges its nblk partials,
+// Pass 2 of split-KV: one CTA (4 warps) per query row merges its nblk partials,
 //   M = max(max_blk m_blk, sink),  L = sum_blk l_blk 2^(m_blk - M) + 2^(sink - M),
 //   out = sum_blk o_blk 2^(m_blk - M) / L,  lse = (M + log2 L) ln 2.
+// The blocks are split over the warps (warp w takes blocks w, w+4, ...) and each lane
+// reads 4 columns at a time, so a row's partials are read with many loads in flight.
 constexpr int kMergeWarps = 4;
 constexpr int kMaxBlk = 1024;
 
 template <typename T>
 __global__ void __launch_bounds__(kMergeWarps * 32)
 sdpa_merge_partials(const Params p) {
-  __shared__ float w_s[kMergeWarps][kMaxBlk];
+  __shared__ float red[kMergeWarps];
+  __shared__ float part[kMergeWarps][256 + 1];  // per-warp partial sums of one row, + L
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t rows = p.B * p.Hq * p.Lq;
-  const int64_t row = (int64_t)blockIdx.x * kMergeWarps + warp;
-  if (row >= rows) return;
+  const int64_t row = blockIdx.x;
   const int64_t h = (row / p.Lq) % p.Hq;
   const int nb = (int)p.nblk;
+  const int dv = (int)p.dv;
   const float* ml = p.part_ml + row * p.nblk * 2;
   const float sk = sink_log2<T>(p, h);
+  // M over every block's max (and the sink)
   float M = sk;
-  for (int k = lane; k < nb; k += 32) M = fmaxf(M, ml[2 * k]);
+  for (int k = threadIdx.x; k < nb; k += kMergeWarps * 32) M = fmaxf(M, ml[2 * k]);
 #pragma unroll
   for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  if (lane == 0) red[warp] = M;
+  __syncthreads();
+  M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
   T* orow = reinterpret_cast<T*>(p.out) + row * p.dv;
   if (M == -INFINITY) {
-    for (int c = lane; c < p.dv; c += 32) orow[c] = from_f32<T>(0.f);
-    if (lane == 0 && p.lse) p.lse[row] = -INFINITY;
+    for (int c = threadIdx.x; c < dv; c += kMergeWarps * 32) orow[c] = from_f32<T>(0.f);
+    if (threadIdx.x == 0 && p.lse) p.lse[row] = -INFINITY;
     return;
   }
-  float L = 0.f;
-  for (int k = lane; k < nb; k += 32) {
-    const float mk = ml[2 * k];
-    const float w = (mk == -INFINITY) ? 0.f : ex2(mk - M);
-    w_s[warp][k] = w;
-    L += ml[2 * k + 1] * w;
-  }
-#pragma unroll
-  for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-  L += ex2(sk - M);
-  __syncwarp();
-  const float inv = 1.f / L;
+  // this warp's blocks: weighted sums of o (4 columns per lane per pass) and of l
   const float* po = p.part_o + row * p.nblk * p.dv;
-  for (int c = lane; c < p.dv; c += 32) {
-    float acc = 0.f;
-    for (int k = 0; k < nb; ++k) acc = fmaf(po[(int64_t)k * p.dv + c], w_s[warp][k], acc);
-    orow[c] = from_f32<T>(acc * inv);
+  float L = 0.f;
+  for (int c0 = lane * 4; c0 < dv; c0 += 128) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int k = warp; k < nb; k += kMergeWarps) {
+      const float mk = ml[2 * k];
+      const float w = (mk == -INFINITY) ? 0.f : ex2(mk - M);
+      const float4 o = *reinterpret_cast<const float4*>(po + (int64_t)k * p.dv + c0);
+      acc.x = fmaf(o.x, w, acc.x);
+      acc.y = fmaf(o.y, w, acc.y);
+      acc.z = fmaf(o.z, w, acc.z);
+      acc.w = fmaf(o.w, w, acc.w);
+      if (c0 == lane * 4) L = fmaf(ml[2 * k + 1], w, L);
+    }
+    part[warp][c0] = acc.x;
+    part[warp][c0 + 1] = acc.y;
+    part[warp][c0 + 2] = acc.z;
+    part[warp][c0 + 3] = acc.w;
   }
-  if (lane == 0 && p.lse) p.lse[row] = (M + log2f(L)) * kLn2;
+  if (lane == 0) part[warp][256] = L;
+  __syncthreads();
+  const float Lt = (part[0][256] + part[1][256]) + (part[2][256] + part[3][256]) + ex2(sk - M);
+  const float inv = 1.f / Lt;
+  for (int c = threadIdx.x; c < dv; c += kMergeWarps * 32) {
+    const float s = (part[0][c] + part[1][c]) + (part[2][c] + part[3][c]);
+    orow[c] = from_f32<T>(s * inv);
+  }
+  if (threadIdx.x == 0 && p.lse) p.lse[row] = (M + log2f(Lt)) * kLn2;
 }
 
 // Lk == 0: every row sees no key.  out = 0; lse = the sink, or -inf without sinks.
@@ -282,8 +299,7 @@ cudaError_t launch_simt_t(const Params& p, cudaStream_t st) {
 template <typename T>
 cudaError_t launch_merge_t(const Params& p, cudaStream_t st) {
   const int64_t rows = p.B * p.Hq * p.Lq;
-  const int64_t grid = (rows + kMergeWarps - 1) / kMergeWarps;
-  sdpa_merge_partials<T><<<(unsigned)grid, kMergeWarps * 32, 0, st>>>(p);
+  sdpa_merge_partials<T><<<(unsigned)rows, kMergeWarps * 32, 0, st>>>(p);
   return cudaGetLastError();
 }
 
