@@ -82,9 +82,9 @@ int make_plan(const nv_sdpa_dims& x, int mask_kind, int has_sinks, int dtype, nv
   }
   pl->path = x.Lq > 8 ? NV_SDPA_PATH_PREFILL : NV_SDPA_PATH_DECODE;
   if (pl->path == NV_SDPA_PATH_PREFILL && prefill_tc_supported(dtype, x.d, x.dv)) {
-    // tcgen05 kernel: one CTA per 128 rows of one KV head, all keys (no split)
+    // tcgen05 kernel: one CTA per 128 or 256 rows of one KV head, all keys (no split)
     pl->kernel = NV_SDPA_KERNEL_PREFILL_TC;
-    pl->rows_per_cta = prefill_tc_rows_per_cta();
+    pl->rows_per_cta = prefill_tc_rows_per_cta(x.d, x.dv, G);
     pl->keys_per_blk = x.Lk;
     int64_t grid;
     if (!mul_ok(x.B * x.Hkv, cdiv(G, pl->rows_per_cta), &grid) || grid > 0x7fffffff)

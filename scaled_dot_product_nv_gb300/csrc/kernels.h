@@ -22,8 +22,9 @@ cudaError_t launch_fill_no_keys(int dtype, const Params& p, cudaStream_t st);
 // prefill_tc.cu
 bool prefill_tc_supported(int dtype, int64_t d, int64_t dv);
 int prefill_tc_bn(int64_t d, int64_t dv);
-size_t prefill_tc_smem_bytes(int64_t d, int64_t dv, int bn);
-int64_t prefill_tc_rows_per_cta();
+int prefill_tc_q_tiles(int64_t d, int64_t dv, int64_t G);
+size_t prefill_tc_smem_bytes(int64_t d, int64_t dv, int bn, int nq);
+int64_t prefill_tc_rows_per_cta(int64_t d, int64_t dv, int64_t G);
 size_t prefill_tc_mask_words(int64_t Lk);
 cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, cudaStream_t st);
 

@@ -6,22 +6,28 @@
 // end; masked keys at minus infinity and all-masked rows giving zeros.  The blocking,
 // the memory movement and the exponent bookkeeping are this kernel's own:
 //
-// * One CTA owns 128 query rows of one KV head (rows of the g query heads sharing it,
-//   head-major -- contiguous in memory) and walks the key tiles of BN keys.
-// * Warp 0 (one lane) streams Q once and K/V tiles through a 2-stage ring with TMA
-//   (128-byte swizzle), completion on mbarriers.
-// * Warp 1 allocates 512 TMEM columns; one lane issues tcgen05.mma:
-//     S_t = Q K_t^T      (A, B from shared memory, f32 accumulator in TMEM, 2 buffers)
-//     O  += P_t V_t      (A = P from TMEM, B = V from shared memory, MN-major)
+// * One CTA owns NQ x 128 query rows of one KV head (rows of the g query heads sharing
+//   it, head-major -- contiguous in memory) and walks their visible key tiles of BN keys.
+// * Warp 0 (one lane) streams the Q tile(s) once and K/V tiles through a 2-stage ring
+//   with 3-D TMA (128-byte swizzle, zero fill out of range); completion on mbarriers.
+// * Warp 1 allocates the 512 TMEM columns; one lane issues every tcgen05.mma:
+//     S = Q K_t^T      (A, B from shared memory, f32 accumulator in TMEM)
+//     O += P V_t       (A = P from TMEM, B = V from shared memory, MN-major)
 //   and signals completions with tcgen05.commit.
-// * Warps 2-5 (one query row per thread = one TMEM lane): read S_t, mask, keep the
-//   running max in log2 units, write P_t = 2^(s - m) as 16-bit values back into the
-//   TMEM columns of S_t, and rescale O only when the max grew by more than 2^8
-//   (otherwise the stale max is kept: exact after the final division, and every
-//   weight stays <= 2^8).  The epilogue folds in the sink logit, divides once, rounds
-//   once to the output type and writes the log-sum-exp.
-// * Causal: key tiles wholly above the (bottom-right aligned) diagonal are skipped.
-//   Boolean masks arrive as a bit-packed copy made by sdpa_pack_mask_bits.
+// * NQ softmax warpgroups (4 warps, one query row per thread = one TMEM lane) read S,
+//   mask it, keep the running max in log2 units, write P = 2^(s - m) as 16-bit pairs
+//   over the TMEM columns of S, and rescale O only when the max grew by more than 2^8
+//   (otherwise the stale max stays: exact after the final division, weights <= 2^8).
+//   The epilogue folds in the sink logit, divides once, rounds once to the output type
+//   and writes the log-sum-exp.
+//   - NQ = 1 (any head up to 256): S is double-buffered, so S_{t+1} is computed while
+//     the warpgroup works on S_t.
+//   - NQ = 2 (d, dv <= 128): two Q tiles share each K/V tile; the MMA issue order
+//     S0 S1 | P0V, S0' | P1V, S1' | ... lets one warpgroup's softmax run while the
+//     tensor pipe works for the other (ping-pong), with two warps per scheduler.
+// * Causal: key tiles wholly above the (bottom-right aligned) diagonal are never loaded,
+//   and a warp takes the unmasked fast path on every tile it sees completely.  Boolean
+//   masks arrive as a bit-packed copy made by sdpa_pack_mask_bits.
 // * Every mbarrier wait is bounded; a wait that runs out records a status bit, raises
 //   a shared abort flag that the other roles also watch, and the CTA drains its
 //   in-flight copies and MMAs before freeing TMEM and exiting.
@@ -37,7 +43,6 @@ namespace {
 using namespace sm100;
 
 constexpr int kBM = 128;
-constexpr int kTcThreads = 192;
 constexpr int kStages = 2;
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
@@ -49,17 +54,18 @@ struct TcArgs {
   Params p;
   const uint32_t* mask_bits;  // [Lq][mask_words], bit j%32 of word j/32 = key j visible
   int64_t mask_words;
-  int n_rt;          // row tiles per (b, kv head)
+  int n_rt;          // CTA row blocks (NQ x 128 rows) per (b, kv head)
   int dpanels;       // 64-element panels of d
   int dvpanels;      // 64-element panels of dv
   int ksteps_qk;     // ceil(d / 16)
   int n_pv;          // dv rounded up to 16 (MMA N of P V)
-  int itile_order;   // Lq % 128 == 0: launch the late (heavier, causal) row tiles first
+  int itile_order;   // Lq % (NQ x 128) == 0: launch the late (heavier, causal) blocks first
 };
 
+// barrier slots
 enum { kBarQ = 0, kBarKvFull = 1, kBarKvEmpty = 1 + kStages, kBarSFull = 1 + 2 * kStages,
-       kBarPFull = 3 + 2 * kStages, kBarPvDone = 5 + 2 * kStages, kBarDrain = 6 + 2 * kStages,
-       kNumBars = 7 + 2 * kStages };
+       kBarPFull = 3 + 2 * kStages, kBarPvDone = 5 + 2 * kStages, kBarDrain = 7 + 2 * kStages,
+       kNumBars = 8 + 2 * kStages };
 
 __device__ __forceinline__ void fail(const Params& p, volatile int* abort, uint32_t bit) {
   *abort = 1;
@@ -77,48 +83,200 @@ template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, f
   return pack_bf16(lo, hi);
 }
 
+// Last key row i may see (causal: bottom-right diagonal; otherwise the last key).
+__device__ __forceinline__ int64_t row_last_key(const Params& p, int64_t i) {
+  return p.mask_kind == kMaskCausal ? causal_last_key(p, i) : p.Lk - 1;
+}
+
+// Key tiles of BN keys that rows [r0, r0 + 128) of a KV head need (0 past the last row).
+template <int BN>
+__device__ __forceinline__ int tiles_for_rows(const Params& p, int64_t r0) {
+  if (r0 >= p.G) return 0;
+  int64_t kend = p.Lk;
+  if (p.mask_kind == kMaskCausal) {
+    const int64_t r1 = (r0 + kBM < p.G ? r0 + kBM : p.G) - 1;
+    const int64_t imax = (r0 / p.Lq == r1 / p.Lq) ? r1 % p.Lq : p.Lq - 1;
+    const int64_t lim = causal_last_key(p, imax) + 1;
+    if (lim < kend) kend = lim;
+  }
+  return kend > 0 ? (int)((kend + BN - 1) / BN) : 0;
+}
+
+// One query row's softmax step on key tile t.  tS / tO: TMEM addresses (lane base
+// included) of this tile's S columns and of O.  Returns false if a wait gave up.
 template <typename T, int BN>
-__global__ void __launch_bounds__(kTcThreads, 1) sdpa_prefill_tc(const __grid_constant__ TcArgs a) {
+__device__ __forceinline__ bool softmax_tile(const TcArgs& a, int t, uint32_t tS, uint32_t tO,
+                                             bool row_ok, int64_t last_key, const uint32_t* mrow,
+                                             float& m_run, float& l_run, uint32_t pv_bar,
+                                             uint64_t limit, volatile int* abort) {
+  const Params& p = a.p;
+  uint32_t sr[BN];
+  if constexpr (BN == 128) tmem_ld128_sync(tS, sr);
+  else tmem_ld64_sync(tS, sr);
+  const int64_t j0 = (int64_t)t * BN;
+  // columns [0, vis_cols) pass the causal / key-count bound for this row
+  const int64_t vc = last_key - j0 + 1;
+  const int vis_cols = vc < 0 ? 0 : (vc > BN ? BN : (int)vc);
+  const bool masked = !row_ok || mrow != nullptr || vis_cols < BN;
+  // warp-uniform fast path: nothing masked and scale >= 0, so the maximum of the raw
+  // scores gives the scaled maximum and 2^(s*c - m) is one FFMA and one MUFU op
+  const bool fast = !__any_sync(0xffffffffu, masked) && p.scale_log2 >= 0.f;
+  float mt;
+  if (fast) {
+    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int e = 0; e < BN; ++e) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(sr[e]));
+    mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
+  } else {
+    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t bits = 0xffffffffu;
+      if (mrow) bits = row_ok ? __ldg(mrow + j0 / 32 + c) : 0u;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int col = c * 32 + e;
+        const bool vis = row_ok && col < vis_cols && ((bits >> e) & 1u);
+        const float x = vis ? __uint_as_float(sr[col]) * p.scale_log2 : -INFINITY;
+        sr[col] = __float_as_uint(x);
+        m4[e & 3] = fmaxf(m4[e & 3], x);
+      }
+    }
+    mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+  }
+  const float m_new = fmaxf(m_run, mt);
+  const bool need = m_new > m_run + kRescaleLog2;
+  float alpha = 1.f;
+  if (need) {
+    alpha = ex2(m_run - m_new);
+    m_run = m_new;
+  }
+  // P = 2^(s - m) as 16-bit pairs over the TMEM columns of S (the A operand of P V)
+  const bool none = (m_run == -INFINITY);
+  const float neg_m = -m_run;
+  float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int c2 = 0; c2 < BN / 64; ++c2) {
+    uint32_t pk[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int idx = c2 * 64 + 2 * e;
+      float p0, p1;
+      if (fast) {
+        p0 = ex2(fmaf(__uint_as_float(sr[idx]), p.scale_log2, neg_m));
+        p1 = ex2(fmaf(__uint_as_float(sr[idx + 1]), p.scale_log2, neg_m));
+      } else {
+        p0 = none ? 0.f : ex2(__uint_as_float(sr[idx]) + neg_m);
+        p1 = none ? 0.f : ex2(__uint_as_float(sr[idx + 1]) + neg_m);
+      }
+      s4[e & 3] += p0 + p1;
+      pk[e] = pack2<T>(p0, p1);
+    }
+    tmem_st32(tS + c2 * 32, pk);
+  }
+  l_run = l_run * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+  tmem_st_wait();
+  if (t > 0 && __any_sync(0xffffffffu, need)) {
+    // O must hold P_{t-1} V_{t-1} before it is rescaled (the newest phase pv_done can
+    // have completed here is t-1: P_t is not released yet)
+    if (!__all_sync(0xffffffffu, mbar_wait(pv_bar, (t - 1) & 1, limit, abort))) return false;
+    tc_fence_after();
+    for (int c = 0; c < (a.n_pv + 31) / 32; ++c) {
+      uint32_t o[32];
+      tmem_ld32_sync(tO + c * 32, o);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+      tmem_st32(tO + c * 32, o);
+    }
+    tmem_st_wait();
+  }
+  return true;
+}
+
+// Final output of one query row: sink folded in, one division, one rounding; lse.
+template <typename T>
+__device__ __forceinline__ void epilogue_row(const Params& p, uint32_t tO, bool have_o, bool row_ok,
+                                             int64_t out_row, int64_t h, float m_run, float l_run) {
+  const float sk = sink_log2<T>(p, h);
+  const float M = fmaxf(m_run, sk);
+  float f = 0.f, L = 0.f;
+  if (M != -INFINITY) {
+    const float am = ex2(m_run - M);
+    L = l_run * am + ex2(sk - M);
+    f = am / L;
+  }
+  T* orow = reinterpret_cast<T*>(p.out) + out_row * p.dv;
+  const int dv = (int)p.dv;
+  for (int c = 0; c < (dv + 31) / 32; ++c) {
+    uint32_t o[32];
+    if (have_o) {
+      tmem_ld32_sync(tO + c * 32, o);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) o[e] = 0u;
+    }
+    if (row_ok) {
+#pragma unroll
+      for (int e8 = 0; e8 < 4; ++e8) {
+        const int col = c * 32 + e8 * 8;
+        if (col < dv) {
+          uint4 v;
+          v.x = pack2<T>(__uint_as_float(o[e8 * 8 + 0]) * f, __uint_as_float(o[e8 * 8 + 1]) * f);
+          v.y = pack2<T>(__uint_as_float(o[e8 * 8 + 2]) * f, __uint_as_float(o[e8 * 8 + 3]) * f);
+          v.z = pack2<T>(__uint_as_float(o[e8 * 8 + 4]) * f, __uint_as_float(o[e8 * 8 + 5]) * f);
+          v.w = pack2<T>(__uint_as_float(o[e8 * 8 + 6]) * f, __uint_as_float(o[e8 * 8 + 7]) * f);
+          *reinterpret_cast<uint4*>(orow + col) = v;
+        }
+      }
+    }
+  }
+  if (row_ok && p.lse) p.lse[out_row] = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
+}
+
+template <int NQ>
+constexpr int tc_threads() { return (2 + 4 * NQ) * 32; }
+
+template <typename T, int BN, int NQ>
+__global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __grid_constant__ TcArgs a) {
+  static_assert(NQ == 1 || NQ == 2, "one or two Q tiles per CTA");
+  static_assert(NQ == 1 || BN == 128, "the two-tile variant uses 128-key tiles");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const Params& p = a.p;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const uint32_t q_bytes = a.dpanels * kBM * 128;
+  const uint32_t q_bytes = a.dpanels * kBM * 128;  // one Q tile
   const uint32_t k_bytes = a.dpanels * BN * 128;
   const uint32_t v_bytes = a.dvpanels * BN * 128;
   const uint32_t sQ = smem_addr(base);
-  const uint32_t sK = sQ + q_bytes;
+  const uint32_t sK = sQ + NQ * q_bytes;
   const uint32_t sV = sK + kStages * k_bytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + q_bytes + kStages * (k_bytes + v_bytes));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + NQ * q_bytes + kStages * (k_bytes + v_bytes));
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_holder + 1);
   auto bar = [&](int i) { return smem_addr(bars + i); };
 
   // ---- which rows and keys this CTA owns
   const int64_t BH = p.B * p.Hkv;
-  int64_t rt, bh;
+  int64_t rb, bh;  // row block (NQ x 128 rows) and (b, kv head)
   if (a.itile_order) {
-    const int64_t ipt = p.Lq / kBM;  // row tiles per head
+    const int64_t ipt = p.Lq / (kBM * NQ);  // row blocks per head
     int64_t x = blockIdx.x;
     const int64_t hh = x % p.g; x /= p.g;
     bh = x % BH;
     const int64_t it = ipt - 1 - x / BH;
-    rt = hh * ipt + it;
+    rb = hh * ipt + it;
   } else {
-    rt = blockIdx.x % a.n_rt;
+    rb = blockIdx.x % a.n_rt;
     bh = blockIdx.x / a.n_rt;
   }
   const int64_t hkv = bh % p.Hkv;
-  int64_t kend = p.Lk;
-  if (p.mask_kind == kMaskCausal) {
-    const int64_t r0 = rt * kBM;
-    const int64_t r1 = (r0 + kBM < p.G ? r0 + kBM : p.G) - 1;
-    const int64_t imax = (r0 / p.Lq == r1 / p.Lq) ? r1 % p.Lq : p.Lq - 1;
-    const int64_t lim = causal_last_key(p, imax) + 1;
-    if (lim < kend) kend = lim;
-  }
-  const int n_tiles = kend > 0 ? (int)((kend + BN - 1) / BN) : 0;
+  int n_q[NQ];
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) n_q[q] = tiles_for_rows<BN>(p, (rb * NQ + q) * kBM);
+  int n_max = 0;
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) n_max = n_q[q] > n_max ? n_q[q] : n_max;
 
   // ---- set-up: barriers, TMEM
   if (threadIdx.x == 0) {
@@ -130,8 +288,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) sdpa_prefill_tc(const __grid_co
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(kBarSFull + b), 1);
       mbar_init(bar(kBarPFull + b), 128);
+      mbar_init(bar(kBarPvDone + b), 1);
     }
-    mbar_init(bar(kBarPvDone), 1);
     mbar_init(bar(kBarDrain), 1);
     *abort = 0;
     fence_mbar_init();
@@ -145,18 +303,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) sdpa_prefill_tc(const __grid_co
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
   const uint64_t limit = p.wait_limit;
+  // TMEM columns: S slot b at b*BN (NQ = 1: the two buffers; NQ = 2: one per Q tile);
+  // O of Q tile q at 2*BN + q*128.
+  auto tS_col = [&](int slot) { return (uint32_t)(slot * BN); };
+  auto tO_col = [&](int q) { return (uint32_t)(2 * BN + q * 128); };
 
   if (warp == 0) {
     // ================================================================ TMA producer
-    if (lane == 0 && n_tiles > 0) {
+    if (lane == 0 && n_max > 0) {
       tma_prefetch_desc(&a.tmq);
       tma_prefetch_desc(&a.tmk);
       tma_prefetch_desc(&a.tmv);
-      mbar_arrive_expect_tx(bar(kBarQ), q_bytes);
-      for (int pn = 0; pn < a.dpanels; ++pn)
-        tma_load_3d(sQ + pn * kBM * 128, &a.tmq, bar(kBarQ), pn * 64, (int)(rt * kBM), (int)bh);
+      mbar_arrive_expect_tx(bar(kBarQ), NQ * q_bytes);
+      for (int q = 0; q < NQ; ++q)
+        for (int pn = 0; pn < a.dpanels; ++pn)
+          tma_load_3d(sQ + q * q_bytes + pn * kBM * 128, &a.tmq, bar(kBarQ), pn * 64,
+                      (int)((rb * NQ + q) * kBM), (int)bh);
       int issued = 0;
-      for (int t = 0; t < n_tiles; ++t) {
+      for (int t = 0; t < n_max; ++t) {
         const int s = t % kStages;
         if (!mbar_wait(bar(kBarKvEmpty + s), ((t / kStages) & 1) ^ 1, limit, abort)) {
           fail(p, abort, kStatTimeoutSlotFree);
@@ -177,54 +341,79 @@ __global__ void __launch_bounds__(kTcThreads, 1) sdpa_prefill_tc(const __grid_co
     __syncwarp();
   } else if (warp == 1) {
     // ================================================================ MMA issuer
-    if (lane == 0 && n_tiles > 0) {
+    if (lane == 0 && n_max > 0) {
       const uint32_t idesc_s = idesc_f16(TypeCode<T>::v, 0, 0, kBM, BN);
       const uint32_t idesc_o = idesc_f16(TypeCode<T>::v, 0, 1, kBM, a.n_pv);
-      const uint32_t tO = tmem + 2 * BN;
-      bool ok = mbar_wait(bar(kBarQ), 0, limit, abort);
-      if (!ok) fail(p, abort, kStatTimeoutTmaFull);
-      auto issue_s = [&](int t) {
+      // S = Q_q K_t^T into S slot `slot`, then commit to s_full[slot]
+      auto issue_s = [&](int t, int q, int slot) {
         const int s = t % kStages;
-        const uint32_t tS = tmem + (t & 1) * BN;
         for (int k = 0; k < a.ksteps_qk; ++k) {
           const uint32_t off = (uint32_t)(k & 3) * 32;  // 16 elements inside the 128-byte row
-          const uint64_t ad = smem_desc_sw128(sQ + (k >> 2) * kBM * 128 + off, 16, 1024);
+          const uint64_t ad = smem_desc_sw128(sQ + q * q_bytes + (k >> 2) * kBM * 128 + off, 16, 1024);
           const uint64_t bd = smem_desc_sw128(sK + s * k_bytes + (k >> 2) * BN * 128 + off, 16, 1024);
-          mma_ss(tS, ad, bd, idesc_s, k > 0);
+          mma_ss(tmem + tS_col(slot), ad, bd, idesc_s, k > 0);
         }
-        mma_commit(bar(kBarSFull + (t & 1)));
+        mma_commit(bar(kBarSFull + slot));
       };
-      if (ok) {
-        ok = mbar_wait(bar(kBarKvFull), 0, limit, abort);
-        if (!ok) fail(p, abort, kStatTimeoutTmaFull);
-      }
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-      }
-      for (int t = 0; ok && t < n_tiles; ++t) {
-        if (t + 1 < n_tiles) {
-          const int s1 = (t + 1) % kStages;
-          if (!mbar_wait(bar(kBarKvFull + s1), ((t + 1) / kStages) & 1, limit, abort)) {
-            fail(p, abort, kStatTimeoutTmaFull);
-            break;
-          }
-          tc_fence_after();
-          issue_s(t + 1);
-        }
-        if (!mbar_wait(bar(kBarPFull + (t & 1)), (t >> 1) & 1, limit, abort)) {
-          fail(p, abort, kStatTimeoutMma);
-          break;
-        }
-        tc_fence_after();
+      // O_q += P (from S slot `slot`) V_t, then commit to pv_done[q]
+      auto issue_pv = [&](int t, int q, int slot) {
         const int s = t % kStages;
-        const uint32_t tP = tmem + (t & 1) * BN;
         for (int kk = 0; kk < BN / 16; ++kk) {
           const uint64_t bd = smem_desc_sw128(sV + s * v_bytes + kk * 16 * 128, BN * 128, 1024);
-          mma_ts(tO, tP + kk * 8, bd, idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + tO_col(q), tmem + tS_col(slot) + kk * 8, bd, idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(bar(kBarKvEmpty + s));
-        mma_commit(bar(kBarPvDone));
+        mma_commit(bar(kBarPvDone + q));
+      };
+      auto wait_kv = [&](int t) {
+        if (mbar_wait(bar(kBarKvFull + t % kStages), (t / kStages) & 1, limit, abort)) {
+          tc_fence_after();
+          return true;
+        }
+        fail(p, abort, kStatTimeoutTmaFull);
+        return false;
+      };
+      auto wait_p = [&](int slot, uint32_t parity) {
+        if (mbar_wait(bar(kBarPFull + slot), parity, limit, abort)) {
+          tc_fence_after();
+          return true;
+        }
+        fail(p, abort, kStatTimeoutMma);
+        return false;
+      };
+      bool ok = mbar_wait(bar(kBarQ), 0, limit, abort);
+      if (!ok) fail(p, abort, kStatTimeoutTmaFull);
+      ok = ok && wait_kv(0);
+      if constexpr (NQ == 1) {
+        if (ok) issue_s(0, 0, 0);
+        for (int t = 0; ok && t < n_max; ++t) {
+          if (t + 1 < n_max) {
+            if (!(ok = wait_kv(t + 1))) break;
+            issue_s(t + 1, 0, (t + 1) & 1);
+          }
+          if (!(ok = wait_p(t & 1, (t >> 1) & 1))) break;
+          issue_pv(t, 0, t & 1);
+          mma_commit(bar(kBarKvEmpty + t % kStages));
+        }
+      } else {
+        if (ok) {
+          if (n_q[0] > 0) issue_s(0, 0, 0);
+          if (n_q[1] > 0) issue_s(0, 1, 1);
+        }
+        for (int t = 0; ok && t < n_max; ++t) {
+          const bool nxt = t + 1 < n_max;
+          if (t < n_q[0]) {
+            if (!(ok = wait_p(0, t & 1))) break;
+            issue_pv(t, 0, 0);
+          }
+          if (nxt && !(ok = wait_kv(t + 1))) break;
+          if (nxt && t + 1 < n_q[0]) issue_s(t + 1, 0, 0);
+          if (t < n_q[1]) {
+            if (!(ok = wait_p(1, t & 1))) break;
+            issue_pv(t, 1, 1);
+          }
+          mma_commit(bar(kBarKvEmpty + t % kStages));
+          if (nxt && t + 1 < n_q[1]) issue_s(t + 1, 1, 1);
+        }
       }
       // all MMAs issued by this thread complete before TMEM can be freed
       mma_commit(bar(kBarDrain));
@@ -233,156 +422,46 @@ __global__ void __launch_bounds__(kTcThreads, 1) sdpa_prefill_tc(const __grid_co
     __syncwarp();
   } else {
     // ================================================================ softmax / epilogue
-    const int q4 = warp & 3;
+    const int q = (warp - 2) / 4;  // which Q tile this warpgroup serves
+    const int q4 = warp & 3;       // TMEM lane quarter this warp may access
     const int row = q4 * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-    const int64_t rho = rt * kBM + row;
+    const int64_t rho = (rb * NQ + q) * kBM + row;
     const bool row_ok = rho < p.G;
     const int64_t i = row_ok ? rho % p.Lq : 0;
     const int64_t h = hkv * p.g + (row_ok ? rho / p.Lq : 0);
-    const int64_t last_key = (p.mask_kind == kMaskCausal) ? causal_last_key(p, i) : p.Lk - 1;
+    const int64_t last_key = row_last_key(p, i);
     const uint32_t* mrow = a.mask_bits ? a.mask_bits + i * a.mask_words : nullptr;
+    const int n_tiles = n_q[q];
+    const uint32_t tO = tmem + lane_base + tO_col(q);
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int t = 0; t < n_tiles; ++t) {
-      const int buf = t & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull + buf), (t >> 1) & 1, limit, abort));
+      const int slot = (NQ == 1) ? (t & 1) : q;
+      const uint32_t par = (NQ == 1) ? ((t >> 1) & 1) : (t & 1);
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull + slot), par, limit, abort));
       if (!ok) {
         fail(p, abort, kStatTimeoutMma);
         break;
       }
       tc_fence_after();
-      // scores of this row: raw dot products from TMEM
-      uint32_t sr[BN];
-      if constexpr (BN == 128) tmem_ld128_sync(tmem + lane_base + buf * BN, sr);
-      else tmem_ld64_sync(tmem + lane_base + buf * BN, sr);
-      const int64_t j0 = (int64_t)t * BN;
-      // columns [0, vis_cols) pass the causal / key-count bound for this row
-      int64_t vc = last_key - j0 + 1;
-      const int vis_cols = vc < 0 ? 0 : (vc > BN ? BN : (int)vc);
-      const bool masked = !row_ok || mrow != nullptr || vis_cols < BN;
-      // warp-uniform fast path: nothing masked in the tile and scale >= 0, so the row
-      // maximum of the raw scores gives the scaled maximum and 2^(s*c - m) is one FFMA
-      const bool fast = !__any_sync(0xffffffffu, masked) && p.scale_log2 >= 0.f;
-      float mt;
-      if (fast) {
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int e = 0; e < BN; ++e) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(sr[e]));
-        mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
-      } else {
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t bits = 0xffffffffu;
-          if (mrow) bits = row_ok ? __ldg(mrow + j0 / 32 + c) : 0u;
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int col = c * 32 + e;
-            const bool vis = row_ok && col < vis_cols && ((bits >> e) & 1u);
-            const float x = vis ? __uint_as_float(sr[col]) * p.scale_log2 : -INFINITY;
-            sr[col] = __float_as_uint(x);
-            m4[e & 3] = fmaxf(m4[e & 3], x);
-          }
-        }
-        mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-      }
-      const float m_new = fmaxf(m_run, mt);
-      const bool need = m_new > m_run + kRescaleLog2;
-      float alpha = 1.f;
-      if (need) {
-        alpha = ex2(m_run - m_new);
-        m_run = m_new;
-      }
-      // P = 2^(s - m) as 16-bit pairs into the TMEM columns of S (its A operand of P V)
-      const bool none = (m_run == -INFINITY);
-      const float neg_m = -m_run;
-      float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c2 = 0; c2 < BN / 64; ++c2) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int idx = c2 * 64 + 2 * e;
-          float p0, p1;
-          if (fast) {
-            p0 = ex2(fmaf(__uint_as_float(sr[idx]), p.scale_log2, neg_m));
-            p1 = ex2(fmaf(__uint_as_float(sr[idx + 1]), p.scale_log2, neg_m));
-          } else {
-            p0 = none ? 0.f : ex2(__uint_as_float(sr[idx]) + neg_m);
-            p1 = none ? 0.f : ex2(__uint_as_float(sr[idx + 1]) + neg_m);
-          }
-          s4[e & 3] += p0 + p1;
-          pk[e] = pack2<T>(p0, p1);
-        }
-        tmem_st32(tmem + lane_base + buf * BN + c2 * 32, pk);
-      }
-      l_run = l_run * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
-      tmem_st_wait();
-      if (t > 0 && __any_sync(0xffffffffu, need)) {
-        // O must hold P_{t-1} V_{t-1} before it is rescaled for this tile's max (the
-        // newest phase pv_done can have completed here is t-1: P_t is not released yet)
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarPvDone), (t - 1) & 1, limit, abort));
-        if (!ok) {
-          fail(p, abort, kStatTimeoutMma);
-          break;
-        }
-        tc_fence_after();
-        for (int c = 0; c < (a.n_pv + 31) / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32_sync(tmem + lane_base + 2 * BN + c * 32, o);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(tmem + lane_base + 2 * BN + c * 32, o);
-        }
-        tmem_st_wait();
+      ok = softmax_tile<T, BN>(a, t, tmem + lane_base + tS_col(slot), tO, row_ok, last_key, mrow, m_run,
+                               l_run, bar(kBarPvDone + q), limit, abort);
+      if (!ok) {
+        fail(p, abort, kStatTimeoutMma);
+        break;
       }
       tc_fence_before();
-      mbar_arrive(bar(kBarPFull + buf));
+      mbar_arrive(bar(kBarPFull + slot));
     }
     // ---- epilogue
     if (ok && n_tiles > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarPvDone), (n_tiles - 1) & 1, limit, abort));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarPvDone + q), (n_tiles - 1) & 1, limit, abort));
       if (!ok) fail(p, abort, kStatTimeoutMma);
       tc_fence_after();
     }
     ok = __all_sync(0xffffffffu, ok && !*abort);
-    if (ok) {
-      const float sk = sink_log2<T>(p, h);
-      const float M = fmaxf(m_run, sk);
-      float f = 0.f, L = 0.f;
-      if (M != -INFINITY) {
-        const float am = ex2(m_run - M);
-        L = l_run * am + ex2(sk - M);
-        f = am / L;
-      }
-      T* orow = reinterpret_cast<T*>(p.out) + (bh * p.G + rho) * p.dv;
-      const int dv = (int)p.dv;
-      for (int c = 0; c < (dv + 31) / 32; ++c) {
-        uint32_t o[32];
-        if (n_tiles > 0) {
-          tmem_ld32_sync(tmem + lane_base + 2 * BN + c * 32, o);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0u;
-        }
-        if (row_ok) {
-#pragma unroll
-          for (int e8 = 0; e8 < 4; ++e8) {
-            const int col = c * 32 + e8 * 8;
-            if (col < dv) {
-              uint4 v;
-              v.x = pack2<T>(__uint_as_float(o[e8 * 8 + 0]) * f, __uint_as_float(o[e8 * 8 + 1]) * f);
-              v.y = pack2<T>(__uint_as_float(o[e8 * 8 + 2]) * f, __uint_as_float(o[e8 * 8 + 3]) * f);
-              v.z = pack2<T>(__uint_as_float(o[e8 * 8 + 4]) * f, __uint_as_float(o[e8 * 8 + 5]) * f);
-              v.w = pack2<T>(__uint_as_float(o[e8 * 8 + 6]) * f, __uint_as_float(o[e8 * 8 + 7]) * f);
-              *reinterpret_cast<uint4*>(orow + col) = v;
-            }
-          }
-        }
-      }
-      if (row_ok && p.lse) p.lse[bh * p.G + rho] = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
-    }
+    if (ok) epilogue_row<T>(p, tO, n_tiles > 0, row_ok, bh * p.G + rho, h, m_run, l_run);
   }
 
   // ---- tear-down
@@ -449,43 +528,61 @@ bool encode_3d(CUtensorMap* m, int dtype, const void* ptr, int64_t inner, int64_
   return r == CUDA_SUCCESS;
 }
 
-template <typename T, int BN>
+template <typename T, int BN, int NQ>
 cudaError_t launch_tc_t(const TcArgs& a, size_t smem, int64_t grid, cudaStream_t st) {
   static unsigned long long configured = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64 || !(configured >> dev & 1ull)) {
-    e = cudaFuncSetAttribute(sdpa_prefill_tc<T, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(sdpa_prefill_tc<T, BN, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kTcMaxSmem);
     if (e != cudaSuccess) return e;
     if (dev < 64) configured |= 1ull << dev;
   }
-  sdpa_prefill_tc<T, BN><<<(unsigned)grid, kTcThreads, smem, st>>>(a);
+  sdpa_prefill_tc<T, BN, NQ><<<(unsigned)grid, tc_threads<NQ>(), smem, st>>>(a);
   return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_tc_cfg(int bn, int nq, const TcArgs& a, size_t smem, int64_t grid, cudaStream_t st) {
+  if (nq == 2) return launch_tc_t<T, 128, 2>(a, smem, grid, st);
+  return bn == 128 ? launch_tc_t<T, 128, 1>(a, smem, grid, st) : launch_tc_t<T, 64, 1>(a, smem, grid, st);
+}
+
+size_t smem_need(int64_t d, int64_t dv, int bn, int nq) {
+  const int64_t dp = (d + 63) / 64, dvp = (dv + 63) / 64;
+  return (size_t)(nq * dp * kBM * 128 + kStages * (dp + dvp) * bn * 128) + 1024 /*align*/ + 256 /*bars*/;
 }
 
 }  // namespace
 
 int prefill_tc_bn(int64_t d, int64_t dv) {
-  // largest key tile whose 2-stage K/V ring plus the Q tile fit in shared memory and
+  // largest key tile whose 2-stage K/V ring plus one Q tile fit in shared memory and
   // whose two S buffers plus O fit in the 512 TMEM columns
-  const int64_t dp = (d + 63) / 64, dvp = (dv + 63) / 64, npv = (dv + 15) / 16 * 16;
+  const int64_t npv = (dv + 15) / 16 * 16;
   for (int bn : {128, 64}) {
-    const int64_t smem = dp * kBM * 128 + kStages * (dp + dvp) * bn * 128 + 1024 + 256;
-    if (smem <= kTcMaxSmem && 2 * bn + npv <= kTmemCols) return bn;
+    if ((int64_t)smem_need(d, dv, bn, 1) <= kTcMaxSmem && 2 * bn + npv <= kTmemCols) return bn;
   }
   return 0;
 }
 
-size_t prefill_tc_smem_bytes(int64_t d, int64_t dv, int bn) {
-  const int64_t dp = (d + 63) / 64, dvp = (dv + 63) / 64;
-  size_t s = (size_t)(dp * kBM * 128 + kStages * (dp + dvp) * bn * 128) + 1024 /*align*/ + 256 /*bars*/;
+int prefill_tc_q_tiles(int64_t d, int64_t dv, int64_t G) {
+  // two Q tiles share each K/V tile when both O accumulators fit next to the two S
+  // tiles (dv <= 128), both Q tiles and the ring fit in shared memory, and there are
+  // more than 128 rows to fill them
+  if (dv <= 128 && prefill_tc_bn(d, dv) == 128 && (int64_t)smem_need(d, dv, 128, 2) <= kTcMaxSmem && G > kBM)
+    return 2;
+  return 1;
+}
+
+size_t prefill_tc_smem_bytes(int64_t d, int64_t dv, int bn, int nq) {
+  const size_t s = smem_need(d, dv, bn, nq);
   // at least 120 KB so that one CTA (with its 512 TMEM columns) owns the SM
   return s < 120 * 1024 ? 120 * 1024 : s;
 }
 
-int64_t prefill_tc_rows_per_cta() { return kBM; }
+int64_t prefill_tc_rows_per_cta(int64_t d, int64_t dv, int64_t G) { return kBM * prefill_tc_q_tiles(d, dv, G); }
 
 bool prefill_tc_supported(int dtype, int64_t d, int64_t dv) {
   return (dtype == 1 || dtype == 2) && d % 8 == 0 && dv % 8 == 0 && d <= 256 && dv <= 256 &&
@@ -503,16 +600,17 @@ cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, c
   a.p = p;
   const int bn = prefill_tc_bn(p.d, p.dv);
   if (!bn) return cudaErrorInvalidValue;
+  const int nq = prefill_tc_q_tiles(p.d, p.dv, p.G);
   const int64_t BH = p.B * p.Hkv;
   if (!encode_3d(&a.tmq, dtype, p.q, p.d, p.G, BH, kBM) || !encode_3d(&a.tmk, dtype, p.k, p.d, p.Lk, BH, bn) ||
       !encode_3d(&a.tmv, dtype, p.v, p.dv, p.Lk, BH, bn))
     return cudaErrorInvalidValue;
-  a.n_rt = (int)((p.G + kBM - 1) / kBM);
+  a.n_rt = (int)((p.G + kBM * nq - 1) / (kBM * nq));
   a.dpanels = (int)((p.d + 63) / 64);
   a.dvpanels = (int)((p.dv + 63) / 64);
   a.ksteps_qk = (int)((p.d + 15) / 16);
   a.n_pv = (int)((p.dv + 15) / 16 * 16);
-  a.itile_order = (p.Lq % kBM == 0) ? 1 : 0;
+  a.itile_order = (p.Lq % (kBM * nq) == 0) ? 1 : 0;
   if (p.mask_kind == kMaskBool) {
     a.mask_words = (int64_t)prefill_tc_mask_words(p.Lk);
     a.mask_bits = mask_bits;
@@ -524,10 +622,9 @@ cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, c
     if (e != cudaSuccess) return e;
   }
   const int64_t grid = BH * a.n_rt;
-  const size_t smem = prefill_tc_smem_bytes(p.d, p.dv, bn);
-  if (dtype == 1) return bn == 128 ? launch_tc_t<__half, 128>(a, smem, grid, st) : launch_tc_t<__half, 64>(a, smem, grid, st);
-  return bn == 128 ? launch_tc_t<__nv_bfloat16, 128>(a, smem, grid, st)
-                   : launch_tc_t<__nv_bfloat16, 64>(a, smem, grid, st);
+  const size_t smem = prefill_tc_smem_bytes(p.d, p.dv, bn, nq);
+  if (dtype == 1) return launch_tc_cfg<__half>(bn, nq, a, smem, grid, st);
+  return launch_tc_cfg<__nv_bfloat16>(bn, nq, a, smem, grid, st);
 }
 
 }  // namespace nvsdpa
