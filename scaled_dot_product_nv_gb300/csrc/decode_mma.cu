@@ -35,7 +35,7 @@ constexpr int kWarpsC = 4;       // compute warps
 constexpr int kDecThreads = (kWarpsC + 1) * 32;
 constexpr int kDecStages = 3;
 constexpr float kRescaleLog2Dec = 8.0f;
-constexpr uint64_t kDrainLimitDec = 1ull << 22;
+constexpr uint64_t kDrainLimitDec = 1ull << 18;  // polls of <= ~10 us each
 
 struct DecArgs {
   CUtensorMap tmk, tmv;

@@ -46,7 +46,7 @@ constexpr int kBM = 128;
 constexpr int kStages = 2;
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
-constexpr uint64_t kDrainLimit = 1ull << 22;
+constexpr uint64_t kDrainLimit = 1ull << 18;  // polls of <= ~10 us each
 constexpr int64_t kTcMaxSmem = 227 * 1024;  // opt-in dynamic shared memory per CTA
 
 struct TcArgs {
@@ -121,12 +121,46 @@ __device__ __forceinline__ bool softmax_tile(const TcArgs& a, int t, uint32_t tS
   // warp-uniform fast path: nothing masked and scale >= 0, so the maximum of the raw
   // scores gives the scaled maximum and 2^(s*c - m) is one FFMA and one MUFU op
   const bool fast = !__any_sync(0xffffffffu, masked) && p.scale_log2 >= 0.f;
-  float mt;
+  float alpha = 1.f;
+  bool need;
   if (fast) {
     float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-    for (int e = 0; e < BN; ++e) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(sr[e]));
-    mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
+    for (int e = 0; e < BN; e += 8) {
+      m4[0] = fmax3(m4[0], __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+      m4[1] = fmax3(m4[1], __uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3]));
+      m4[2] = fmax3(m4[2], __uint_as_float(sr[e + 4]), __uint_as_float(sr[e + 5]));
+      m4[3] = fmax3(m4[3], __uint_as_float(sr[e + 6]), __uint_as_float(sr[e + 7]));
+    }
+    const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
+    const float m_new = fmaxf(m_run, mt);
+    need = m_new > m_run + kRescaleLog2;
+    if (need) {
+      alpha = ex2(m_run - m_new);
+      m_run = m_new;
+    }
+    // P = 2^(s*c - m): one two-wide FFMA per pair of scores, the sum two-wide as well
+    const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2), nm2 = f2_pack(-m_run, -m_run);
+    uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+    for (int c2i = 0; c2i < BN / 64; ++c2i) {
+      uint32_t pk[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int idx = c2i * 64 + 2 * e;
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[idx]), __uint_as_float(sr[idx + 1])), c2, nm2), x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
+        pk[e] = pack2<T>(p0, p1);
+      }
+      tmem_st32(tS + c2i * 32, pk);
+    }
+    float a0, a1, b0, b1, c0, c1, d0, d1;
+    f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
+    f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
+    (void)c0; (void)c1; (void)d0; (void)d1;
+    l_run = l_run * alpha + ((a0 + a1) + (b0 + b1));
   } else {
     float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
@@ -142,45 +176,42 @@ __device__ __forceinline__ bool softmax_tile(const TcArgs& a, int t, uint32_t tS
         m4[e & 3] = fmaxf(m4[e & 3], x);
       }
     }
-    mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-  }
-  const float m_new = fmaxf(m_run, mt);
-  const bool need = m_new > m_run + kRescaleLog2;
-  float alpha = 1.f;
-  if (need) {
-    alpha = ex2(m_run - m_new);
-    m_run = m_new;
-  }
-  // P = 2^(s - m) as 16-bit pairs over the TMEM columns of S (the A operand of P V)
-  const bool none = (m_run == -INFINITY);
-  const float neg_m = -m_run;
-  float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int c2 = 0; c2 < BN / 64; ++c2) {
-    uint32_t pk[32];
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const int idx = c2 * 64 + 2 * e;
-      float p0, p1;
-      if (fast) {
-        p0 = ex2(fmaf(__uint_as_float(sr[idx]), p.scale_log2, neg_m));
-        p1 = ex2(fmaf(__uint_as_float(sr[idx + 1]), p.scale_log2, neg_m));
-      } else {
-        p0 = none ? 0.f : ex2(__uint_as_float(sr[idx]) + neg_m);
-        p1 = none ? 0.f : ex2(__uint_as_float(sr[idx + 1]) + neg_m);
-      }
-      s4[e & 3] += p0 + p1;
-      pk[e] = pack2<T>(p0, p1);
+    const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+    const float m_new = fmaxf(m_run, mt);
+    need = m_new > m_run + kRescaleLog2;
+    if (need) {
+      alpha = ex2(m_run - m_new);
+      m_run = m_new;
     }
-    tmem_st32(tS + c2 * 32, pk);
+    // P = 2^(s - m); zeros while no key of the row has been visible
+    const bool none = (m_run == -INFINITY);
+    const float neg_m = -m_run;
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int c2i = 0; c2i < BN / 64; ++c2i) {
+      uint32_t pk[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int idx = c2i * 64 + 2 * e;
+        const float p0 = none ? 0.f : ex2(__uint_as_float(sr[idx]) + neg_m);
+        const float p1 = none ? 0.f : ex2(__uint_as_float(sr[idx + 1]) + neg_m);
+        s4[e & 3] += p0 + p1;
+        pk[e] = pack2<T>(p0, p1);
+      }
+      tmem_st32(tS + c2i * 32, pk);
+    }
+    l_run = l_run * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
   }
-  l_run = l_run * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
   tmem_st_wait();
-  if (t > 0 && __any_sync(0xffffffffu, need)) {
-    // O must hold P_{t-1} V_{t-1} before it is rescaled (the newest phase pv_done can
-    // have completed here is t-1: P_t is not released yet)
+  if (t > 0) {
+    // Wait for P_{t-1} V_{t-1} on every tile, rescale or not.  The wait tests a phase
+    // parity, so this thread must never fall two phases behind pv_done: here the newest
+    // completed phase is at most t-1 (P_t is not released yet) and, because tile t-1
+    // waited for phase t-2, at least t-2.  O is then stable for the rescale.
     if (!__all_sync(0xffffffffu, mbar_wait(pv_bar, (t - 1) & 1, limit, abort))) return false;
     tc_fence_after();
+  }
+  if (t > 0 && __any_sync(0xffffffffu, need)) {
     for (int c = 0; c < (a.n_pv + 31) / 32; ++c) {
       uint32_t o[32];
       tmem_ld32_sync(tO + c * 32, o);

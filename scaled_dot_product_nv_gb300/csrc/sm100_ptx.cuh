@@ -32,21 +32,25 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
+// One poll: true when the phase of `parity` has completed.  The thread may be suspended
+// inside the poll until the phase completes or about kSuspendNs pass, so waiting warps
+// do not burn issue slots spinning.
+constexpr uint32_t kSuspendNs = 10000;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.b32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendNs)
       : "memory");
   return ok != 0;
 }
 
-// Waits for the phase of `parity` to complete, at most `limit` polls.  Every 64 polls
-// it also looks at `*abort` (set by any role that gave up) and stops early.  Returns
-// true when the phase completed.
+// Waits for the phase of `parity` to complete, at most `limit` polls (each at most
+// ~kSuspendNs).  Every 64 polls it also looks at `*abort` (set by any role that gave
+// up) and stops early.  Returns true when the phase completed.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit,
                                           const volatile int* abort) {
   for (uint64_t i = 0; i < limit; ++i) {
@@ -198,6 +202,32 @@ __host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_type, uint32_t a_mn
                                                  uint32_t b_mn_major, uint32_t m, uint32_t n) {
   return (1u << 4) | (ab_type << 7) | (ab_type << 10) | (a_mn_major << 15) | (b_mn_major << 16) |
          ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+// Packed pairs of f32 in one 64-bit register (Blackwell's two-wide FP32 FMA / ADD).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// max of three f32
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 // Two f32 -> one 32-bit word of two 16-bit values, `lo` in the low half.

@@ -184,3 +184,33 @@ def test_lse_only_optional_and_status_clean():
                        want_lse=False)
     assert none is None and torch.equal(o1.view(torch.int16), o2.view(torch.int16))
     assert nv.nv_sdpa_device_status(0) == (0, 0)
+
+
+@pytest.mark.parametrize("case", [
+    # one Q tile per CTA, 128-key tiles, long key loop (the 192/128 head)
+    W.Case(1, 8, 2, 1024, 4096, 192, 128, "bf16", "none", False, None, "u2", seed=41, name="nq1_d192"),
+    # two Q tiles per CTA (ping-pong), causal and unmasked
+    W.Case(1, 8, 2, 2048, 4096, 128, 128, "bf16", "causal", True, None, "n0.5", seed=42, name="nq2_causal"),
+    W.Case(2, 4, 4, 1000, 3000, 64, 64, "f16", "none", False, None, "n1", seed=43, name="nq2_d64"),
+    # 64-key tiles (the 256 head)
+    W.Case(1, 4, 1, 700, 3000, 256, 256, "f16", "causal", True, None, "n0.5", seed=44, name="bn64_d256"),
+], ids=lambda c: c.name)
+def test_pipeline_repeats_are_identical_and_correct(case):
+    """Long key loops through every CTA variant of the tensor-core prefill, run several
+    times: every run must give the same bits and match the oracle on sampled rows
+    (a synchronisation race shows up as run-to-run or oracle differences)."""
+    import torch
+    nv = ensure_built()
+    x = W.make_inputs(case)
+    dev = upload(case, x)
+    outs = []
+    for _ in range(4):
+        o, l = nv.sdpa(dev["q"], dev["k"], dev["v"], mask_kind=case.mask, scale=case.scale_f32,
+                       sinks=dev["sinks"])
+        outs.append((o.clone(), l.clone()))
+    torch.cuda.synchronize()
+    assert nv.nv_sdpa_device_status(0) == (nv.OK, 0)
+    for o, l in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0][0].view(torch.int16))
+        assert torch.equal(l, outs[0][1])
+    check_case(case, x)
