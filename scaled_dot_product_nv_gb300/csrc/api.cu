@@ -11,7 +11,7 @@
 #include <cmath>
 #include <cstring>
 
-#include "../../include/nv_sdpa.h"
+#include "nv_sdpa.h"
 #include "common.cuh"
 #include "kernels.h"
 

@@ -107,7 +107,7 @@ __device__ __forceinline__ int tiles_for_rows(const Params& p, int64_t r0) {
 template <typename T, int BN>
 __device__ __forceinline__ bool softmax_tile(const TcArgs& a, int t, uint32_t tS, uint32_t tO,
                                              bool row_ok, int64_t last_key, const uint32_t* mrow,
-                                             float& m_run, float& l_run, uint32_t pv_bar,
+                                             float& m_run, float& l_run, uint32_t pv_bar, bool wait_pv,
                                              uint64_t limit, volatile int* abort) {
   const Params& p = a.p;
   uint32_t sr[BN];
@@ -203,7 +203,7 @@ __device__ __forceinline__ bool softmax_tile(const TcArgs& a, int t, uint32_t tS
     l_run = l_run * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
   }
   tmem_st_wait();
-  if (t > 0) {
+  if (t > 0 && wait_pv) {
     // Wait for P_{t-1} V_{t-1} on every tile, rescale or not.  The wait tests a phase
     // parity, so this thread must never fall two phases behind pv_done: here the newest
     // completed phase is at most t-1 (P_t is not released yet) and, because tile t-1
@@ -238,18 +238,20 @@ __device__ __forceinline__ void epilogue_row(const Params& p, uint32_t tO, bool 
   }
   T* orow = reinterpret_cast<T*>(p.out) + out_row * p.dv;
   const int dv = (int)p.dv;
-  for (int c = 0; c < (dv + 31) / 32; ++c) {
-    uint32_t o[32];
+  // 128 columns of O per TMEM load (the O region is 128-column aligned and inside the
+  // allocation for every head this kernel takes)
+  for (int c0 = 0; c0 < dv; c0 += 128) {
+    uint32_t o[128];
     if (have_o) {
-      tmem_ld32_sync(tO + c * 32, o);
+      tmem_ld128_sync(tO + c0, o);
     } else {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) o[e] = 0u;
+      for (int e = 0; e < 128; ++e) o[e] = 0u;
     }
     if (row_ok) {
 #pragma unroll
-      for (int e8 = 0; e8 < 4; ++e8) {
-        const int col = c * 32 + e8 * 8;
+      for (int e8 = 0; e8 < 16; ++e8) {
+        const int col = c0 + e8 * 8;
         if (col < dv) {
           uint4 v;
           v.x = pack2<T>(__uint_as_float(o[e8 * 8 + 0]) * f, __uint_as_float(o[e8 * 8 + 1]) * f);
@@ -271,6 +273,7 @@ template <typename T, int BN, int NQ>
 __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __grid_constant__ TcArgs a) {
   static_assert(NQ == 1 || NQ == 2, "one or two Q tiles per CTA");
   static_assert(NQ == 1 || BN == 128, "the two-tile variant uses 128-key tiles");
+  constexpr int kMaxKsteps = (NQ == 2) ? 8 : 16;  // d <= 128 for two tiles, <= 256 otherwise
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const Params& p = a.p;
@@ -375,24 +378,39 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
     if (lane == 0 && n_max > 0) {
       const uint32_t idesc_s = idesc_f16(TypeCode<T>::v, 0, 0, kBM, BN);
       const uint32_t idesc_o = idesc_f16(TypeCode<T>::v, 0, 1, kBM, a.n_pv);
+      // Descriptors are built once; a K-step or a stage only moves the start address,
+      // which sits in the low bits (16-byte units, below 256 KB: no carry out of the
+      // field), so issuing an MMA costs one add -- the single issuing thread must keep
+      // up with 64-cycle 128x128x16 MMAs.
+      const uint64_t qd0 = smem_desc_sw128(sQ, 16, 1024);
+      const uint64_t kd0 = smem_desc_sw128(sK, 16, 1024);
+      const uint64_t vd0 = smem_desc_sw128(sV, BN * 128, 1024);
       // S = Q_q K_t^T into S slot `slot`, then commit to s_full[slot]
       auto issue_s = [&](int t, int q, int slot) {
-        const int s = t % kStages;
-        for (int k = 0; k < a.ksteps_qk; ++k) {
-          const uint32_t off = (uint32_t)(k & 3) * 32;  // 16 elements inside the 128-byte row
-          const uint64_t ad = smem_desc_sw128(sQ + q * q_bytes + (k >> 2) * kBM * 128 + off, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(sK + s * k_bytes + (k >> 2) * BN * 128 + off, 16, 1024);
-          mma_ss(tmem + tS_col(slot), ad, bd, idesc_s, k > 0);
+        const uint32_t dst = tmem + tS_col(slot);
+        const uint64_t ad = qd0 + (uint64_t)(q * (q_bytes >> 4));
+        const uint64_t bd = kd0 + (uint64_t)((t % kStages) * (k_bytes >> 4));
+        if (a.ksteps_qk == kMaxKsteps) {
+          // the head fills this variant: straight-line issue, no branch between MMAs (the
+          // single issuing thread must keep pace with 64-cycle 128x128x16 MMAs)
+#pragma unroll
+          for (int k = 0; k < kMaxKsteps; ++k)
+            mma_ss(dst, ad + (uint64_t)((k >> 2) * (kBM * 8) + (k & 3) * 2),
+                   bd + (uint64_t)((k >> 2) * (BN * 8) + (k & 3) * 2), idesc_s, k > 0);
+        } else {
+          for (int k = 0; k < a.ksteps_qk; ++k)
+            mma_ss(dst, ad + (uint64_t)((k >> 2) * (kBM * 8) + (k & 3) * 2),
+                   bd + (uint64_t)((k >> 2) * (BN * 8) + (k & 3) * 2), idesc_s, k > 0);
         }
         mma_commit(bar(kBarSFull + slot));
       };
       // O_q += P (from S slot `slot`) V_t, then commit to pv_done[q]
       auto issue_pv = [&](int t, int q, int slot) {
-        const int s = t % kStages;
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t bd = smem_desc_sw128(sV + s * v_bytes + kk * 16 * 128, BN * 128, 1024);
-          mma_ts(tmem + tO_col(q), tmem + tS_col(slot) + kk * 8, bd, idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
-        }
+        const uint32_t dst = tmem + tO_col(q), src = tmem + tS_col(slot);
+        const uint64_t bd = vd0 + (uint64_t)((t % kStages) * (v_bytes >> 4));
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(dst, src + kk * 8, bd + (uint64_t)(kk * 128), idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(kBarPvDone + q));
       };
       auto wait_kv = [&](int t) {
@@ -476,8 +494,11 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
         break;
       }
       tc_fence_after();
+      // NQ = 2: S of this tile was issued after P_{t-1} V_{t-1} of the same Q tile, and a
+      // commit tracks every earlier MMA of the issuing thread, so s_full already implies
+      // that O holds P_{t-1} V_{t-1}; NQ = 1 issues S_{t} before P_{t-1} V_{t-1} and waits.
       ok = softmax_tile<T, BN>(a, t, tmem + lane_base + tS_col(slot), tO, row_ok, last_key, mrow, m_run,
-                               l_run, bar(kBarPvDone + q), limit, abort);
+                               l_run, bar(kBarPvDone + q), NQ == 1, limit, abort);
       if (!ok) {
         fail(p, abort, kStatTimeoutMma);
         break;
