@@ -100,6 +100,8 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
   auto full = [&](int s) { return smem_addr(bars + s); };
   auto empty = [&](int s) { return smem_addr(bars + kDecStages + s); };
 
+  // the merge pass may be scheduled once every CTA of this grid is running
+  asm volatile("griddepcontrol.launch_dependents;");
   // ---- work unit
   int64_t x = blockIdx.x;
   const int64_t rc = x % a.n_rc; x /= a.n_rc;

@@ -39,6 +39,8 @@ sdpa_tiled_simt(const Params p) {
   float* red_sum = red_max + 4 * 32;          // [4][32]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the merge pass may be scheduled once every CTA of this grid is running
+  asm volatile("griddepcontrol.launch_dependents;");
   int64_t x = blockIdx.x;
   const int64_t rt = x % p.row_tiles; x /= p.row_tiles;
   const int64_t blk = x % p.nblk;
@@ -196,19 +198,23 @@ sdpa_tiled_simt(const Params p) {
   }
 }
 
-// Pass 2 of split-KV: one CTA (4 warps) per query row merges its nblk partials,
+// Pass 2 of split-KV: one CTA (8 warps) per query row merges its nblk partials,
 //   M = max(max_blk m_blk, sink),  L = sum_blk l_blk 2^(m_blk - M) + 2^(sink - M),
 //   out = sum_blk o_blk 2^(m_blk - M) / L,  lse = (M + log2 L) ln 2.
-// The blocks are split over the warps (warp w takes blocks w, w+4, ...) and each lane
-// reads 4 columns at a time, so a row's partials are read with many loads in flight.
-constexpr int kMergeWarps = 4;
+// Warp w takes blocks w, w+8, ...; each lane owns 4 columns per 128.  The loads of a
+// batch of blocks are all issued before any is used, so a row costs about one memory
+// latency instead of one per block.  Launched as a programmatic dependent of pass 1:
+// griddepcontrol.wait holds it until pass 1 has finished and its writes are visible.
+constexpr int kMergeWarps = 8;
 constexpr int kMaxBlk = 1024;
+constexpr int kMergeBatch = 8;  // blocks per warp whose loads are in flight together
 
 template <typename T>
 __global__ void __launch_bounds__(kMergeWarps * 32)
 sdpa_merge_partials(const Params p) {
   __shared__ float red[kMergeWarps];
   __shared__ float part[kMergeWarps][256 + 1];  // per-warp partial sums of one row, + L
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t row = blockIdx.x;
   const int64_t h = (row / p.Lq) % p.Hq;
@@ -223,28 +229,38 @@ sdpa_merge_partials(const Params p) {
   for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   if (lane == 0) red[warp] = M;
   __syncthreads();
-  M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+#pragma unroll
+  for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, red[w]);
   T* orow = reinterpret_cast<T*>(p.out) + row * p.dv;
   if (M == -INFINITY) {
     for (int c = threadIdx.x; c < dv; c += kMergeWarps * 32) orow[c] = from_f32<T>(0.f);
     if (threadIdx.x == 0 && p.lse) p.lse[row] = -INFINITY;
     return;
   }
-  // this warp's blocks: weighted sums of o (4 columns per lane per pass) and of l
   const float* po = p.part_o + row * p.nblk * p.dv;
   float L = 0.f;
   for (int c0 = lane * 4; c0 < dv; c0 += 128) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int k = warp; k < nb; k += kMergeWarps) {
-      const float mk = ml[2 * k];
-      const float w = (mk == -INFINITY) ? 0.f : ex2(mk - M);
-      const float4 o = *reinterpret_cast<const float4*>(po + (int64_t)k * p.dv + c0);
-      acc.x = fmaf(o.x, w, acc.x);
-      acc.y = fmaf(o.y, w, acc.y);
-      acc.z = fmaf(o.z, w, acc.z);
-      acc.w = fmaf(o.w, w, acc.w);
-      if (c0 == lane * 4) L = fmaf(ml[2 * k + 1], w, L);
+    for (int k0 = warp; k0 < nb; k0 += kMergeWarps * kMergeBatch) {
+      float mk[kMergeBatch], lk[kMergeBatch];
+      float4 o[kMergeBatch];
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u) {
+        const int k = k0 + u * kMergeWarps;
+        const bool in = k < nb;
+        mk[u] = in ? ml[2 * k] : -INFINITY;
+        lk[u] = in ? ml[2 * k + 1] : 0.f;
+        o[u] = in ? *reinterpret_cast<const float4*>(po + (int64_t)k * p.dv + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u) {
+        const float w = (mk[u] == -INFINITY) ? 0.f : ex2(mk[u] - M);
+        acc.x = fmaf(o[u].x, w, acc.x);
+        acc.y = fmaf(o[u].y, w, acc.y);
+        acc.z = fmaf(o[u].z, w, acc.z);
+        acc.w = fmaf(o[u].w, w, acc.w);
+        if (c0 == lane * 4) L = fmaf(lk[u], w, L);
+      }
     }
     part[warp][c0] = acc.x;
     part[warp][c0 + 1] = acc.y;
@@ -253,10 +269,14 @@ sdpa_merge_partials(const Params p) {
   }
   if (lane == 0) part[warp][256] = L;
   __syncthreads();
-  const float Lt = (part[0][256] + part[1][256]) + (part[2][256] + part[3][256]) + ex2(sk - M);
+  float Lt = ex2(sk - M);
+#pragma unroll
+  for (int w = 0; w < kMergeWarps; ++w) Lt += part[w][256];
   const float inv = 1.f / Lt;
   for (int c = threadIdx.x; c < dv; c += kMergeWarps * 32) {
-    const float s = (part[0][c] + part[1][c]) + (part[2][c] + part[3][c]);
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; ++w) s += part[w][c];
     orow[c] = from_f32<T>(s * inv);
   }
   if (threadIdx.x == 0 && p.lse) p.lse[row] = (M + log2f(Lt)) * kLn2;
@@ -299,8 +319,18 @@ cudaError_t launch_simt_t(const Params& p, cudaStream_t st) {
 template <typename T>
 cudaError_t launch_merge_t(const Params& p, cudaStream_t st) {
   const int64_t rows = p.B * p.Hq * p.Lq;
-  sdpa_merge_partials<T><<<(unsigned)rows, kMergeWarps * 32, 0, st>>>(p);
-  return cudaGetLastError();
+  // programmatic dependent launch: the merge grid is set up while pass 1 drains
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)rows);
+  cfg.blockDim = dim3(kMergeWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, sdpa_merge_partials<T>, p);
 }
 
 template <typename T>
