@@ -48,14 +48,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// One poll that returns at once (no suspension): used when the poll budget is tiny, so
+// that a small budget really makes a wait run out.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase of `parity` to complete, at most `limit` polls (each at most
-// ~kSuspendNs).  Every 64 polls it also looks at `*abort` (set by any role that gave
-// up) and stops early.  Returns true when the phase completed.
+// ~kSuspendNs; with a budget under 64 the polls do not suspend).  Every 8 polls it
+// also looks at `*abort` (set by any role that gave up) and stops early.  Returns true
+// when the phase completed.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit,
                                           const volatile int* abort) {
+  if (limit < 64) {
+    for (uint64_t i = 0; i < limit; ++i)
+      if (mbar_test_wait(bar, parity)) return true;
+    return false;
+  }
   for (uint64_t i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63) == 63 && abort && *abort) return false;
+    if ((i & 7) == 7 && abort && *abort) return false;
   }
   return false;
 }
