@@ -254,6 +254,21 @@ def host_threads():
 
 # ----------------------------------------------------------------------------- GPU arm
 
+def max_over_ranks(torch, dist, seconds, device):
+    """The slowest rank's time: every rank contributes its own elapsed time and all
+    receive the maximum (the job is as fast as its slowest replica)."""
+    t = torch.tensor([float(seconds)], dtype=torch.float64, device=device)
+    if dist is not None and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world_size, work_per_step_per_rank, steps, max_seconds, scale=1e12):
+    """Aggregate throughput of N replicas (weak scaling): all ranks' work over the
+    slowest rank's time, in units of `scale`."""
+    return world_size * work_per_step_per_rank * steps / max_seconds / scale
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -357,12 +372,9 @@ def run_ours(args):
     if pg:
         pg.barrier()
     clocks = sampler.stop()
-    t = torch.tensor([total_ms], device=dev)
-    if pg:
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-    total_ms_max = float(t.item())
+    total_ms_max = max_over_ranks(torch, pg, total_ms, dev)
     flops_step = prefill_flops(pc)
-    value = ws * flops_step * args.steps / (total_ms_max / 1e3) / 1e12
+    value = whole_job_rate(ws, flops_step, args.steps, total_ms_max / 1e3)
     launch_avg = statistics.mean(launch_ms)
     peak_t = pk["bf16_tflops"]
     p_achieved = flops_step / (launch_avg / 1e3) / 1e12
@@ -391,6 +403,30 @@ def run_ours(args):
         "algorithmic_bytes_per_call": dbytes,
     }
 
+    # --------------------------------------------------------------- boolean mask + sinks, head 256
+    mc = W.prefill_f16_boolmask_sinks()
+    mx = W.make_inputs(mc)
+    msets = device_sets(mc, mx, max(2, math.ceil(2 * L2_BYTES / set_bytes(mc)) + 1))
+    _, mplan = nv.nv_sdpa_plan((mc.B, mc.Hq, mc.Hkv, mc.Lq, mc.Lk, mc.d, mc.dv),
+                               W.MASK_CODES[mc.mask], 1, W.DTYPE_CODES[mc.dtype])
+    msteps = max(args.steps, 50)
+    _, m_launch = time_calls(torch, caller(mc), msets, msteps, max(args.warmup, 3), stream)
+    mflops = prefill_flops(mc)  # dense: a boolean mask is not halved
+    m_call_avg = statistics.mean(m_launch)
+    m_tf = mflops / (m_call_avg / 1e3) / 1e12
+    prefill_mask = {
+        "workload": mc.name, "metric": "prefill attention TFLOP/s", "value": round(m_tf, 2),
+        "unit": "TFLOP/s", "ms_per_call": round(m_call_avg, 5), "steps": msteps,
+        "kernel": mplan["kernel"], "launches_per_call": mplan["launches"],
+        "flops_per_call": mflops,
+        "l2": f"inputs rotate over {len(msets)} device copies",
+        "roofline": {"bound": "tensor", "achieved": round(m_tf, 2), "peak": pk["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": round(m_tf / pk["bf16_tflops"], 4),
+                     "peak_source": pk_src + " bf16_tflops (f16 runs at the bf16 rate)",
+                     "timed": "whole call (mask packing + attention) per CUDA-event pair",
+                     "traffic": recorded_traffic("prefill:" + mc.name)},
+    }
+
     # --------------------------------------------------------------- end to end (host buffers)
     e2e_steps = min(args.steps, 10)
     pin = {n: torch.from_numpy(np.ascontiguousarray(px[n]).view(np.int16)).pin_memory()
@@ -413,10 +449,7 @@ def run_ours(args):
     for _ in range(e2e_steps):
         host_call(None)
     e2e_s = time.perf_counter() - t0
-    te = torch.tensor([e2e_s], device=dev)
-    if pg:
-        pg.all_reduce(te, op=pg.ReduceOp.MAX)
-    e2e_value = ws * flops_step * e2e_steps / float(te.item()) / 1e12
+    e2e_value = whole_job_rate(ws, flops_step, e2e_steps, max_over_ranks(torch, pg, e2e_s, dev))
     h2d = sum(int(pin[n].numel()) * 2 for n in pin)
     d2h = int(hout.numel()) * 2 + int(hlse.numel()) * 4
 
@@ -451,6 +484,7 @@ def run_ours(args):
                      "kernel_ms": round(launch_avg, 5),
                      "traffic": recorded_traffic("prefill:" + pc.name)},
         "decode": decode,
+        "prefill_mask": prefill_mask,
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "api": "nv_sdpa_host (pinned host buffers; copies, device alloc, sync inside)"},

@@ -413,8 +413,9 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
           mma_ts(dst, src + kk * 8, bd + (uint64_t)(kk * 128), idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(kBarPvDone + q));
       };
+      // (the issuer's waits never suspend: see mbar_wait)
       auto wait_kv = [&](int t) {
-        if (mbar_wait(bar(kBarKvFull + t % kStages), (t / kStages) & 1, limit, abort)) {
+        if (mbar_wait<false>(bar(kBarKvFull + t % kStages), (t / kStages) & 1, limit, abort)) {
           tc_fence_after();
           return true;
         }
@@ -422,14 +423,14 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
         return false;
       };
       auto wait_p = [&](int slot, uint32_t parity) {
-        if (mbar_wait(bar(kBarPFull + slot), parity, limit, abort)) {
+        if (mbar_wait<false>(bar(kBarPFull + slot), parity, limit, abort)) {
           tc_fence_after();
           return true;
         }
         fail(p, abort, kStatTimeoutMma);
         return false;
       };
-      bool ok = mbar_wait(bar(kBarQ), 0, limit, abort);
+      bool ok = mbar_wait<false>(bar(kBarQ), 0, limit, abort);
       if (!ok) fail(p, abort, kStatTimeoutTmaFull);
       ok = ok && wait_kv(0);
       if constexpr (NQ == 1) {

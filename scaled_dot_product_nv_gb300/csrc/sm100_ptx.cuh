@@ -62,10 +62,18 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase of `parity` to complete, at most `limit` polls (each at most
-// ~kSuspendNs; with a budget under 64 the polls do not suspend).  Every 8 polls it
-// also looks at `*abort` (set by any role that gave up) and stops early.  Returns true
-// when the phase completed.
+// Waits for the phase of `parity` to complete, at most `limit` polls.  Every 8 polls
+// it also looks at `*abort` (set by any role that gave up) and stops early.  Returns
+// true when the phase completed.
+//   kSleep = true: each poll may suspend the thread up to ~kSuspendNs, so a waiting warp
+//     does not take issue slots from the warps that work.
+//   kSleep = false: polls that return at once (about 50 cycles each; 64 of them count as
+//     one unit of `limit`).  This is the form for the thread that issues MMAs: a hinted
+//     poll costs about twice as long even on a completed phase, and the tensor pipe,
+//     which queues very little ahead of the issuing thread, runs dry meanwhile.
+// With a budget under 64 the polls never suspend and are not scaled (so that a tiny
+// budget really makes a wait run out).
+template <bool kSleep = true>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit,
                                           const volatile int* abort) {
   if (limit < 64) {
@@ -73,9 +81,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
       if (mbar_test_wait(bar, parity)) return true;
     return false;
   }
-  for (uint64_t i = 0; i < limit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 7) == 7 && abort && *abort) return false;
+  if (kSleep) {
+    for (uint64_t i = 0; i < limit; ++i) {
+      if (mbar_try_wait(bar, parity)) return true;
+      if ((i & 7) == 7 && abort && *abort) return false;
+    }
+  } else {
+    for (uint64_t i = 0; i < limit * 64; ++i) {
+      if (mbar_test_wait(bar, parity)) return true;
+      if ((i & 63) == 63 && abort && *abort) return false;
+    }
   }
   return false;
 }
