@@ -35,6 +35,18 @@ bool mul_ok(int64_t a, int64_t b, int64_t* r) {
   return *r <= (int64_t(1) << 62);
 }
 
+// Warps sharing one (b, KV head, 16-row tile)'s nblk key blocks in the decode kernel:
+// as many as keep every warp of the grid resident at once (at least one, at most one
+// per block).
+int64_t decode_spans(const nv_sdpa_dims& x, int64_t nblk) {
+  const int64_t rows = (x.Hq / x.Hkv) * x.Lq;
+  const int64_t rc = (rows + decode_mma_rows_per_warp() - 1) / decode_mma_rows_per_warp();
+  const int64_t warp_slots = kNumSms * decode_mma_ctas_per_sm(x.d, x.dv) * decode_mma_warps_per_cta(x.d, x.dv);
+  int64_t units;
+  if (!mul_ok(x.B * x.Hkv, rc, &units) || units < 1) return 1;
+  return std::max<int64_t>(1, std::min(nblk, warp_slots / units));
+}
+
 // Checks that need no pointer.  Returns NV_SDPA_OK or the status.
 int check_dims(const nv_sdpa_dims* dm, int mask_kind, int dtype) {
   if (!dm) return NV_SDPA_ERR_INVALID;
@@ -98,23 +110,29 @@ int make_plan(const nv_sdpa_dims& x, int mask_kind, int has_sinks, int dtype, nv
     return NV_SDPA_OK;
   }
   if (pl->path == NV_SDPA_PATH_DECODE && decode_mma_supported(dtype, x.d, x.dv)) {
-    // tensor-core decode: one CTA per (b, KV head, key block, 16 query rows); enough
-    // key blocks that one batch item alone fills every CTA slot of the GPU
+    // Tensor-core decode.  The keys of each KV head are cut into blocks that depend on
+    // the head shape and Lk alone, never on B: enough of them that one batch item alone
+    // keeps 2 x 152 warps streaming, each at least 256 keys.  Every block's partial is
+    // computed the same way whichever warp computes it, so a batch item gets the bits
+    // it would get alone.  How many warps share a (b, KV head, 16-row tile)'s blocks
+    // (each walking a contiguous run of them) is free, and is chosen so that all warps
+    // run as one wave: fewer, longer streams read K and V best (measured: one wave at
+    // 85-95 % of the slots beats two full waves, and far beats eight).
     pl->kernel = NV_SDPA_KERNEL_DECODE_MMA;
-    pl->rows_per_cta = decode_mma_rows_per_cta();
+    pl->rows_per_cta = decode_mma_rows_per_warp();
     const int64_t rc = cdiv(G, pl->rows_per_cta);
-    const int64_t slots = kNumSms * decode_mma_ctas_per_sm(x.d, x.dv);
-    const int64_t kt = decode_mma_key_tile();
-    int64_t nblk = cdiv(slots, x.Hkv * rc);
-    nblk = std::min(nblk, cdiv(x.Lk, 4 * kt));
+    int64_t nblk = cdiv(2 * kNumSms, x.Hkv * rc);
+    nblk = std::min(nblk, cdiv(x.Lk, 256));
     nblk = std::max<int64_t>(1, std::min(nblk, merge_max_blocks()));
-    const int64_t kpb = cdiv(cdiv(x.Lk, nblk), kt) * kt;
+    const int64_t kpb = cdiv(cdiv(x.Lk, nblk), 64) * 64;  // whole key tiles
     nblk = cdiv(x.Lk, kpb);
     pl->nblk = nblk;
     pl->keys_per_blk = kpb;
-    int64_t grid;
-    if (!mul_ok(x.B * x.Hkv, rc, &grid) || !mul_ok(grid, nblk, &grid) || grid > 0x7fffffff)
+    int64_t units, warp_units;
+    if (!mul_ok(x.B * x.Hkv, rc, &units) || !mul_ok(units, decode_spans(x, nblk), &warp_units))
       return NV_SDPA_ERR_UNSUPPORTED;
+    const int64_t grid = decode_mma_grid(warp_units, x.d, x.dv);
+    if (grid > 0x7fffffff) return NV_SDPA_ERR_UNSUPPORTED;
     pl->grid = grid;
     pl->launches = nblk > 1 ? 2 : 1;
     if (nblk > 1) {
@@ -229,6 +247,8 @@ NV_SDPA_API int nv_sdpa(const void* q, const void* k, const void* v, const nv_sd
   p.g = x.Hq / x.Hkv; p.G = p.g * x.Lq;
   p.nblk = pl.nblk; p.keys_per_blk = pl.keys_per_blk;
   p.row_tiles = pl.rows_per_cta ? (p.G + pl.rows_per_cta - 1) / pl.rows_per_cta : 1;
+  p.spans = 1;
+  if (pl.kernel == NV_SDPA_KERNEL_DECODE_MMA) p.spans = decode_spans(x, pl.nblk);
   p.mask_kind = mask_kind;
   p.has_sinks = sinks != nullptr;
   p.scale = scale;
@@ -405,6 +425,8 @@ NV_SDPA_API int nv_sdpa_noalloc(const void* q, const void* k, const void* v, con
   p.g = x.Hq / x.Hkv; p.G = p.g * x.Lq;
   p.nblk = pl.nblk; p.keys_per_blk = pl.keys_per_blk;
   p.row_tiles = pl.rows_per_cta ? (p.G + pl.rows_per_cta - 1) / pl.rows_per_cta : 1;
+  p.spans = 1;
+  if (pl.kernel == NV_SDPA_KERNEL_DECODE_MMA) p.spans = decode_spans(x, pl.nblk);
   p.mask_kind = mask_kind;
   p.has_sinks = sinks != nullptr;
   p.scale = scale;

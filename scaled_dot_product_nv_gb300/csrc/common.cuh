@@ -40,6 +40,7 @@ struct Params {
   int64_t nblk;         // key blocks per KV head (1 = final output written directly)
   int64_t keys_per_blk; // keys per block (a multiple of every kernel's key tile)
   int64_t row_tiles;    // ceil(G / rows per CTA)
+  int64_t spans;        // decode: CTAs sharing the key blocks of one (b, KV head, row tile)
   int mask_kind;
   int has_sinks;
   float scale;          // as passed

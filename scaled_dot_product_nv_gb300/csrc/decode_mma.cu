@@ -1,23 +1,27 @@
-// Decode (Lq <= 8) pass 1 for f16/bf16: stream one block of keys of one KV head from
-// HBM through a TMA ring and reduce it against the (up to 16) query rows that share
-// that KV head, writing either the final output (one block) or a partial
-// (m, l, o) per row for the log-sum-exp merge (sdpa_merge_partials).
+// Decode (Lq <= 8) pass 1 for f16/bf16: stream the keys of one KV head from HBM
+// through TMA rings and reduce them against the (up to 16) query rows that share that
+// KV head, writing one partial (m, l, o) per row and key block for the log-sum-exp merge
+// (sdpa_merge_partials), or the final output when there is a single block.
 //
 // This is the split-KV two-pass scheme whose kernels are named in "nuvec-core 0.6.1
 // tests/attention_plan.rs" (the vector 2-pass pair, one grid layer per key block); the
 // arithmetic per block is the online softmax of "lattice-inference 0.4.0
 // src/attention/flash.rs" (run_tiled_attention_head).  The GB300 design:
 //
-// * The path is bound by reading K and V once.  A producer warp keeps a 3-stage ring of
-//   64-key K and V tiles in flight with 3-D TMA (128-byte swizzle, zero fill past Lk);
-//   two CTAs per SM keep ~190 KB of loads outstanding per SM.
-// * Four compute warps take 16 keys of each tile.  The query rows (g heads x Lq, padded
-//   to 16) are the M side of mma.sync.m16n8k16 (f16/bf16 in, f32 accumulate): S = Q K^T
-//   over the warp's 16 keys, the online softmax on the accumulator fragments (row max
-//   over a lane quad), P re-packed in registers as the A operand of O += P V with V
-//   read by ldmatrix.trans.  Tensor-core math keeps the SMs far from the ALU limit that
-//   FP32 dot products would hit at 8 query rows per key.
-// * At the end of the block the four warps' (m, l, O) are merged through shared memory.
+// * The path is bound by reading K and V once.  Every warp of a CTA works alone: it owns
+//   a ring of ST stages of 16- or 32-key K and V tiles (3-D TMA, 128-byte swizzle, zero fill
+//   past Lk), issues its own loads ST tiles ahead, and walks a contiguous run of key
+//   blocks of one (b, KV head, 16-row tile).  With no producer warp, no consumer
+//   barriers and no cross-warp merge, a block boundary costs a partial's write and
+//   nothing else.
+// * The key blocks depend on the head shape and Lk alone.  Each block's online softmax
+//   starts afresh and runs in the same order in whichever warp takes it, so the number
+//   of warps (one wave of them, whatever the batch size) changes no bit of any item.
+// * The query rows (g heads x Lq, padded to 16) are the M side of mma.sync.m16n8k16
+//   (f16/bf16 in, f32 accumulate): S = Q K^T over the tile's keys, the online softmax
+//   on the accumulator fragments (row max over a lane quad), P re-packed in registers as
+//   the A operand of O += P V with V read by ldmatrix.trans.  Tensor-core math keeps the
+//   SMs far from the ALU limit that FP32 dot products would hit at 8 query rows per key.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -29,18 +33,15 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kRowsDec = 16;     // query rows per CTA (the M of m16n8k16)
-constexpr int kKT = 64;          // keys per TMA tile
-constexpr int kWarpsC = 4;       // compute warps
-constexpr int kDecThreads = (kWarpsC + 1) * 32;
-constexpr int kDecStages = 3;
+constexpr int kRowsDec = 16;     // query rows per warp (the M of m16n8k16)
+constexpr int kKTMax = 32;       // the largest key tile of any bucket (key blocks are multiples of 64)
 constexpr float kRescaleLog2Dec = 8.0f;
 constexpr uint64_t kDrainLimitDec = 1ull << 18;  // polls of <= ~10 us each
 
 struct DecArgs {
   CUtensorMap tmk, tmv;
   Params p;
-  int n_rc;       // row chunks of 16 rows per KV head
+  int n_rc;       // row tiles of 16 rows per KV head
   int dpanels, dvpanels;
 };
 
@@ -83,9 +84,29 @@ __device__ __forceinline__ uint32_t sw128(uint32_t panel, int row, int chunk) {
   return panel + row * 128 + ((chunk ^ (row & 7)) << 4);
 }
 
+// Shape of each (d, dv) bucket's kernel: keys per tile, warps per CTA and ring stages
+// per warp, so that about 192 KB of loads are in flight per SM.  The per-warp mma.sync
+// work is what bounds the stream, so heads up to 128 run 8 warps (two per scheduler) on
+// 16-key tiles; larger heads, whose accumulators would not fit 8 warps' registers, run
+// 3-4 warps on 32-key tiles.  (Measured on the 8 x 32/4 x 32769-key f16 decode: 4 warps
+// of 32-key tiles 4430 GB/s, 8 warps of 16-key tiles 5390 GB/s; 6, 7, 10 or 12 warps
+// lose to an uneven share of key blocks or to register spills.)
+template <int DMAX, int DV> struct DecShape {
+  static constexpr bool kSmallHead = DMAX <= 128 && DV <= 128;
+  static constexpr int KT = kSmallHead ? 16 : 32;
+  static constexpr int kStageBytes = (DMAX / 64 + DV / 64) * KT * 128;
+  static constexpr int WPC = kSmallHead ? 8 : (DMAX >= 256) ? 3 : 4;
+  static constexpr int ST = (WPC * 3 * kStageBytes <= 192 * 1024) ? 3 : 2;
+  static constexpr int kSmem = WPC * ST * kStageBytes + 1024 + WPC * ST * 8 + 64;
+  static constexpr int kCtasPerSm = (kSmem <= 113 * 1024) ? 2 : 1;
+};
+
 template <typename T, int DMAX, int DV>
-__global__ void __launch_bounds__(kDecThreads, (DMAX <= 128 && DV <= 128) ? 2 : 1)
+__global__ void __launch_bounds__(DecShape<DMAX, DV>::WPC * 32, DecShape<DMAX, DV>::kCtasPerSm)
 sdpa_decode_mma(const __grid_constant__ DecArgs a) {
+  using Sh = DecShape<DMAX, DV>;
+  constexpr int ST = Sh::ST;
+  constexpr int kKT = Sh::KT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const Params& p = a.p;
@@ -94,70 +115,51 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
 
   const uint32_t k_bytes = a.dpanels * kKT * 128, v_bytes = a.dvpanels * kKT * 128;
   const uint32_t stage_bytes = k_bytes + v_bytes;
-  const uint32_t s0 = smem_addr(base);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kDecStages * stage_bytes);
-  volatile int* abort = reinterpret_cast<volatile int*>(bars + 2 * kDecStages);
-  auto full = [&](int s) { return smem_addr(bars + s); };
-  auto empty = [&](int s) { return smem_addr(bars + kDecStages + s); };
+  const uint32_t ring = smem_addr(base) + warp * ST * stage_bytes;  // this warp's stages
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + Sh::WPC * ST * stage_bytes);
+  auto full = [&](int s) { return smem_addr(bars + warp * ST + s); };
 
   // the merge pass may be scheduled once every CTA of this grid is running
   asm volatile("griddepcontrol.launch_dependents;");
-  // ---- work unit
-  int64_t x = blockIdx.x;
-  const int64_t rc = x % a.n_rc; x /= a.n_rc;
-  const int64_t blk = x % p.nblk;
-  const int64_t bh = x / p.nblk;
-  const int64_t b = bh / p.Hkv, hkv = bh % p.Hkv;
-  const int64_t j_begin = blk * p.keys_per_blk;
-  const int64_t j_end = (j_begin + p.keys_per_blk < p.Lk) ? j_begin + p.keys_per_blk : p.Lk;
-  const int n_tiles = (int)((j_end - j_begin + kKT - 1) / kKT);
-
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kDecStages; ++s) {
-      mbar_init(full(s), 1);
-      mbar_init(empty(s), kWarpsC);
-    }
-    *abort = 0;
+    for (int i = 0; i < Sh::WPC * ST; ++i) mbar_init(smem_addr(bars + i), 1);
     fence_mbar_init();
   }
   __syncthreads();
+
+  // ---- this warp's work: (b, KV head, row tile) and a contiguous run of its key blocks
+  const int64_t gw = (int64_t)blockIdx.x * Sh::WPC + warp;
+  if (gw >= p.B * p.Hkv * a.n_rc * p.spans) return;
+  const int64_t span = gw % p.spans;
+  const int64_t unit = gw / p.spans;
+  const int64_t rc = unit % a.n_rc;
+  const int64_t bh = unit / a.n_rc;
+  const int64_t b = bh / p.Hkv, hkv = bh % p.Hkv;
+  const int64_t c_begin = span * p.nblk / p.spans, c_end = (span + 1) * p.nblk / p.spans;
+  const int64_t key_begin = c_begin * p.keys_per_blk;
+  const int64_t key_end = (c_end * p.keys_per_blk < p.Lk) ? c_end * p.keys_per_blk : p.Lk;
+  const int n_tiles = (int)((key_end - key_begin + kKT - 1) / kKT);
+  const int tpb = (int)(p.keys_per_blk / kKT);  // tiles per (full) key block
   const uint64_t limit = p.wait_limit;
 
-  // merge buffers (reuse the ring after it drains): per warp m[16], l[16], o[16][DV]
-  float* mo = reinterpret_cast<float*>(base);
-
-  if (warp == kWarpsC) {
-    // ================================================================ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&a.tmk);
-      tma_prefetch_desc(&a.tmv);
-      int issued = 0;
-      for (int t = 0; t < n_tiles; ++t) {
-        const int s = t % kDecStages;
-        if (!mbar_wait(empty(s), ((t / kDecStages) & 1) ^ 1, limit, abort)) {
-          *abort = 1;
-          record_status(p, kStatTimeoutSlotFree);
-          break;
-        }
-        mbar_arrive_expect_tx(full(s), stage_bytes);
-        const int key0 = (int)(j_begin + (int64_t)t * kKT);
-        for (int pn = 0; pn < a.dpanels; ++pn)
-          tma_load_3d(s0 + s * stage_bytes + pn * kKT * 128, &a.tmk, full(s), pn * 64, key0, (int)bh);
-        for (int pn = 0; pn < a.dvpanels; ++pn)
-          tma_load_3d(s0 + s * stage_bytes + k_bytes + pn * kKT * 128, &a.tmv, full(s), pn * 64, key0, (int)bh);
-        issued = t + 1;
-      }
-      for (int t = issued > kDecStages ? issued - kDecStages : 0; t < issued; ++t)
-        mbar_wait(full(t % kDecStages), (t / kDecStages) & 1, kDrainLimitDec, nullptr);
-    }
-    __syncwarp();
-    __syncthreads();  // ring drained: the compute warps may reuse it for the merge
-    __syncthreads();  // merge buffers written
-    return;
+  // tile i of the run into ring slot i % ST (lane 0)
+  auto issue = [&](int i) {
+    const int s = i % ST;
+    mbar_arrive_expect_tx(full(s), stage_bytes);
+    const int key0 = (int)(key_begin + (int64_t)i * kKT);
+    for (int pn = 0; pn < a.dpanels; ++pn)
+      tma_load_3d(ring + s * stage_bytes + pn * kKT * 128, &a.tmk, full(s), pn * 64, key0, (int)bh);
+    for (int pn = 0; pn < a.dvpanels; ++pn)
+      tma_load_3d(ring + s * stage_bytes + k_bytes + pn * kKT * 128, &a.tmv, full(s), pn * 64, key0, (int)bh);
+  };
+  int issued = n_tiles < ST ? n_tiles : ST;
+  if (lane == 0) {
+    tma_prefetch_desc(&a.tmk);
+    tma_prefetch_desc(&a.tmv);
+    for (int i = 0; i < issued; ++i) issue(i);
   }
 
-  // ================================================================ compute warps
-  // This lane's two query rows (gid and gid + 8 of the chunk).
+  // This lane's two query rows (gid and gid + 8 of the row tile).
   const int64_t rows_here = (p.G - rc * kRowsDec < kRowsDec) ? p.G - rc * kRowsDec : kRowsDec;
   int64_t ri[2], last[2];
   bool rok[2];
@@ -190,39 +192,47 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
   }
 
   constexpr int NT = DV / 8;  // n-tiles of the output
+  const int dv = (int)p.dv;
   float o[NT][4];
 #pragma unroll
   for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+  int consumed = 0;
 
-  bool ok = true;
-  for (int t = 0; t < n_tiles; ++t) {
-    const int s = t % kDecStages;
-    ok = __all_sync(0xffffffffu, mbar_wait(full(s), (t / kDecStages) & 1, limit, abort));
-    if (!ok) {
-      *abort = 1;
-      record_status(p, kStatTimeoutTmaFull);
+  for (int gt = 0; gt < n_tiles; ++gt) {
+    const int s = gt % ST;
+    if (!__all_sync(0xffffffffu, mbar_wait(full(s), (gt / ST) & 1, limit, nullptr))) {
+      if (lane == 0) record_status(p, kStatTimeoutTmaFull);
       break;
     }
-    const uint32_t kst = s0 + s * stage_bytes, vst = kst + k_bytes;
-    // ---- S = Q K^T over this warp's 16 keys
-    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    const int krow = warp * 16 + (lane >> 4) * 8 + (lane & 7);
+    consumed = gt + 1;
+    const int64_t c = c_begin + gt / tpb;  // key block of this tile
+    const int64_t j_end = ((c + 1) * p.keys_per_blk < p.Lk) ? (c + 1) * p.keys_per_blk : p.Lk;
+    const uint32_t kst = ring + s * stage_bytes, vst = kst + k_bytes;
+    // ---- S = Q K^T over the tile's keys (n-tiles of 8 keys)
+    constexpr int NS = kKT / 8;  // n-tiles of S
+    float sc[NS][4];
+#pragma unroll
+    for (int nt = 0; nt < NS; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
     for (int kb = 0; kb < kKB; ++kb) {
       if (kb < nkb) {
-        uint32_t b0, b1, b2, b3;
         const int chunk = (kb & 3) * 2 + ((lane >> 3) & 1);
-        ldsm_x4(sw128(kst + (kb >> 2) * kKT * 128, krow, chunk), b0, b1, b2, b3);
-        MmaOp<T>::run(sc[0], qa[kb], b0, b1);
-        MmaOp<T>::run(sc[1], qa[kb], b2, b3);
+#pragma unroll
+        for (int h16 = 0; h16 < kKT / 16; ++h16) {
+          uint32_t b0, b1, b2, b3;
+          const int krow = h16 * 16 + (lane >> 4) * 8 + (lane & 7);
+          ldsm_x4(sw128(kst + (kb >> 2) * kKT * 128, krow, chunk), b0, b1, b2, b3);
+          MmaOp<T>::run(sc[2 * h16], qa[kb], b0, b1);
+          MmaOp<T>::run(sc[2 * h16 + 1], qa[kb], b2, b3);
+        }
       }
     }
     // ---- mask, online softmax (rows gid / gid + 8; keys spread over the lane quad)
-    const int64_t jt = j_begin + (int64_t)t * kKT + warp * 16;
+    const int64_t jt = key_begin + (int64_t)gt * kKT;
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
+    for (int nt = 0; nt < NS; ++nt) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int hrow = e >> 1;
@@ -246,115 +256,108 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
         m[hrow] = m_new;
       }
     }
-    uint32_t pa[4];
+    // P as the A operand of the k16 steps: pa[ks] covers keys 16 ks .. 16 ks + 15
+    uint32_t pa[kKT / 16][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
+    for (int hrow = 0; hrow < 2; ++hrow) l[hrow] *= alpha[hrow];
+#pragma unroll
+    for (int nt = 0; nt < NS; ++nt) {
 #pragma unroll
       for (int hrow = 0; hrow < 2; ++hrow) {
         const bool none = (m[hrow] == -INFINITY);
         const float p0 = none ? 0.f : ex2(sc[nt][2 * hrow] - m[hrow]);
         const float p1 = none ? 0.f : ex2(sc[nt][2 * hrow + 1] - m[hrow]);
-        l[hrow] = l[hrow] * (nt == 0 ? alpha[hrow] : 1.f) + p0 + p1;
-        pa[nt * 2 + hrow] = MmaOp<T>::pack(p0, p1);
+        l[hrow] += p0 + p1;
+        pa[nt >> 1][(nt & 1) * 2 + hrow] = MmaOp<T>::pack(p0, p1);
       }
     }
+    if (alpha[0] != 1.f || alpha[1] != 1.f) {
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      o[j][0] *= alpha[0];
-      o[j][1] *= alpha[0];
-      o[j][2] *= alpha[1];
-      o[j][3] *= alpha[1];
+      for (int j = 0; j < NT; ++j) {
+        o[j][0] *= alpha[0];
+        o[j][1] *= alpha[0];
+        o[j][2] *= alpha[1];
+        o[j][3] *= alpha[1];
+      }
     }
     // ---- O += P V: V tile rows = keys, ldmatrix.trans gives the k16 x n8 B fragments
-    const int vrow = warp * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
 #pragma unroll
-    for (int j2 = 0; j2 < NT / 2; ++j2) {
-      const int chunk = 2 * j2 + (lane >> 4);  // 16-byte chunk of dv (8 columns)
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(sw128(vst + (chunk >> 3) * kKT * 128, vrow, chunk & 7), b0, b1, b2, b3);
-      MmaOp<T>::run(o[2 * j2], pa, b0, b1);
-      MmaOp<T>::run(o[2 * j2 + 1], pa, b2, b3);
+    for (int ks = 0; ks < kKT / 16; ++ks) {
+      const int vrow = ks * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+#pragma unroll
+      for (int j2 = 0; j2 < NT / 2; ++j2) {
+        const int chunk = 2 * j2 + (lane >> 4);  // 16-byte chunk of dv (8 columns)
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(sw128(vst + (chunk >> 3) * kKT * 128, vrow, chunk & 7), b0, b1, b2, b3);
+        MmaOp<T>::run(o[2 * j2], pa[ks], b0, b1);
+        MmaOp<T>::run(o[2 * j2 + 1], pa[ks], b2, b3);
+      }
     }
+    // ---- the slot is read: refill it with tile gt + ST (the async proxy's write must
+    // follow this warp's reads of the slot)
     __syncwarp();
-    if (lane == 0) mbar_arrive(empty(s));
-  }
+    if (lane == 0 && gt + ST < n_tiles) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(gt + ST);
+    }
+    if (gt + ST < n_tiles) issued = gt + ST + 1;
 
-  // ---- merge the four warps through shared memory
-  __syncthreads();  // (1) every warp is done with the ring, the producer drained it
+    // ---- end of a key block: write its partial (or the output when it is the only one)
+    if ((gt + 1) % tpb == 0 || gt + 1 == n_tiles) {
+      float L[2];
 #pragma unroll
-  for (int hrow = 0; hrow < 2; ++hrow) {
-    l[hrow] += __shfl_xor_sync(0xffffffffu, l[hrow], 1);
-    l[hrow] += __shfl_xor_sync(0xffffffffu, l[hrow], 2);
-  }
-  float* wm = mo + warp * (2 * kRowsDec + kRowsDec * DV);
-  float* wl = wm + kRowsDec;
-  float* wo = wl + kRowsDec;
-  if (tig == 0) {
-    wm[gid] = m[0];
-    wm[gid + 8] = m[1];
-    wl[gid] = l[0];
-    wl[gid + 8] = l[1];
-  }
-#pragma unroll
-  for (int j = 0; j < NT; ++j) {
-    const int c = j * 8 + 2 * tig;
-    wo[gid * DV + c] = o[j][0];
-    wo[gid * DV + c + 1] = o[j][1];
-    wo[(gid + 8) * DV + c] = o[j][2];
-    wo[(gid + 8) * DV + c + 1] = o[j][3];
-  }
-  __syncthreads();  // (2)
-  ok = ok && !*abort;
-  if (!ok) return;
-  // 128 compute threads: thread -> (row, column group)
-  const int tid = threadIdx.x;
-  const int dv = (int)p.dv;
-  for (int idx = tid; idx < kRowsDec * (DV / 4); idx += kWarpsC * 32) {
-    const int r = idx / (DV / 4), c4 = (idx % (DV / 4)) * 4;
-    if (r >= rows_here || c4 >= dv) continue;
-    const int stride = 2 * kRowsDec + kRowsDec * DV;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarpsC; ++w) M = fmaxf(M, mo[w * stride + r]);
-    const int64_t rho = rc * kRowsDec + r;
-    const int64_t row_global = (b * p.Hq + hkv * p.g + rho / p.Lq) * p.Lq + rho % p.Lq;
-    float L = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kWarpsC; ++w) {
-        const float mw = mo[w * stride + r];
-        const float sw = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-        L += mo[w * stride + kRowsDec + r] * sw;
-        const float* src = mo + w * stride + 2 * kRowsDec + r * DV + c4;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[e] += src[e] * sw;
+      for (int hrow = 0; hrow < 2; ++hrow) {
+        L[hrow] = l[hrow] + __shfl_xor_sync(0xffffffffu, l[hrow], 1);
+        L[hrow] += __shfl_xor_sync(0xffffffffu, L[hrow], 2);
       }
-    }
-    if (p.nblk == 1) {
-      const int64_t h = hkv * p.g + rho / p.Lq;
-      const float sk = sink_log2<T>(p, h);
-      const float Mf = fmaxf(M, sk);
-      float f = 0.f, Lf = 0.f;
-      if (Mf != -INFINITY) {
-        const float am = (M == -INFINITY) ? 0.f : ex2(M - Mf);
-        Lf = L * am + ex2(sk - Mf);
-        f = am / Lf;
+#pragma unroll
+      for (int hrow = 0; hrow < 2; ++hrow) {
+        const int r = gid + 8 * hrow;
+        if (!rok[hrow]) continue;
+        const int64_t rho = rc * kRowsDec + r;
+        const int64_t row_global = (b * p.Hq + hkv * p.g + rho / p.Lq) * p.Lq + rho % p.Lq;
+        const float M = m[hrow];
+        if (p.nblk == 1) {
+          const int64_t h = hkv * p.g + rho / p.Lq;
+          const float sk = sink_log2<T>(p, h);
+          const float Mf = fmaxf(M, sk);
+          float f = 0.f, Lf = 0.f;
+          if (Mf != -INFINITY) {
+            const float am = (M == -INFINITY) ? 0.f : ex2(M - Mf);
+            Lf = L[hrow] * am + ex2(sk - Mf);
+            f = am / Lf;
+          }
+          T* orow = reinterpret_cast<T*>(p.out) + row_global * p.dv;
+#pragma unroll
+          for (int j = 0; j < NT; ++j) {
+            const int cc = j * 8 + 2 * tig;
+            if (cc < dv)
+              *reinterpret_cast<uint32_t*>(orow + cc) = MmaOp<T>::pack(o[j][2 * hrow] * f, o[j][2 * hrow + 1] * f);
+          }
+          if (tig == 0 && p.lse) p.lse[row_global] = (Mf == -INFINITY) ? -INFINITY : (Mf + log2f(Lf)) * kLn2;
+        } else {
+          float* po = p.part_o + (row_global * p.nblk + c) * p.dv;
+#pragma unroll
+          for (int j = 0; j < NT; ++j) {
+            const int cc = j * 8 + 2 * tig;
+            if (cc < dv) *reinterpret_cast<float2*>(po + cc) = make_float2(o[j][2 * hrow], o[j][2 * hrow + 1]);
+          }
+          if (tig == 0) {
+            p.part_ml[(row_global * p.nblk + c) * 2 + 0] = M;
+            p.part_ml[(row_global * p.nblk + c) * 2 + 1] = L[hrow];
+          }
+        }
       }
-      T* orow = reinterpret_cast<T*>(p.out) + row_global * p.dv + c4;
-      uint2 v;
-      v.x = MmaOp<T>::pack(acc[0] * f, acc[1] * f);
-      v.y = MmaOp<T>::pack(acc[2] * f, acc[3] * f);
-      *reinterpret_cast<uint2*>(orow) = v;
-      if (c4 == 0 && p.lse) p.lse[row_global] = (Mf == -INFINITY) ? -INFINITY : (Mf + log2f(Lf)) * kLn2;
-    } else {
-      float* po = p.part_o + (row_global * p.nblk + blk) * p.dv + c4;
-      *reinterpret_cast<float4*>(po) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      if (c4 == 0) {
-        p.part_ml[(row_global * p.nblk + blk) * 2 + 0] = M;
-        p.part_ml[(row_global * p.nblk + blk) * 2 + 1] = L;
-      }
+#pragma unroll
+      for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+      m[0] = m[1] = -INFINITY;
+      l[0] = l[1] = 0.f;
     }
   }
+  // a wait that gave up leaves copies in flight: they land before the warp leaves
+  if (lane == 0)
+    for (int i = consumed; i < issued; ++i) mbar_wait(full(i % ST), (i / ST) & 1, kDrainLimitDec, nullptr);
+  __syncwarp();
 }
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -375,12 +378,12 @@ EncodeTiled get_encode_dec() {
   return fn;
 }
 
-bool encode_kv(CUtensorMap* m, int dtype, const void* ptr, int64_t inner, int64_t rows, int64_t outer) {
+bool encode_kv(CUtensorMap* m, int dtype, const void* ptr, int64_t inner, int64_t rows, int64_t outer, int kt) {
   EncodeTiled enc = get_encode_dec();
   if (!enc) return false;
   cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)outer};
   cuuint64_t strides[2] = {(cuuint64_t)(inner * 2), (cuuint64_t)(inner * rows * 2)};
-  cuuint32_t box[3] = {64, (cuuint32_t)kKT, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)kt, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
              const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -389,17 +392,18 @@ bool encode_kv(CUtensorMap* m, int dtype, const void* ptr, int64_t inner, int64_
 }
 
 template <typename T, int DMAX, int DV>
-cudaError_t launch_dec_t(const DecArgs& a, size_t smem, int64_t grid, cudaStream_t st) {
+cudaError_t launch_dec_t(const DecArgs& a, int64_t grid, cudaStream_t st) {
+  using Sh = DecShape<DMAX, DV>;
   static unsigned long long configured = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64 || !(configured >> dev & 1ull)) {
-    e = cudaFuncSetAttribute(sdpa_decode_mma<T, DMAX, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    e = cudaFuncSetAttribute(sdpa_decode_mma<T, DMAX, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
     if (e != cudaSuccess) return e;
     if (dev < 64) configured |= 1ull << dev;
   }
-  sdpa_decode_mma<T, DMAX, DV><<<(unsigned)grid, kDecThreads, smem, st>>>(a);
+  sdpa_decode_mma<T, DMAX, DV><<<(unsigned)grid, Sh::WPC * 32, Sh::kSmem, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -413,15 +417,34 @@ int dec_bucket(int64_t d, int64_t dv) {
   return -1;
 }
 
+struct DecInfo {
+  int wpc, ctas_per_sm, smem, kt;
+};
+template <int DMAX, int DV>
+constexpr DecInfo dec_info_t() {
+  return {DecShape<DMAX, DV>::WPC, DecShape<DMAX, DV>::kCtasPerSm, DecShape<DMAX, DV>::kSmem, DecShape<DMAX, DV>::KT};
+}
+DecInfo dec_info(int64_t d, int64_t dv) {
+  switch (dec_bucket(d, dv)) {
+    case 0: return dec_info_t<64, 64>();
+    case 1: return dec_info_t<128, 64>();
+    case 2: return dec_info_t<128, 128>();
+    case 3: return dec_info_t<192, 128>();
+    case 4: return dec_info_t<192, 192>();
+    case 5: return dec_info_t<256, 256>();
+    default: return {0, 0, 0, 0};
+  }
+}
+
 template <typename T>
-cudaError_t launch_dec_bucket(const DecArgs& a, size_t smem, int64_t grid, cudaStream_t st) {
+cudaError_t launch_dec_bucket(const DecArgs& a, int64_t grid, cudaStream_t st) {
   switch (dec_bucket(a.p.d, a.p.dv)) {
-    case 0: return launch_dec_t<T, 64, 64>(a, smem, grid, st);
-    case 1: return launch_dec_t<T, 128, 64>(a, smem, grid, st);
-    case 2: return launch_dec_t<T, 128, 128>(a, smem, grid, st);
-    case 3: return launch_dec_t<T, 192, 128>(a, smem, grid, st);
-    case 4: return launch_dec_t<T, 192, 192>(a, smem, grid, st);
-    case 5: return launch_dec_t<T, 256, 256>(a, smem, grid, st);
+    case 0: return launch_dec_t<T, 64, 64>(a, grid, st);
+    case 1: return launch_dec_t<T, 128, 64>(a, grid, st);
+    case 2: return launch_dec_t<T, 128, 128>(a, grid, st);
+    case 3: return launch_dec_t<T, 192, 128>(a, grid, st);
+    case 4: return launch_dec_t<T, 192, 192>(a, grid, st);
+    case 5: return launch_dec_t<T, 256, 256>(a, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -432,22 +455,15 @@ bool decode_mma_supported(int dtype, int64_t d, int64_t dv) {
   return (dtype == 1 || dtype == 2) && d % 16 == 0 && dv % 16 == 0 && dec_bucket(d, dv) >= 0;
 }
 
-int64_t decode_mma_rows_per_cta() { return kRowsDec; }
-int64_t decode_mma_key_tile() { return kKT; }
-int decode_mma_ctas_per_sm(int64_t d, int64_t dv) {
-  const int bk = dec_bucket(d, dv);
-  return (bk >= 0 && kDecBuckets[bk][0] <= 128 && kDecBuckets[bk][1] <= 128 &&
-          decode_mma_smem_bytes(d, dv) <= 113 * 1024) ? 2 : 1;
-}
+int64_t decode_mma_rows_per_warp() { return kRowsDec; }
+int64_t decode_mma_key_tile() { return kKTMax; }
+int decode_mma_warps_per_cta(int64_t d, int64_t dv) { return dec_info(d, dv).wpc; }
+int decode_mma_ctas_per_sm(int64_t d, int64_t dv) { return dec_info(d, dv).ctas_per_sm; }
+size_t decode_mma_smem_bytes(int64_t d, int64_t dv) { return (size_t)dec_info(d, dv).smem; }
 
-size_t decode_mma_smem_bytes(int64_t d, int64_t dv) {
-  const int64_t dp = (d + 63) / 64, dvp = (dv + 63) / 64;
-  const int bk = dec_bucket(d, dv);
-  const int64_t dvt = bk >= 0 ? kDecBuckets[bk][1] : 256;
-  int64_t ring = kDecStages * (dp + dvp) * kKT * 128;
-  const int64_t merge = kWarpsC * (2 * kRowsDec + kRowsDec * dvt) * 4;
-  if (merge > ring) ring = merge;
-  return (size_t)(ring + 1024 + 64);
+int64_t decode_mma_grid(int64_t warp_units, int64_t d, int64_t dv) {
+  const int wpc = dec_info(d, dv).wpc;
+  return wpc ? (warp_units + wpc - 1) / wpc : 0;
 }
 
 cudaError_t launch_decode_mma(int dtype, const Params& p, cudaStream_t st) {
@@ -455,14 +471,17 @@ cudaError_t launch_decode_mma(int dtype, const Params& p, cudaStream_t st) {
   memset(&a, 0, sizeof(a));
   a.p = p;
   const int64_t BH = p.B * p.Hkv;
-  if (!encode_kv(&a.tmk, dtype, p.k, p.d, p.Lk, BH) || !encode_kv(&a.tmv, dtype, p.v, p.dv, p.Lk, BH))
+  const int kt = dec_info(p.d, p.dv).kt;
+  if (!kt || !encode_kv(&a.tmk, dtype, p.k, p.d, p.Lk, BH, kt) || !encode_kv(&a.tmv, dtype, p.v, p.dv, p.Lk, BH, kt))
     return cudaErrorInvalidValue;
   a.n_rc = (int)((p.G + kRowsDec - 1) / kRowsDec);
   a.dpanels = (int)((p.d + 63) / 64);
   a.dvpanels = (int)((p.dv + 63) / 64);
-  const int64_t grid = BH * p.nblk * a.n_rc;
-  const size_t smem = decode_mma_smem_bytes(p.d, p.dv);
-  return dtype == 1 ? launch_dec_bucket<__half>(a, smem, grid, st) : launch_dec_bucket<__nv_bfloat16>(a, smem, grid, st);
+  // every warp walks whole key blocks: a block size that is not a whole number of tiles,
+  // or a run count outside [1, blocks], is a planner error
+  if (p.spans < 1 || p.spans > p.nblk || p.keys_per_blk % kt != 0) return cudaErrorInvalidValue;
+  const int64_t grid = decode_mma_grid(BH * a.n_rc * p.spans, p.d, p.dv);
+  return dtype == 1 ? launch_dec_bucket<__half>(a, grid, st) : launch_dec_bucket<__nv_bfloat16>(a, grid, st);
 }
 
 }  // namespace nvsdpa

@@ -30,10 +30,12 @@ cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, c
 
 // decode_mma.cu
 bool decode_mma_supported(int dtype, int64_t d, int64_t dv);
-int64_t decode_mma_rows_per_cta();
+int64_t decode_mma_rows_per_warp();
 int64_t decode_mma_key_tile();
 size_t decode_mma_smem_bytes(int64_t d, int64_t dv);
 int decode_mma_ctas_per_sm(int64_t d, int64_t dv);
+int decode_mma_warps_per_cta(int64_t d, int64_t dv);
+int64_t decode_mma_grid(int64_t warp_units, int64_t d, int64_t dv);
 cudaError_t launch_decode_mma(int dtype, const Params& p, cudaStream_t st);
 
 }  // namespace nvsdpa

@@ -124,6 +124,21 @@ def test_decode_scratch_is_small_next_to_the_keys(nv):
     assert pl["nblk"] * pl["keys_per_blk"] >= Lk > (pl["nblk"] - 1) * pl["keys_per_blk"]
 
 
+def test_decode_grid_is_one_wave_and_splits_only_by_shape(nv):
+    """The decode kernel's warps (8 per CTA, one CTA per SM of 152 for d = dv = 128) run as
+    one wave for any batch size, each walking a run of key blocks; the blocks themselves
+    depend on the head shape and Lk only."""
+    wpc, warp_slots = 8, 8 * 152
+    for B in (1, 2, 8, 64):
+        st, pl = plan(nv, (B, 32, 4, 1, 32769, 128, 128), "causal", 1, "f16")
+        assert st == 0 and pl["path"] == "decode" and pl["kernel"] == "decode_mma"
+        assert (pl["nblk"], pl["keys_per_blk"]) == (74, 448)
+        units = B * 4
+        spans = min(pl["nblk"], max(1, warp_slots // units))
+        assert pl["grid"] == -(-units * spans // wpc)
+        assert pl["grid"] <= max(152, -(-units // wpc))
+
+
 # ----------------------------------------------------------------------------- entry points
 
 def test_nv_sdpa_rejects_before_touching_a_device(nv):

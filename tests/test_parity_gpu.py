@@ -141,6 +141,30 @@ def test_batch_items_equal_each_item_alone(lq, lk, dt):
         assert torch.equal(allb[b:b + 1].view(torch.int16), one.view(torch.int16)), b
 
 
+def test_decode_items_keep_their_bits_when_ctas_take_runs_of_key_blocks():
+    """The decode grid follows the batch size (one wave of CTAs, each walking a run of key
+    blocks) while the key blocks do not: in an 8-item batch a CTA takes several blocks,
+    alone one, and the item's output and log-sum-exp keep every bit."""
+    import torch
+    nv = ensure_built()
+    c = W.decode_f16_long_kv()
+    shape = (c.B, c.Hq, c.Hkv, c.Lq, c.Lk, c.d, c.dv)
+    _, pl_b = nv.nv_sdpa_plan(shape, 1, 1, 1)
+    _, pl_1 = nv.nv_sdpa_plan((1,) + shape[1:], 1, 1, 1)
+    assert (pl_b["nblk"], pl_b["keys_per_blk"]) == (pl_1["nblk"], pl_1["keys_per_blk"])
+    assert pl_b["grid"] < c.B * pl_1["grid"]  # CTAs of the batch walk runs of blocks
+    x = W.make_inputs(c)
+    dev = upload(c, x)
+    allb, all_lse = nv.sdpa(dev["q"], dev["k"], dev["v"], mask_kind=c.mask, scale=c.scale_f32,
+                            sinks=dev["sinks"])
+    for b in (0, 3, c.B - 1):
+        one, one_lse = nv.sdpa(dev["q"][b:b + 1].contiguous(), dev["k"][b:b + 1].contiguous(),
+                               dev["v"][b:b + 1].contiguous(), mask_kind=c.mask, scale=c.scale_f32,
+                               sinks=dev["sinks"])
+        assert torch.equal(allb[b:b + 1].view(torch.int16), one.view(torch.int16)), b
+        assert torch.equal(all_lse[b:b + 1], one_lse), b
+
+
 def test_run_to_run_deterministic():
     import torch
     nv = ensure_built()
