@@ -95,11 +95,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   return false;
 }
 
-// Named barrier `id` (1..15; 0 is __syncthreads') over `count` threads, a multiple of 32.
-__device__ __forceinline__ void named_bar_sync(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 // ----------------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* desc) {
