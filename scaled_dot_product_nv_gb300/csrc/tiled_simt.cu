@@ -207,7 +207,7 @@ sdpa_tiled_simt(const Params p) {
 // griddepcontrol.wait holds it until pass 1 has finished and its writes are visible.
 constexpr int kMergeWarps = 8;
 constexpr int kMaxBlk = 1024;
-constexpr int kMergeBatch = 8;  // blocks per warp whose loads are in flight together
+constexpr int kMergeBatch = 12;  // blocks per warp whose loads are in flight together
 
 template <typename T>
 __global__ void __launch_bounds__(kMergeWarps * 32)
@@ -221,10 +221,29 @@ sdpa_merge_partials(const Params p) {
   const int nb = (int)p.nblk;
   const int dv = (int)p.dv;
   const float* ml = p.part_ml + row * p.nblk * 2;
+  const float* po = p.part_o + row * p.nblk * p.dv;
   const float sk = sink_log2<T>(p, h);
-  // M over every block's max (and the sink)
+
+  // Warp w takes blocks w, w + 8, w + 16, ... and lane l columns 4 l .. 4 l + 3 of each
+  // 128-column group; a batch is kMergeBatch such blocks, loaded together.
+  float mk[kMergeBatch], lk[kMergeBatch];
+  float4 o[kMergeBatch];
+  auto load_batch = [&](int k0, int c0) {
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) {
+      const int k = k0 + u * kMergeWarps;
+      const bool in = k < nb;
+      mk[u] = in ? ml[2 * k] : -INFINITY;
+      lk[u] = in ? ml[2 * k + 1] : 0.f;
+      o[u] = (in && c0 < dv) ? *reinterpret_cast<const float4*>(po + (int64_t)k * p.dv + c0)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  // The first batch and this thread's share of the block maxima are loaded before any
+  // of them is used: up to 8 x kMergeBatch blocks cost one trip to memory.
   float M = sk;
   for (int k = threadIdx.x; k < nb; k += kMergeWarps * 32) M = fmaxf(M, ml[2 * k]);
+  load_batch(warp, lane * 4);
 #pragma unroll
   for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   if (lane == 0) red[warp] = M;
@@ -237,21 +256,11 @@ sdpa_merge_partials(const Params p) {
     if (threadIdx.x == 0 && p.lse) p.lse[row] = -INFINITY;
     return;
   }
-  const float* po = p.part_o + row * p.nblk * p.dv;
   float L = 0.f;
   for (int c0 = lane * 4; c0 < dv; c0 += 128) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int k0 = warp; k0 < nb; k0 += kMergeWarps * kMergeBatch) {
-      float mk[kMergeBatch], lk[kMergeBatch];
-      float4 o[kMergeBatch];
-#pragma unroll
-      for (int u = 0; u < kMergeBatch; ++u) {
-        const int k = k0 + u * kMergeWarps;
-        const bool in = k < nb;
-        mk[u] = in ? ml[2 * k] : -INFINITY;
-        lk[u] = in ? ml[2 * k + 1] : 0.f;
-        o[u] = in ? *reinterpret_cast<const float4*>(po + (int64_t)k * p.dv + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+      if (c0 != lane * 4 || k0 != warp) load_batch(k0, c0);
 #pragma unroll
       for (int u = 0; u < kMergeBatch; ++u) {
         const float w = (mk[u] == -INFINITY) ? 0.f : ex2(mk[u] - M);
