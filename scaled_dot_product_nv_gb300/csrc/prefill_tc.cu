@@ -63,9 +63,12 @@ struct TcArgs {
 };
 
 // barrier slots
+// (NQ = 2: K and V of a stage land on kv_full and are released together; NQ = 1: K on
+// kv_full / kv_empty, V on v_full / v_empty, each released as soon as its last reader
+// is done)
 enum { kBarQ = 0, kBarKvFull = 1, kBarKvEmpty = 1 + kStages, kBarSFull = 1 + 2 * kStages,
        kBarPFull = 3 + 2 * kStages, kBarPvDone = 5 + 2 * kStages, kBarDrain = 7 + 2 * kStages,
-       kNumBars = 8 + 2 * kStages };
+       kBarVFull = 8 + 2 * kStages, kBarVEmpty = 8 + 3 * kStages, kNumBars = 8 + 4 * kStages };
 
 __device__ __forceinline__ void fail(const Params& p, volatile int* abort, uint32_t bit) {
   *abort = 1;
@@ -103,12 +106,15 @@ __device__ __forceinline__ int tiles_for_rows(const Params& p, int64_t r0) {
 }
 
 // One query row's softmax step on key tile t.  tS / tO: TMEM addresses (lane base
-// included) of this tile's S columns and of O.  Returns false if a wait gave up.
-template <typename T, int BN>
+// included) of this tile's S columns and of O; mrow: this row's bit-packed mask words
+// (or null).  PF: the tile's words were loaded ahead by the caller into mw.  Returns
+// false if a wait gave up.
+template <typename T, int BN, bool PF>
 __device__ __forceinline__ bool softmax_tile(const TcArgs& a, int t, uint32_t tS, uint32_t tO,
                                              bool row_ok, int64_t last_key, const uint32_t* mrow,
-                                             float& m_run, float& l_run, uint32_t pv_bar, bool wait_pv,
-                                             uint64_t limit, volatile int* abort) {
+                                             const uint32_t (&mw)[BN / 32], float& m_run, float& l_run,
+                                             uint32_t pv_bar, bool wait_pv, uint64_t limit,
+                                             volatile int* abort) {
   const Params& p = a.p;
   uint32_t sr[BN];
   if constexpr (BN == 128) tmem_ld128_sync(tS, sr);
@@ -166,7 +172,7 @@ __device__ __forceinline__ bool softmax_tile(const TcArgs& a, int t, uint32_t tS
 #pragma unroll
     for (int c = 0; c < BN / 32; ++c) {
       uint32_t bits = 0xffffffffu;
-      if (mrow) bits = row_ok ? __ldg(mrow + j0 / 32 + c) : 0u;
+      if (mrow) bits = PF ? mw[c] : (row_ok ? __ldg(mrow + j0 / 32 + c) : 0u);
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
         const int col = c * 32 + e;
@@ -318,6 +324,8 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(kBarKvFull + s), 1);
       mbar_init(bar(kBarKvEmpty + s), 1);
+      mbar_init(bar(kBarVFull + s), 1);
+      mbar_init(bar(kBarVEmpty + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(kBarSFull + b), 1);
@@ -353,24 +361,58 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
         for (int pn = 0; pn < a.dpanels; ++pn)
           tma_load_3d(sQ + q * q_bytes + pn * kBM * 128, &a.tmq, bar(kBarQ), pn * 64,
                       (int)((rb * NQ + q) * kBM), (int)bh);
-      int issued = 0;
-      for (int t = 0; t < n_max; ++t) {
+      // one ring slot: wait until its previous tile is released, then load tile t into it
+      auto load = [&](int full, int empty, uint32_t ring, uint32_t bytes, const CUtensorMap* tm1, int panels1,
+                      uint32_t ring2, const CUtensorMap* tm2, int panels2, int t) {
         const int s = t % kStages;
-        if (!mbar_wait(bar(kBarKvEmpty + s), ((t / kStages) & 1) ^ 1, limit, abort)) {
+        if (!mbar_wait(bar(empty + s), ((t / kStages) & 1) ^ 1, limit, abort)) {
           fail(p, abort, kStatTimeoutSlotFree);
-          break;
+          return false;
         }
-        mbar_arrive_expect_tx(bar(kBarKvFull + s), k_bytes + v_bytes);
-        for (int pn = 0; pn < a.dpanels; ++pn)
-          tma_load_3d(sK + s * k_bytes + pn * BN * 128, &a.tmk, bar(kBarKvFull + s), pn * 64, t * BN, (int)bh);
-        for (int pn = 0; pn < a.dvpanels; ++pn)
-          tma_load_3d(sV + s * v_bytes + pn * BN * 128, &a.tmv, bar(kBarKvFull + s), pn * 64, t * BN, (int)bh);
-        issued = t + 1;
+        mbar_arrive_expect_tx(bar(full + s), bytes);
+        for (int pn = 0; pn < panels1; ++pn)
+          tma_load_3d(ring + s * (panels1 * BN * 128) + pn * BN * 128, tm1, bar(full + s), pn * 64, t * BN, (int)bh);
+        for (int pn = 0; pn < panels2; ++pn)
+          tma_load_3d(ring2 + s * (panels2 * BN * 128) + pn * BN * 128, tm2, bar(full + s), pn * 64, t * BN, (int)bh);
+        return true;
+      };
+      int k_issued = 0, v_issued = 0;
+      if constexpr (NQ == 2) {
+        // K and V of tile t together into stage t % kStages
+        for (int t = 0; t < n_max; ++t) {
+          const int s = t % kStages;
+          if (!mbar_wait(bar(kBarKvEmpty + s), ((t / kStages) & 1) ^ 1, limit, abort)) {
+            fail(p, abort, kStatTimeoutSlotFree);
+            break;
+          }
+          mbar_arrive_expect_tx(bar(kBarKvFull + s), k_bytes + v_bytes);
+          for (int pn = 0; pn < a.dpanels; ++pn)
+            tma_load_3d(sK + s * k_bytes + pn * BN * 128, &a.tmk, bar(kBarKvFull + s), pn * 64, t * BN, (int)bh);
+          for (int pn = 0; pn < a.dvpanels; ++pn)
+            tma_load_3d(sV + s * v_bytes + pn * BN * 128, &a.tmv, bar(kBarKvFull + s), pn * 64, t * BN, (int)bh);
+          k_issued = v_issued = t + 1;
+        }
+      } else {
+        // K runs one tile ahead of V (S of tile t + 1 is issued before P V of tile t)
+        if (load(kBarKvFull, kBarKvEmpty, sK, k_bytes, &a.tmk, a.dpanels, sV, &a.tmv, 0, 0)) {
+          k_issued = 1;
+          for (int t = 0; t < n_max; ++t) {
+            if (t + 1 < n_max) {
+              if (!load(kBarKvFull, kBarKvEmpty, sK, k_bytes, &a.tmk, a.dpanels, sV, &a.tmv, 0, t + 1)) break;
+              k_issued = t + 2;
+            }
+            if (!load(kBarVFull, kBarVEmpty, sV, v_bytes, &a.tmv, a.dvpanels, sK, &a.tmk, 0, t)) break;
+            v_issued = t + 1;
+          }
+        }
       }
       // Every copy issued must land before the CTA may exit (a no-op when all were consumed).
       mbar_wait(bar(kBarQ), 0, kDrainLimit, nullptr);
-      for (int t = issued > kStages ? issued - kStages : 0; t < issued; ++t)
+      for (int t = k_issued > kStages ? k_issued - kStages : 0; t < k_issued; ++t)
         mbar_wait(bar(kBarKvFull + t % kStages), (t / kStages) & 1, kDrainLimit, nullptr);
+      if constexpr (NQ == 1)
+        for (int t = v_issued > kStages ? v_issued - kStages : 0; t < v_issued; ++t)
+          mbar_wait(bar(kBarVFull + t % kStages), (t / kStages) & 1, kDrainLimit, nullptr);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -434,15 +476,29 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
       if (!ok) fail(p, abort, kStatTimeoutTmaFull);
       ok = ok && wait_kv(0);
       if constexpr (NQ == 1) {
-        if (ok) issue_s(0, 0, 0);
+        // K slots are released once their S is done, V slots once their P V is
+        auto wait_v = [&](int t) {
+          if (mbar_wait<false>(bar(kBarVFull + t % kStages), (t / kStages) & 1, limit, abort)) {
+            tc_fence_after();
+            return true;
+          }
+          fail(p, abort, kStatTimeoutTmaFull);
+          return false;
+        };
+        if (ok) {
+          issue_s(0, 0, 0);
+          mma_commit(bar(kBarKvEmpty));
+        }
         for (int t = 0; ok && t < n_max; ++t) {
           if (t + 1 < n_max) {
             if (!(ok = wait_kv(t + 1))) break;
             issue_s(t + 1, 0, (t + 1) & 1);
+            mma_commit(bar(kBarKvEmpty + (t + 1) % kStages));
           }
           if (!(ok = wait_p(t & 1, (t >> 1) & 1))) break;
+          if (!(ok = wait_v(t))) break;
           issue_pv(t, 0, t & 1);
-          mma_commit(bar(kBarKvEmpty + t % kStages));
+          mma_commit(bar(kBarVEmpty + t % kStages));
         }
       } else {
         if (ok) {
@@ -486,26 +542,58 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
     const uint32_t tO = tmem + lane_base + tO_col(q);
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int t = 0; t < n_tiles; ++t) {
-      const int slot = (NQ == 1) ? (t & 1) : q;
-      const uint32_t par = (NQ == 1) ? ((t >> 1) & 1) : (t & 1);
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull + slot), par, limit, abort));
-      if (!ok) {
-        fail(p, abort, kStatTimeoutMma);
-        break;
+    if constexpr (NQ == 2) {
+      uint32_t no_words[BN / 32];  // (the mask words are loaded inside the softmax)
+      for (int t = 0; t < n_tiles; ++t) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull + q), t & 1, limit, abort));
+        if (!ok) {
+          fail(p, abort, kStatTimeoutMma);
+          break;
+        }
+        tc_fence_after();
+        // S of this tile was issued after P_{t-1} V_{t-1} of the same Q tile, and a commit
+        // tracks every earlier MMA of the issuing thread, so s_full already implies that O
+        // holds P_{t-1} V_{t-1}
+        ok = softmax_tile<T, BN, false>(a, t, tmem + lane_base + tS_col(q), tO, row_ok, last_key, mrow, no_words,
+                                        m_run, l_run, bar(kBarPvDone + q), false, limit, abort);
+        if (!ok) {
+          fail(p, abort, kStatTimeoutMma);
+          break;
+        }
+        tc_fence_before();
+        mbar_arrive(bar(kBarPFull + q));
       }
-      tc_fence_after();
-      // NQ = 2: S of this tile was issued after P_{t-1} V_{t-1} of the same Q tile, and a
-      // commit tracks every earlier MMA of the issuing thread, so s_full already implies
-      // that O holds P_{t-1} V_{t-1}; NQ = 1 issues S_{t} before P_{t-1} V_{t-1} and waits.
-      ok = softmax_tile<T, BN>(a, t, tmem + lane_base + tS_col(slot), tO, row_ok, last_key, mrow, m_run,
-                               l_run, bar(kBarPvDone + q), NQ == 1, limit, abort);
-      if (!ok) {
-        fail(p, abort, kStatTimeoutMma);
-        break;
+    } else {
+      // this row's bit-packed mask words of a key tile, loaded one tile ahead so that the
+      // global-memory latency falls in the wait for S rather than in the softmax
+      uint32_t mw[BN / 32];
+      auto load_mw = [&](int t, uint32_t (&dst)[BN / 32]) {
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) dst[c] = (mrow && row_ok) ? __ldg(mrow + (t * BN) / 32 + c) : 0u;
+      };
+      if (n_tiles > 0) load_mw(0, mw);
+      for (int t = 0; t < n_tiles; ++t) {
+        uint32_t mw_next[BN / 32];
+        if (t + 1 < n_tiles) load_mw(t + 1, mw_next);
+        const int slot = t & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull + slot), (t >> 1) & 1, limit, abort));
+        if (!ok) {
+          fail(p, abort, kStatTimeoutMma);
+          break;
+        }
+        tc_fence_after();
+        // S_t was issued before P_{t-1} V_{t-1}: the softmax waits for that product
+        ok = softmax_tile<T, BN, true>(a, t, tmem + lane_base + tS_col(slot), tO, row_ok, last_key, mrow, mw,
+                                       m_run, l_run, bar(kBarPvDone + q), true, limit, abort);
+        if (!ok) {
+          fail(p, abort, kStatTimeoutMma);
+          break;
+        }
+        tc_fence_before();
+        mbar_arrive(bar(kBarPFull + slot));
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) mw[c] = mw_next[c];
       }
-      tc_fence_before();
-      mbar_arrive(bar(kBarPFull + slot));
     }
     // ---- epilogue
     if (ok && n_tiles > 0) {

@@ -76,21 +76,19 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 template <bool kSleep = true>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit,
                                           const volatile int* abort) {
-  if (limit < 64) {
-    for (uint64_t i = 0; i < limit; ++i)
-      if (mbar_test_wait(bar, parity)) return true;
-    return false;
-  }
-  if (kSleep) {
+  if (kSleep && limit >= 64) {
     for (uint64_t i = 0; i < limit; ++i) {
       if (mbar_try_wait(bar, parity)) return true;
       if ((i & 7) == 7 && abort && *abort) return false;
     }
-  } else {
-    for (uint64_t i = 0; i < limit * 64; ++i) {
-      if (mbar_test_wait(bar, parity)) return true;
-      if ((i & 63) == 63 && abort && *abort) return false;
-    }
+    return false;
+  }
+  // one plain loop (its shape matters in the MMA issuer: a branchier wait measurably
+  // slows the tensor pipe it feeds)
+  const uint64_t n = (kSleep || limit < 64) ? limit : limit * 64;
+  for (uint64_t i = 0; i < n; ++i) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((i & 63) == 63 && abort && *abort) return false;
   }
   return false;
 }
