@@ -51,6 +51,7 @@ constexpr int64_t kTcMaxSmem = 227 * 1024;  // opt-in dynamic shared memory per 
 
 struct TcArgs {
   CUtensorMap tmq, tmk, tmv;  // 64-byte aligned by type
+  CUtensorMap tmo;            // the output, for TMA stores of whole tiles (when tma_out)
   Params p;
   const uint32_t* mask_bits;  // [Lq][mask_words], bit j%32 of word j/32 = key j visible
   int64_t mask_words;
@@ -60,6 +61,7 @@ struct TcArgs {
   int ksteps_qk;     // ceil(d / 16)
   int n_pv;          // dv rounded up to 16 (MMA N of P V)
   int itile_order;   // Lq % (NQ x 128) == 0: launch the late (heavier, causal) blocks first
+  int tma_out;       // the output tile fits the Q tile's shared memory: store it by TMA
 };
 
 // barrier slots
@@ -266,6 +268,48 @@ __device__ __forceinline__ void epilogue_row(const Params& p, uint32_t tO, bool 
           v.w = pack2<T>(__uint_as_float(o[e8 * 8 + 6]) * f, __uint_as_float(o[e8 * 8 + 7]) * f);
           *reinterpret_cast<uint4*>(orow + col) = v;
         }
+      }
+    }
+  }
+  if (row_ok && p.lse) p.lse[out_row] = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
+}
+
+// The same, for a TMA store of the whole tile: the row is written (scaled and rounded)
+// into `stage`, the tile's shared-memory image in the 128-byte-swizzled layout of the
+// loads (64-column panels of 128 rows x 128 B, 16-byte chunk c of row r at
+// (c ^ (r mod 8)) * 16); the log-sum-exp is written directly.
+template <typename T>
+__device__ __forceinline__ void epilogue_row_smem(const Params& p, uint32_t tO, bool have_o, bool row_ok,
+                                                  int64_t out_row, int64_t h, float m_run, float l_run,
+                                                  uint8_t* stage, int r) {
+  const float sk = sink_log2<T>(p, h);
+  const float M = fmaxf(m_run, sk);
+  float f = 0.f, L = 0.f;
+  if (M != -INFINITY) {
+    const float am = ex2(m_run - M);
+    L = l_run * am + ex2(sk - M);
+    f = am / L;
+  }
+  const int dv = (int)p.dv;
+  for (int c0 = 0; c0 < dv; c0 += 128) {
+    uint32_t o[128];
+    if (have_o) {
+      tmem_ld128_sync(tO + c0, o);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 128; ++e) o[e] = 0u;
+    }
+#pragma unroll
+    for (int e8 = 0; e8 < 16; ++e8) {
+      const int col = c0 + e8 * 8;
+      if (col < dv) {
+        uint4 v;
+        v.x = pack2<T>(__uint_as_float(o[e8 * 8 + 0]) * f, __uint_as_float(o[e8 * 8 + 1]) * f);
+        v.y = pack2<T>(__uint_as_float(o[e8 * 8 + 2]) * f, __uint_as_float(o[e8 * 8 + 3]) * f);
+        v.z = pack2<T>(__uint_as_float(o[e8 * 8 + 4]) * f, __uint_as_float(o[e8 * 8 + 5]) * f);
+        v.w = pack2<T>(__uint_as_float(o[e8 * 8 + 6]) * f, __uint_as_float(o[e8 * 8 + 7]) * f);
+        const int pn = col >> 6, c = (col >> 3) & 7;
+        *reinterpret_cast<uint4*>(stage + pn * (kBM * 128) + r * 128 + ((c ^ (r & 7)) << 4)) = v;
       }
     }
   }
@@ -602,7 +646,25 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
       tc_fence_after();
     }
     ok = __all_sync(0xffffffffu, ok && !*abort);
-    if (ok) epilogue_row<T>(p, tO, n_tiles > 0, row_ok, bh * p.G + rho, h, m_run, l_run);
+    if (a.tma_out) {
+      // The tile goes out through shared memory and one TMA store per panel: the row
+      // stores of a warp would touch 32 rows each, and a CTA could not retire before
+      // they drained.  The stage is this Q tile's buffer, unread since its last S
+      // product completed (before the last P V that the wait above saw done).  Every
+      // thread of the warpgroup reaches the barrier, whatever happened before it.
+      uint8_t* stage = base + q * q_bytes;
+      if (ok) epilogue_row_smem<T>(p, tO, n_tiles > 0, row_ok, bh * p.G + rho, h, m_run, l_run, stage, row);
+      fence_proxy_async_smem();
+      const bool all_ok = bar_and(1 + q, 128, ok);
+      if (all_ok && warp == 2 + 4 * q && lane == 0) {
+        for (int pn = 0; pn < a.dvpanels; ++pn)
+          tma_store_3d(&a.tmo, smem_addr(stage + pn * (kBM * 128)), pn * 64, (int)((rb * NQ + q) * kBM), (int)bh);
+        bulk_commit_group();
+        bulk_wait_read_all();  // the stage must stay intact until the copy has read it
+      }
+    } else if (ok) {
+      epilogue_row<T>(p, tO, n_tiles > 0, row_ok, bh * p.G + rho, h, m_run, l_run);
+    }
   }
 
   // ---- tear-down
@@ -746,6 +808,8 @@ cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, c
   if (!encode_3d(&a.tmq, dtype, p.q, p.d, p.G, BH, kBM) || !encode_3d(&a.tmk, dtype, p.k, p.d, p.Lk, BH, bn) ||
       !encode_3d(&a.tmv, dtype, p.v, p.dv, p.Lk, BH, bn))
     return cudaErrorInvalidValue;
+  // the output as [B*Hkv][G][dv]: the rows of one KV head are contiguous, as for Q
+  a.tma_out = ((p.dv + 63) / 64 <= (p.d + 63) / 64 && encode_3d(&a.tmo, dtype, p.out, p.dv, p.G, BH, kBM)) ? 1 : 0;
   a.n_rt = (int)((p.G + kBM * nq - 1) / (kBM * nq));
   a.dpanels = (int)((p.d + 63) / 64);
   a.dvpanels = (int)((p.dv + 63) / 64);
