@@ -120,6 +120,16 @@ def test_extreme_scores_stay_finite(dt):
     check_case(c)
 
 
+@pytest.mark.parametrize("d,dv", [(64, 128), (128, 64), (64, 256), (256, 64), (136, 136)])
+@pytest.mark.parametrize("lq", [1, 300])
+def test_head_pairs_beyond_the_listed_ones(d, dv, lq):
+    """Head pairs the ABI accepts beyond the pages' list.  An output tile wider than the Q
+    tile (dv > d) leaves the prefill by direct row stores instead of the TMA store; a
+    136-wide head needs a ninth K-step and a third, partly filled 64-column panel."""
+    c = W.Case(2, 8, 2, lq, 777, d, dv, "bf16", "causal", True, None, "n0.5", seed=15)
+    check_case(c, name=f"d{d}x{dv}_lq{lq}")
+
+
 # ----------------------------------------------------------------------------- invariants
 
 @pytest.mark.parametrize("lq,lk", [(300, 300), (1, 8193), (9, 777)])
