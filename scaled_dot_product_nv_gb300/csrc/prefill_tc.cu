@@ -8,6 +8,9 @@
 //
 // * One CTA owns NQ x 128 query rows of one KV head (rows of the g query heads sharing
 //   it, head-major -- contiguous in memory) and walks their visible key tiles of BN keys.
+//   With two Q tiles these are, where the shape allows, the same 128 positions of two
+//   query heads: both tiles then see the same key tiles, and under the causal mask
+//   neither waits out the other's extra diagonal tile alone.
 // * Warp 0 (one lane) streams the Q tile(s) once and K/V tiles through a 2-stage ring
 //   with 3-D TMA (128-byte swizzle, zero fill out of range); completion on mbarriers.
 // * Warp 1 allocates the 512 TMEM columns; one lane issues every tcgen05.mma:
@@ -61,6 +64,8 @@ struct TcArgs {
   int ksteps_qk;     // ceil(d / 16)
   int n_pv;          // dv rounded up to 16 (MMA N of P V)
   int itile_order;   // Lq % (NQ x 128) == 0: launch the late (heavier, causal) blocks first
+  int head_pairs;    // NQ = 2, g even, Lq % 128 == 0: the two Q tiles are the same positions
+                     // of two query heads (equal key extents), late positions first
   int tma_out;       // the output tile fits the Q tile's shared memory: store it by TMA
 };
 
@@ -340,24 +345,38 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_holder + 1);
   auto bar = [&](int i) { return smem_addr(bars + i); };
 
-  // ---- which rows and keys this CTA owns
+  // ---- which rows and keys this CTA owns: (b, kv head) and the first of the 128 rows
+  // (among the G rows of that KV head) of each Q tile
   const int64_t BH = p.B * p.Hkv;
-  int64_t rb, bh;  // row block (NQ x 128 rows) and (b, kv head)
-  if (a.itile_order) {
-    const int64_t ipt = p.Lq / (kBM * NQ);  // row blocks per head
+  int64_t bh, row0[NQ];
+  if (NQ == 2 && a.head_pairs) {
+    const int64_t hp = p.g / 2, kpt = p.Lq / kBM;
     int64_t x = blockIdx.x;
-    const int64_t hh = x % p.g; x /= p.g;
+    const int64_t pr = x % hp; x /= hp;
     bh = x % BH;
-    const int64_t it = ipt - 1 - x / BH;
-    rb = hh * ipt + it;
+    const int64_t k = kpt - 1 - x / BH;
+    row0[0] = 2 * pr * p.Lq + k * kBM;
+    row0[NQ - 1] = row0[0] + p.Lq;
   } else {
-    rb = blockIdx.x % a.n_rt;
-    bh = blockIdx.x / a.n_rt;
+    int64_t rb;  // row block of NQ x 128 consecutive rows
+    if (a.itile_order) {
+      const int64_t ipt = p.Lq / (kBM * NQ);  // row blocks per head
+      int64_t x = blockIdx.x;
+      const int64_t hh = x % p.g; x /= p.g;
+      bh = x % BH;
+      const int64_t it = ipt - 1 - x / BH;
+      rb = hh * ipt + it;
+    } else {
+      rb = blockIdx.x % a.n_rt;
+      bh = blockIdx.x / a.n_rt;
+    }
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) row0[q] = (rb * NQ + q) * kBM;
   }
   const int64_t hkv = bh % p.Hkv;
   int n_q[NQ];
 #pragma unroll
-  for (int q = 0; q < NQ; ++q) n_q[q] = tiles_for_rows<BN>(p, (rb * NQ + q) * kBM);
+  for (int q = 0; q < NQ; ++q) n_q[q] = tiles_for_rows<BN>(p, row0[q]);
   int n_max = 0;
 #pragma unroll
   for (int q = 0; q < NQ; ++q) n_max = n_q[q] > n_max ? n_q[q] : n_max;
@@ -400,11 +419,16 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
       tma_prefetch_desc(&a.tmq);
       tma_prefetch_desc(&a.tmk);
       tma_prefetch_desc(&a.tmv);
-      mbar_arrive_expect_tx(bar(kBarQ), NQ * q_bytes);
+      // Only Q tiles that see a key are loaded: the epilogue of a tile that sees none
+      // stages its zeros in that tile's buffer, which no copy may still be filling.
+      uint32_t q_tx = 0;
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) q_tx += n_q[q] > 0 ? q_bytes : 0u;
+      mbar_arrive_expect_tx(bar(kBarQ), q_tx);
       for (int q = 0; q < NQ; ++q)
-        for (int pn = 0; pn < a.dpanels; ++pn)
-          tma_load_3d(sQ + q * q_bytes + pn * kBM * 128, &a.tmq, bar(kBarQ), pn * 64,
-                      (int)((rb * NQ + q) * kBM), (int)bh);
+        if (n_q[q] > 0)
+          for (int pn = 0; pn < a.dpanels; ++pn)
+            tma_load_3d(sQ + q * q_bytes + pn * kBM * 128, &a.tmq, bar(kBarQ), pn * 64, (int)row0[q], (int)bh);
       // one ring slot: wait until its previous tile is released, then load tile t into it
       auto load = [&](int full, int empty, uint32_t ring, uint32_t bytes, const CUtensorMap* tm1, int panels1,
                       uint32_t ring2, const CUtensorMap* tm2, int panels2, int t) {
@@ -576,7 +600,7 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
     const int q4 = warp & 3;       // TMEM lane quarter this warp may access
     const int row = q4 * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-    const int64_t rho = (rb * NQ + q) * kBM + row;
+    const int64_t rho = (q == 0 ? row0[0] : row0[NQ - 1]) + row;
     const bool row_ok = rho < p.G;
     const int64_t i = row_ok ? rho % p.Lq : 0;
     const int64_t h = hkv * p.g + (row_ok ? rho / p.Lq : 0);
@@ -650,15 +674,16 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
       // The tile goes out through shared memory and one TMA store per panel: the row
       // stores of a warp would touch 32 rows each, and a CTA could not retire before
       // they drained.  The stage is this Q tile's buffer, unread since its last S
-      // product completed (before the last P V that the wait above saw done).  Every
-      // thread of the warpgroup reaches the barrier, whatever happened before it.
+      // product completed (before the last P V that the wait above saw done), and never
+      // loaded at all when the tile sees no key.  Every thread of the warpgroup reaches
+      // the barrier, whatever happened before it.
       uint8_t* stage = base + q * q_bytes;
       if (ok) epilogue_row_smem<T>(p, tO, n_tiles > 0, row_ok, bh * p.G + rho, h, m_run, l_run, stage, row);
       fence_proxy_async_smem();
       const bool all_ok = bar_and(1 + q, 128, ok);
       if (all_ok && warp == 2 + 4 * q && lane == 0) {
         for (int pn = 0; pn < a.dvpanels; ++pn)
-          tma_store_3d(&a.tmo, smem_addr(stage + pn * (kBM * 128)), pn * 64, (int)((rb * NQ + q) * kBM), (int)bh);
+          tma_store_3d(&a.tmo, smem_addr(stage + pn * (kBM * 128)), pn * 64, (int)(q == 0 ? row0[0] : row0[NQ - 1]), (int)bh);
         bulk_commit_group();
         bulk_wait_read_all();  // the stage must stay intact until the copy has read it
       }
@@ -816,6 +841,7 @@ cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, c
   a.ksteps_qk = (int)((p.d + 15) / 16);
   a.n_pv = (int)((p.dv + 15) / 16 * 16);
   a.itile_order = (p.Lq % (kBM * nq) == 0) ? 1 : 0;
+  a.head_pairs = (nq == 2 && p.g % 2 == 0 && p.Lq % kBM == 0) ? 1 : 0;
   if (p.mask_kind == kMaskBool) {
     a.mask_words = (int64_t)prefill_tc_mask_words(p.Lk);
     a.mask_bits = mask_bits;

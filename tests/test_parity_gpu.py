@@ -130,6 +130,33 @@ def test_head_pairs_beyond_the_listed_ones(d, dv, lq):
     check_case(c, name=f"d{d}x{dv}_lq{lq}")
 
 
+WAVES = [
+    # 352 work tiles of 256 rows (ragged: G = 2600); the first rows see no key at all
+    W.Case(4, 16, 8, 1300, 1000, 64, 64, "bf16", "causal", True, None, "n0.5", seed=21,
+           name="waves_causal_lk_lt_lq_d64"),
+    # 192 tiles of two query heads' rows, heaviest first, boolean mask and sinks
+    W.Case(3, 32, 8, 512, 700, 128, 128, "f16", "bool", True, None, "u2", seed=22,
+           name="waves_bool_sinks_d128"),
+    # 512 tiles of two query heads' rows, no mask, a head pair with dv < d
+    W.Case(2, 32, 8, 2048, 2048, 96, 64, "bf16", "none", False, None, "u0.25", seed=23,
+           name="waves_none_d96x64"),
+    # an odd group (g = 3): 192 tiles of 256 consecutive rows, some across two heads
+    W.Case(6, 12, 4, 640, 900, 128, 128, "bf16", "causal", True, None, "n0.5", seed=24,
+           name="waves_causal_odd_group_d128"),
+]
+
+
+@pytest.mark.parametrize("case", WAVES, ids=[c.name for c in WAVES])
+def test_prefill_more_work_tiles_than_sms(case):
+    """More 256-row work tiles than SMs, so CTAs run in several waves, each tile on
+    whichever SM frees first."""
+    nv = ensure_built()
+    _, pl = nv.nv_sdpa_plan((case.B, case.Hq, case.Hkv, case.Lq, case.Lk, case.d, case.dv),
+                            nv.MASKS[case.mask], int(case.sinks), nv.DTYPES[case.dtype])
+    assert pl["rows_per_cta"] == 256
+    check_case(case)
+
+
 # ----------------------------------------------------------------------------- invariants
 
 @pytest.mark.parametrize("lq,lk", [(300, 300), (1, 8193), (9, 777)])
