@@ -176,17 +176,25 @@ __device__ __forceinline__ bool softmax_tile(const TcArgs& a, int t, uint32_t tS
     l_run = l_run * alpha + ((a0 + a1) + (b0 + b1));
   } else {
     float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
 #pragma unroll
     for (int c = 0; c < BN / 32; ++c) {
       uint32_t bits = 0xffffffffu;
       if (mrow) bits = PF ? mw[c] : (row_ok ? __ldg(mrow + j0 / 32 + c) : 0u);
+      // the visible columns of this word: mask bits, causal / key-count bound, the row
+      const int lim = vis_cols - c * 32;
+      const uint32_t bound = lim >= 32 ? 0xffffffffu : (lim <= 0 ? 0u : (1u << lim) - 1u);
+      const uint32_t vb = row_ok ? (bits & bound) : 0u;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
+      for (int e = 0; e < 32; e += 2) {
         const int col = c * 32 + e;
-        const bool vis = row_ok && col < vis_cols && ((bits >> e) & 1u);
-        const float x = vis ? __uint_as_float(sr[col]) * p.scale_log2 : -INFINITY;
-        sr[col] = __float_as_uint(x);
-        m4[e & 3] = fmaxf(m4[e & 3], x);
+        float x0, x1;
+        f2_unpack(f2_mul(f2_pack(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])), c2), x0, x1);
+        x0 = (vb & (1u << e)) ? x0 : -INFINITY;
+        x1 = (vb & (2u << e)) ? x1 : -INFINITY;
+        sr[col] = __float_as_uint(x0);
+        sr[col + 1] = __float_as_uint(x1);
+        m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], x0, x1);
       }
     }
     const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
@@ -196,24 +204,31 @@ __device__ __forceinline__ bool softmax_tile(const TcArgs& a, int t, uint32_t tS
       alpha = ex2(m_run - m_new);
       m_run = m_new;
     }
-    // P = 2^(s - m); zeros while no key of the row has been visible
-    const bool none = (m_run == -INFINITY);
-    const float neg_m = -m_run;
-    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+    // P = 2^(s - m); while no key of the row has been visible every s is -inf and
+    // 2^(s + 0) = 0
+    const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+    const uint64_t nm2 = f2_pack(neg_m, neg_m);
+    uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
     for (int c2i = 0; c2i < BN / 64; ++c2i) {
       uint32_t pk[32];
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
         const int idx = c2i * 64 + 2 * e;
-        const float p0 = none ? 0.f : ex2(__uint_as_float(sr[idx]) + neg_m);
-        const float p1 = none ? 0.f : ex2(__uint_as_float(sr[idx + 1]) + neg_m);
-        s4[e & 3] += p0 + p1;
+        float y0, y1;
+        f2_unpack(f2_add(f2_pack(__uint_as_float(sr[idx]), __uint_as_float(sr[idx + 1])), nm2), y0, y1);
+        const float p0 = ex2(y0), p1 = ex2(y1);
+        acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
         pk[e] = pack2<T>(p0, p1);
       }
       tmem_st32(tS + c2i * 32, pk);
     }
-    l_run = l_run * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+    {
+      float a0, a1, b0, b1;
+      f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
+      f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
+      l_run = l_run * alpha + ((a0 + a1) + (b0 + b1));
+    }
   }
   tmem_st_wait();
   if (t > 0 && wait_pv) {
