@@ -109,9 +109,11 @@ typedef struct {
  *             half_precision_softmax_is_precise: one rounding at the end).
  *   lse       device [B, Hq, Lq] float32 or NULL: m + ln(sum of weights incl. sink).
  *   dtype     nv_sdpa_dtype.   stream: cudaStream_t.
- * Ownership: the caller owns every buffer.  When the plan has nblk > 1, the call takes
- * plan.scratch_bytes of device memory with cudaMallocAsync on `stream` and frees it with
- * cudaFreeAsync on the same stream; nothing else is allocated, nothing synchronises.
+ * Ownership: the caller owns every buffer.  When the plan needs scratch, the call takes
+ * plan.scratch_bytes from the library's own stream-ordered pool on the current device
+ * (cudaMallocFromPoolAsync on `stream`) and frees it with cudaFreeAsync on the same
+ * stream; the pool keeps freed blocks for later calls (at most the largest call's
+ * scratch at a time).  Nothing else is allocated, nothing synchronises.
  * Returns NV_SDPA_OK or an nv_sdpa_status; on error nothing was launched (INVALID,
  * UNSUPPORTED) or a launch failed (CUDA). */
 int nv_sdpa(const void* q, const void* k, const void* v, const nv_sdpa_dims* dims,
@@ -126,10 +128,10 @@ int nv_sdpa_plan(const nv_sdpa_dims* dims, int mask_kind, int has_sinks, int dty
                  nv_sdpa_plan_t* plan);
 
 /* nv_sdpa_host: the same operation on HOST buffers (same layouts), for callers without
- * device memory of their own.  Allocates device buffers with cudaMallocAsync on `stream`,
- * copies the inputs in, runs nv_sdpa, copies out (and lse, if not NULL) back, frees, and
- * synchronises `stream` before returning.  Pinned host memory makes the copies fastest.
- * `bool_mask` and `sinks` are host pointers here too. */
+ * device memory of their own.  Takes one device block from the library's pool (as nv_sdpa
+ * does its scratch), copies the inputs in, runs nv_sdpa, copies out (and lse, if not
+ * NULL) back, frees, and synchronises `stream` before returning.  Pinned host memory
+ * makes the copies fastest.  `bool_mask` and `sinks` are host pointers here too. */
 int nv_sdpa_host(const void* q, const void* k, const void* v, const nv_sdpa_dims* dims,
                  int mask_kind, const uint8_t* bool_mask, const void* sinks, float scale,
                  void* out, float* lse, int dtype, void* stream);

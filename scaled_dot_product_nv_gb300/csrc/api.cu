@@ -8,6 +8,7 @@
 // overflow before anything is allocated, like the guards of "lattice-inference 0.4.0
 // src/attention/flash.rs" (assert_tiled_scratch_no_overflow).
 #include <atomic>
+#include <mutex>
 #include <cmath>
 #include <cstring>
 
@@ -29,6 +30,45 @@ std::atomic<uint64_t> g_wait_limit{0};
 constexpr uint64_t kDefaultWaitLimit = 1ull << 18;  // polls, each suspending <= ~10 us
 
 int elt_bytes(int dtype) { return dtype == NV_SDPA_F32 ? 4 : 2; }
+
+// The library's own stream-ordered memory pool on each device.  Freed blocks stay in it
+// for the next call: a pool whose release threshold is 0 (the default pool's default)
+// hands its memory back to the system at every synchronisation, and mapping it again
+// costs each call far more than the work it does.  Calls made with the library's memory
+// keep at most their own peak of it.
+std::mutex g_pool_mu;
+cudaMemPool_t g_pools[kMaxDevices];
+
+cudaError_t pool_alloc(void** ptr, size_t bytes, cudaStream_t st) {
+  int dev = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) return ce;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  cudaMemPool_t pool;
+  {
+    std::lock_guard<std::mutex> lock(g_pool_mu);
+    if (!g_pools[dev]) {
+      cudaMemPoolProps props;
+      memset(&props, 0, sizeof(props));
+      props.allocType = cudaMemAllocationTypePinned;
+      props.handleTypes = cudaMemHandleTypeNone;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      cudaMemPool_t created;
+      ce = cudaMemPoolCreate(&created, &props);
+      if (ce != cudaSuccess) return ce;
+      uint64_t keep = UINT64_MAX;
+      ce = cudaMemPoolSetAttribute(created, cudaMemPoolAttrReleaseThreshold, &keep);
+      if (ce != cudaSuccess) {
+        cudaMemPoolDestroy(created);
+        return ce;
+      }
+      g_pools[dev] = created;
+    }
+    pool = g_pools[dev];
+  }
+  return cudaMallocFromPoolAsync(ptr, bytes, pool, st);
+}
 
 bool mul_ok(int64_t a, int64_t b, int64_t* r) {
   if (__builtin_mul_overflow(a, b, r)) return false;
@@ -262,7 +302,7 @@ NV_SDPA_API int nv_sdpa(const void* q, const void* k, const void* v, const nv_sd
   }
   void* scratch = nullptr;
   if (pl.scratch_bytes) {
-    ce = cudaMallocAsync(&scratch, (size_t)pl.scratch_bytes, cs);
+    ce = pool_alloc(&scratch, (size_t)pl.scratch_bytes, cs);
     if (ce != cudaSuccess) return NV_SDPA_ERR_CUDA;
     const int64_t rows = x.B * x.Hq * x.Lq;
     const int64_t o_bytes = (rows * pl.nblk * x.dv * 4 + 255) / 256 * 256;
@@ -319,12 +359,14 @@ NV_SDPA_API int nv_sdpa_host(const void* q, const void* k, const void* v, const 
   const bool use_mask = mask_kind == NV_SDPA_MASK_BOOL && nm;
   const bool use_lse = lse && nl;
   const bool use_sinks = sinks != nullptr;
-  // one device block holds every buffer, each piece 256-byte aligned
+  // one device block from the library's pool holds every buffer, each piece 256-byte
+  // aligned; copies in, the call and copies out follow each other on `stream` (copies
+  // in flight beside the attention of other parts measured slower on this part)
   auto up = [](size_t n) { return (n + 255) / 256 * 256; };
   const size_t oq = 0, ok = oq + up(nq), ov = ok + up(nk), oo = ov + up(nv), ol = oo + up(no),
                om = ol + up(use_lse ? nl : 0), os = om + up(use_mask ? nm : 0), total = os + up(use_sinks ? ns : 0);
   char* dbuf = nullptr;
-  cudaError_t ce = cudaMallocAsync(reinterpret_cast<void**>(&dbuf), total ? total : 256, cs);
+  cudaError_t ce = pool_alloc(reinterpret_cast<void**>(&dbuf), total ? total : 256, cs);
   if (ce != cudaSuccess) return NV_SDPA_ERR_CUDA;
   if (nq) ce = cudaMemcpyAsync(dbuf + oq, q, nq, cudaMemcpyHostToDevice, cs);
   if (ce == cudaSuccess && nk) ce = cudaMemcpyAsync(dbuf + ok, k, nk, cudaMemcpyHostToDevice, cs);
@@ -355,7 +397,7 @@ NV_SDPA_API int nv_sdpa_host(const void* q, const void* k, const void* v, const 
 // another allocator -- a serving runtime or framework that reserves the GPU's memory up
 // front and forbids allocations outside its own pool -- or in a loop that cannot
 // afford an allocation call at all.  nv_sdpa() takes its scratch (split-KV partials,
-// the bit-packed boolean mask) with cudaMallocAsync; this entry point takes it from the
+// the bit-packed boolean mask) from the library's pool; this entry point takes it from the
 // fixed array below instead and allocates nothing.
 //
 // The array is a file-scope device variable: every GPU that loads this library holds

@@ -235,6 +235,32 @@ def test_host_buffer_entry_point_matches_device_entry_point():
     np.testing.assert_array_equal(lse, l_dev.cpu().numpy())
 
 
+@pytest.mark.parametrize("mask,sinks", [("causal", False), ("bool", True)])
+def test_large_host_buffer_call_gives_the_device_call_bits(mask, sinks):
+    """A large host-buffer call from pinned memory (its device block from the library's
+    pool, reused from call to call) gives every output and lse bit of the device call."""
+    import torch
+    nv = ensure_built()
+    c = W.Case(2, 32, 8, 2048, 2048, 128, 128, "bf16", mask, sinks, None, "n0.5", seed=31)
+    x = W.make_inputs(c)
+    dev = upload(c, x)
+    o_dev, l_dev = nv.sdpa(dev["q"], dev["k"], dev["v"], mask_kind=c.mask, scale=c.scale_f32,
+                           bool_mask=dev["mask"], sinks=dev["sinks"])
+    torch.cuda.synchronize()
+    pin = {n: torch.from_numpy(np.ascontiguousarray(x[n]).view(np.int16)).pin_memory()
+           for n in ("q", "k", "v")}
+    hout = torch.empty((c.B, c.Hq, c.Lq, c.dv), dtype=torch.int16).pin_memory()
+    hlse = torch.empty((c.B, c.Hq, c.Lq), dtype=torch.float32).pin_memory()
+    st = nv.nv_sdpa_host(pin["q"].data_ptr(), pin["k"].data_ptr(), pin["v"].data_ptr(),
+                         (c.B, c.Hq, c.Hkv, c.Lq, c.Lk, c.d, c.dv), nv.MASKS[mask],
+                         x["mask"].ctypes.data if mask == "bool" else None,
+                         x["sinks"].ctypes.data if sinks else None, c.scale_f32,
+                         hout.data_ptr(), hlse.data_ptr(), nv.DTYPES["bf16"], 0)
+    assert st == 0
+    assert torch.equal(hout, o_dev.view(torch.int16).cpu())
+    assert torch.equal(hlse, l_dev.cpu())
+
+
 def test_lse_only_optional_and_status_clean():
     import torch
     nv = ensure_built()
