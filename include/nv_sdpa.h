@@ -130,8 +130,12 @@ int nv_sdpa_plan(const nv_sdpa_dims* dims, int mask_kind, int has_sinks, int dty
 /* nv_sdpa_host: the same operation on HOST buffers (same layouts), for callers without
  * device memory of their own.  Takes one device block from the library's pool (as nv_sdpa
  * does its scratch), copies the inputs in, runs nv_sdpa, copies out (and lse, if not
- * NULL) back, frees, and synchronises `stream` before returning.  Pinned host memory
- * makes the copies fastest.  `bool_mask` and `sinks` are host pointers here too. */
+ * NULL) back, frees, and synchronises `stream` before returning.  A large tensor-core
+ * prefill (32 MiB of inputs or more) runs as a pipeline over 4 runs of (batch item,
+ * KV head) units: copies in, attention and copies out on three internal streams of the
+ * library, ordered by events, so that the copies of one run overlap the attention of
+ * another; the results are the bits of the single call.  Pinned host memory makes the
+ * copies fastest.  `bool_mask` and `sinks` are host pointers here too. */
 int nv_sdpa_host(const void* q, const void* k, const void* v, const nv_sdpa_dims* dims,
                  int mask_kind, const uint8_t* bool_mask, const void* sinks, float scale,
                  void* out, float* lse, int dtype, void* stream);

@@ -237,8 +237,9 @@ def test_host_buffer_entry_point_matches_device_entry_point():
 
 @pytest.mark.parametrize("mask,sinks", [("causal", False), ("bool", True)])
 def test_large_host_buffer_call_gives_the_device_call_bits(mask, sinks):
-    """A large host-buffer call from pinned memory (its device block from the library's
-    pool, reused from call to call) gives every output and lse bit of the device call."""
+    """A large host-buffer call from pinned memory runs as a pipeline over 4 runs of
+    (batch item, KV head) units (48 MiB of inputs: 2 batch items x 2 runs of 4 KV heads)
+    and gives every output and lse bit of the single device call."""
     import torch
     nv = ensure_built()
     c = W.Case(2, 32, 8, 2048, 2048, 128, 128, "bf16", mask, sinks, None, "n0.5", seed=31)
