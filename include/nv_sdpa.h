@@ -131,7 +131,7 @@ int nv_sdpa_plan(const nv_sdpa_dims* dims, int mask_kind, int has_sinks, int dty
  * device memory of their own.  Takes one device block from the library's pool (as nv_sdpa
  * does its scratch), copies the inputs in, runs nv_sdpa, copies out (and lse, if not
  * NULL) back, frees, and synchronises `stream` before returning.  A large tensor-core
- * prefill (32 MiB of inputs or more) runs as a pipeline over 4 runs of (batch item,
+ * prefill (24 MiB of inputs or more) runs as a pipeline over up to 8 runs of (batch item,
  * KV head) units: copies in, attention and copies out on three internal streams of the
  * library, ordered by events, so that the copies of one run overlap the attention of
  * another; the results are the bits of the single call.  Pinned host memory makes the

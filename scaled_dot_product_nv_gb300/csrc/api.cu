@@ -375,15 +375,20 @@ struct HostChunk {
 // How a host-buffer call is cut.  The (batch item, KV head) units of the tensor-core
 // prefill are computed independently (no key split, no cross-unit reduction) and each
 // unit's rows of q, k, v, out and lse are contiguous, so a run of units is one call on
-// contiguous sub-buffers that gives the same bits.  A large call is cut into 4 runs, so
-// that copies in, attention and copies out of different runs overlap (measured with the
-// 2x32/8 heads, 4096-position causal prefill: 1.12 ms per call in one piece, 1.01 ms in
-// 2 runs, 0.91 ms in 4 runs); every other case is one run.
+// contiguous sub-buffers that gives the same bits.  A large call is cut into up to 8
+// runs of at least 12 MiB of inputs, so that copies in, attention and copies out of
+// different runs overlap (measured with the 2x32/8 heads, 4096-position causal prefill,
+// 96 MiB in: 1.12 ms per call in one piece, 1.01 ms in 2 runs, 0.91 ms in 4, 0.87 ms in
+// 6, 0.86 ms in 8); every other case is one run.
 std::vector<HostChunk> host_chunks(const nv_sdpa_dims& x, int kernel, size_t h2d_bytes) {
   std::vector<HostChunk> out;
   const int64_t units = x.B * x.Hkv;
   int64_t n = 1;
-  if (kernel == NV_SDPA_KERNEL_PREFILL_TC && h2d_bytes >= (32u << 20)) n = 4;
+  if (kernel == NV_SDPA_KERNEL_PREFILL_TC) {
+    n = (int64_t)(h2d_bytes / (12u << 20));  // runs of at least 12 MiB of inputs, at most 8
+    if (n > 8) n = 8;
+    if (n < 1) n = 1;
+  }
   if (n > units) n = units;
   if (n == 1) {
     out.push_back({0, x.B, 0, x.Hkv});

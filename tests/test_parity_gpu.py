@@ -237,7 +237,7 @@ def test_host_buffer_entry_point_matches_device_entry_point():
 
 @pytest.mark.parametrize("mask,sinks", [("causal", False), ("bool", True)])
 def test_large_host_buffer_call_gives_the_device_call_bits(mask, sinks):
-    """A large host-buffer call from pinned memory runs as a pipeline over 4 runs of
+    """A large host-buffer call from pinned memory runs as a pipeline over runs of
     (batch item, KV head) units (48 MiB of inputs: 2 batch items x 2 runs of 4 KV heads)
     and gives every output and lse bit of the single device call."""
     import torch
