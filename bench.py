@@ -37,6 +37,15 @@ import workloads as W  # noqa: E402
 
 L2_BYTES = 129 * 2 ** 20 * 1.0
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# The targets' own denominators, beside the measured ones: ~8 TB/s of HBM for the decode
+# and the dense (no 2:4 sparsity) bf16/f16 tensor peak of a GB300, 2.25 PFLOP/s.
+NOMINAL = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0}
+
+
+def vs_nominal(achieved, key):
+    return {"peak": NOMINAL[key], "frac": round(achieved / NOMINAL[key], 4),
+            "source": "nominal: ~8 TB/s HBM3e" if key == "hbm_gbs"
+            else "nominal: 2.25 PFLOP/s dense bf16/f16"}
 
 
 def peaks():
@@ -297,6 +306,16 @@ def time_calls(torch, call, sets, steps, warmup, stream):
     return total_ms, launch_ms
 
 
+def steady_ms(torch, call, sets, stream, windows=5, per_window=50):
+    """Median over `windows` CUDA-event windows of `per_window` back-to-back calls each:
+    ms per call in steady state (a longer look than the K timed steps)."""
+    res = []
+    for _ in range(windows):
+        tot, _ = time_calls(torch, call, sets, per_window, 0, stream)
+        res.append(tot / per_window)
+    return round(statistics.median(res), 5), [round(r, 5) for r in res]
+
+
 def run_ours(args):
     import torch
     import scaled_dot_product_nv_gb300 as nv
@@ -376,6 +395,7 @@ def run_ours(args):
     flops_step = prefill_flops(pc)
     value = whole_job_rate(ws, flops_step, args.steps, total_ms_max / 1e3)
     launch_avg = statistics.mean(launch_ms)
+    p_steady = steady_ms(torch, pcall, psets, stream)
     peak_t = pk["bf16_tflops"]
     p_achieved = flops_step / (launch_avg / 1e3) / 1e12
     pkernel = pplan["kernel"]
@@ -398,6 +418,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": round(d_gbs, 1), "peak": pk["hbm_gbs"],
                      "unit": "GB/s", "frac": round(d_gbs / pk["hbm_gbs"], 4),
                      "peak_source": pk_src + " hbm_gbs (copy)",
+                     "vs_nominal": vs_nominal(d_gbs, "hbm_gbs"),
                      "timed": "whole call (pass 1 + merge) per CUDA-event pair",
                      "traffic": recorded_traffic("decode:" + dc.name)},
         "algorithmic_bytes_per_call": dbytes,
@@ -423,6 +444,7 @@ def run_ours(args):
         "roofline": {"bound": "tensor", "achieved": round(m_tf, 2), "peak": pk["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": round(m_tf / pk["bf16_tflops"], 4),
                      "peak_source": pk_src + " bf16_tflops (f16 runs at the bf16 rate)",
+                     "vs_nominal": vs_nominal(m_tf, "bf16_tflops"),
                      "timed": "whole call (mask packing + attention) per CUDA-event pair",
                      "traffic": recorded_traffic("prefill:" + mc.name)},
     }
@@ -456,10 +478,14 @@ def run_ours(args):
     # --------------------------------------------------------------- CPU oracle baseline
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        val, secs, sample = oracle_sample_rate(pc, px, args.cpu_budget)
-        cpu = {"value": round(val, 6), "unit": "TFLOP/s", "cores": host_threads(), "kind": "oracle",
-               "sample": f"{pc.name}: {sample}, {secs:.1f} s of f64 numpy on the host",
-               "seconds": round(secs, 2)}
+        def cpu_line(case, x, budget, unit):
+            val, secs, sample = oracle_sample_rate(case, x, budget)
+            return {"value": round(val, 6), "unit": unit, "cores": host_threads(), "kind": "oracle",
+                    "sample": f"{case.name}: {sample}, {secs:.1f} s of f64 numpy on the host",
+                    "seconds": round(secs, 2)}
+        cpu = cpu_line(pc, px, args.cpu_budget, "TFLOP/s")
+        decode["cpu_baseline"] = cpu_line(dc, dx, args.cpu_budget / 2, "GB/s")
+        prefill_mask["cpu_baseline"] = cpu_line(mc, mx, args.cpu_budget / 2, "TFLOP/s")
 
     if rank != 0:
         if pg:
@@ -481,7 +507,9 @@ def run_ours(args):
         "roofline": {"bound": "tensor", "achieved": round(p_achieved, 2), "peak": peak_t,
                      "unit": "TFLOP/s", "frac": round(p_achieved / peak_t, 4),
                      "peak_source": pk_src + " bf16_tflops (burst, cuBLAS)",
+                     "vs_nominal": vs_nominal(p_achieved, "bf16_tflops"),
                      "kernel_ms": round(launch_avg, 5),
+                     "steady_ms_per_call": p_steady[0], "steady_windows_ms": p_steady[1],
                      "traffic": recorded_traffic("prefill:" + pc.name)},
         "decode": decode,
         "prefill_mask": prefill_mask,

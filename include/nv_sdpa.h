@@ -83,9 +83,11 @@ typedef enum {
   NV_SDPA_KERNEL_DECODE_MMA = 4     /* TMA-staged tensor-core decode pass 1, f16/bf16   */
 } nv_sdpa_kernel;
 
-/* What nv_sdpa() will launch for a problem.  Pure: a function of its arguments only
- * (same answer on every call, thread and device), like the pure attention planner of
- * "nuvec-core 0.6.1 tests/attention_plan.rs" (plans_are_pure). */
+/* What nv_sdpa() will launch for a problem.  Pure for a given device: a function of its
+ * arguments and of the current device's SM count (read once per device; 152, a GB300's,
+ * when no device can be asked) -- the same answer on every call and thread, like the
+ * pure attention planner of "nuvec-core 0.6.1 tests/attention_plan.rs" (plans_are_pure).
+ * The batch size never changes how the keys are split. */
 typedef struct {
   int32_t path;          /* nv_sdpa_path                                                */
   int32_t kernel;        /* nv_sdpa_kernel of the main (first) launch                   */
@@ -164,16 +166,29 @@ int nv_sdpa_noalloc(const void* q, const void* k, const void* v, const nv_sdpa_d
 
 /* nv_sdpa_device_status: synchronises `stream`, then reads and clears the current
  * device's status word.  Returns NV_SDPA_OK, NV_SDPA_ERR_DEVICE_TIMEOUT (a bounded wait
- * in a kernel ran out; that launch's outputs are not valid), or NV_SDPA_ERR_CUDA.
- * If `detail` is not NULL it receives the raw status word (which wait gave up). */
+ * in a kernel ran out; that launch's outputs are not valid), NV_SDPA_ERR_UNSUPPORTED (a
+ * kernel refused a launch configuration it cannot run), or NV_SDPA_ERR_CUDA.
+ * If `detail` is not NULL it receives the raw status word (which wait gave up).
+ * This is how a device-side failure becomes a returned error instead of a hang or a
+ * trap: the pages' kernels report invalid states as errors, never a panic ("nuvec-core
+ * 0.5.0 tests/fast.rs", window_errors_empty_inputs_and_full_windows: invalid options
+ * are sticky errors).  The status word's device address is cached per device, as are
+ * the static scratch of nv_sdpa_noalloc and the kernels' attributes: do not use the
+ * library across a cudaDeviceReset of a device it has run on. */
 int nv_sdpa_device_status(void* stream, uint32_t* detail);
 
 /* Test hook for the bounded waits: sets the iteration limit of every device-side wait
  * of later launches on this process (0 = the built-in default).  A tiny limit makes
- * the waits run out so that the timeout path can be checked without hanging anything. */
+ * the waits run out so that the timeout path can be checked without hanging anything:
+ * the failure becomes NV_SDPA_ERR_DEVICE_TIMEOUT from nv_sdpa_device_status(), an error
+ * and never a panic, as the pages ask of invalid states ("nuvec-core 0.5.0
+ * tests/fast.rs", window_errors_empty_inputs_and_full_windows). */
 int nv_sdpa_set_wait_limit(uint64_t spins);
 
-/* A short, static, human-readable name of a status code. */
+/* A short, static, human-readable name of a status code (errors are returned as codes,
+ * never raised or printed: "nuvec-core 0.6.1 tests/attention_plan.rs",
+ * invalid_options_are_rejected_by_plan_and_op, where the plan and the op reject the same
+ * inputs with an error). */
 const char* nv_sdpa_status_string(int status);
 
 /* NV_SDPA_ABI_VERSION of the loaded library. */

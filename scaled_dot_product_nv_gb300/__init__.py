@@ -116,7 +116,19 @@ def nv_sdpa_noalloc(q, k, v, dims, mask_kind, bool_mask, sinks, scale, out, lse,
                                  stream or None)
 
 
-STATIC_SCRATCH_BYTES = 32 << 20
+def _header_define(name: str) -> int:
+    """An integer #define of the C header (so that the binding never restates a value)."""
+    import re
+    path = os.path.join(os.path.dirname(_PKG), "include", "nv_sdpa.h")
+    with open(path) as f:
+        m = re.search(r"#define\s+" + name + r"\s+\((\d+)u?\s*<<\s*(\d+)\)|#define\s+" + name +
+                      r"\s+(\d+)", f.read())
+    if not m:
+        raise RuntimeError(f"{name} not found in {path}")
+    return int(m.group(1)) << int(m.group(2)) if m.group(1) else int(m.group(3))
+
+
+STATIC_SCRATCH_BYTES = _header_define("NV_SDPA_STATIC_SCRATCH_BYTES")
 
 
 def nv_sdpa_plan(dims, mask_kind, has_sinks, dtype):

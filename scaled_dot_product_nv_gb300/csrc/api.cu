@@ -25,8 +25,7 @@ namespace {
 __device__ uint32_t g_status;  // per-device status word (bounded waits record here)
 
 constexpr int kMaxDevices = 64;
-constexpr int64_t kNumSms = 152;  // GB300: 2 dies x 76 SMs
-uint32_t* g_status_ptr[kMaxDevices];
+std::atomic<uint32_t*> g_status_ptr[kMaxDevices];
 std::atomic<uint64_t> g_wait_limit{0};
 constexpr uint64_t kDefaultWaitLimit = 1ull << 18;  // polls, each suspending <= ~10 us
 
@@ -82,7 +81,7 @@ bool mul_ok(int64_t a, int64_t b, int64_t* r) {
 int64_t decode_spans(const nv_sdpa_dims& x, int64_t nblk) {
   const int64_t rows = (x.Hq / x.Hkv) * x.Lq;
   const int64_t rc = (rows + decode_mma_rows_per_warp() - 1) / decode_mma_rows_per_warp();
-  const int64_t warp_slots = kNumSms * decode_mma_ctas_per_sm(x.d, x.dv) * decode_mma_warps_per_cta(x.d, x.dv);
+  const int64_t warp_slots = (int64_t)device_sm_count() * decode_mma_ctas_per_sm(x.d, x.dv) * decode_mma_warps_per_cta(x.d, x.dv);
   int64_t units;
   if (!mul_ok(x.B * x.Hkv, rc, &units) || units < 1) return 1;
   return std::max<int64_t>(1, std::min(nblk, warp_slots / units));
@@ -113,12 +112,14 @@ int check_dims(const nv_sdpa_dims* dm, int mask_kind, int dtype) {
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// The router.  Pure: depends on its arguments only.  The key-block count depends on
-// Lk and the per-batch-item work (Hkv x row tiles), never on B, so that a batch item
-// gets the bits of the same item run alone.
+// The router.  Pure for a given device: depends on its arguments and the current
+// device's SM count only.  The key-block count depends on Lk and the per-batch-item work
+// (Hkv x row tiles), never on B, so that a batch item gets the bits of the same item run
+// alone.
 int make_plan(const nv_sdpa_dims& x, int mask_kind, int has_sinks, int dtype, nv_sdpa_plan_t* pl) {
   (void)has_sinks;
   std::memset(pl, 0, sizeof(*pl));
+  const int64_t kNumSms = device_sm_count();
   pl->nblk = 1;
   if (x.B == 0 || x.Hq == 0 || x.Lq == 0) {
     pl->path = NV_SDPA_PATH_NOOP;
@@ -178,6 +179,7 @@ int make_plan(const nv_sdpa_dims& x, int mask_kind, int has_sinks, int dtype, nv
     pl->launches = nblk > 1 ? 2 : 1;
     if (nblk > 1) {
       const int64_t rows = x.B * x.Hq * x.Lq;
+      if (rows > 0x7fffffff) return NV_SDPA_ERR_UNSUPPORTED;  // the merge grid: one CTA per row
       pl->scratch_bytes = cdiv(rows * nblk * x.dv * 4, 256) * 256 + rows * nblk * 2 * 4;
     }
     return NV_SDPA_OK;
@@ -204,6 +206,7 @@ int make_plan(const nv_sdpa_dims& x, int mask_kind, int has_sinks, int dtype, nv
   pl->launches = nblk > 1 ? 2 : 1;
   if (nblk > 1) {
     const int64_t rows = x.B * x.Hq * x.Lq;
+    if (rows > 0x7fffffff) return NV_SDPA_ERR_UNSUPPORTED;  // the merge grid: one CTA per row
     const int64_t o_bytes = cdiv(rows * nblk * x.dv * 4, 256) * 256;
     pl->scratch_bytes = o_bytes + rows * nblk * 2 * 4;
   }
@@ -214,13 +217,15 @@ uint32_t* status_ptr_for_current_device(cudaError_t* err) {
   int dev = 0;
   *err = cudaGetDevice(&dev);
   if (*err != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (!g_status_ptr[dev]) {
+  uint32_t* cached = g_status_ptr[dev].load();
+  if (!cached) {
     void* ptr = nullptr;
     *err = cudaGetSymbolAddress(&ptr, g_status);
     if (*err != cudaSuccess) return nullptr;
-    g_status_ptr[dev] = static_cast<uint32_t*>(ptr);
+    cached = static_cast<uint32_t*>(ptr);
+    g_status_ptr[dev].store(cached);
   }
-  return g_status_ptr[dev];
+  return cached;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -256,69 +261,87 @@ NV_SDPA_API int nv_sdpa_set_wait_limit(uint64_t spins) {
   return NV_SDPA_OK;
 }
 
-NV_SDPA_API int nv_sdpa(const void* q, const void* k, const void* v, const nv_sdpa_dims* dims,
-                        int mask_kind, const uint8_t* bool_mask, const void* sinks, float scale,
-                        void* out, float* lse, int dtype, void* stream) {
+namespace nvsdpa {
+namespace {
+
+// Everything nv_sdpa() and nv_sdpa_noalloc() check before launching, and the launch
+// parameters of the call's plan.  Returns NV_SDPA_OK (with *pl and *p filled) or the
+// status to return; nothing has been launched or allocated either way.
+int prepare_call(const void* q, const void* k, const void* v, const nv_sdpa_dims* dims, int mask_kind,
+                 const uint8_t* bool_mask, const void* sinks, float scale, void* out, float* lse, int dtype,
+                 nv_sdpa_plan_t* pl, Params* p) {
   int st = check_dims(dims, mask_kind, dtype);
   if (st != NV_SDPA_OK) return st;
   if (!std::isfinite(scale)) return NV_SDPA_ERR_INVALID;
   const nv_sdpa_dims& x = *dims;
-  nv_sdpa_plan_t pl;
-  st = make_plan(x, mask_kind, sinks != nullptr, dtype, &pl);
+  st = make_plan(x, mask_kind, sinks != nullptr, dtype, pl);
   if (st != NV_SDPA_OK) return st;
-  if (pl.path == NV_SDPA_PATH_NOOP) return NV_SDPA_OK;
+  if (pl->path == NV_SDPA_PATH_NOOP) return NV_SDPA_OK;
   // pointers: required ones present and aligned
   const int64_t e = elt_bytes(dtype);
   if (!out || !aligned(out, 16)) return NV_SDPA_ERR_INVALID;
   if (lse && !aligned(lse, 4)) return NV_SDPA_ERR_INVALID;
   if (sinks && !aligned(sinks, (uintptr_t)e)) return NV_SDPA_ERR_INVALID;
-  if (pl.path != NV_SDPA_PATH_NO_KEYS) {
+  if (pl->path != NV_SDPA_PATH_NO_KEYS) {
     if (!q || !k || !v || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16)) return NV_SDPA_ERR_INVALID;
     if (mask_kind == NV_SDPA_MASK_BOOL && !bool_mask) return NV_SDPA_ERR_INVALID;
   }
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  cudaError_t ce;
-  Params p{};
-  p.q = q; p.k = k; p.v = v;
-  p.mask = mask_kind == NV_SDPA_MASK_BOOL ? bool_mask : nullptr;
-  p.sinks = sinks; p.out = out; p.lse = lse;
-  p.status = status_ptr_for_current_device(&ce);
-  if (!p.status) return NV_SDPA_ERR_CUDA;
-  p.B = x.B; p.Hq = x.Hq; p.Hkv = x.Hkv; p.Lq = x.Lq; p.Lk = x.Lk; p.d = x.d; p.dv = x.dv;
-  p.g = x.Hq / x.Hkv; p.G = p.g * x.Lq;
-  p.nblk = pl.nblk; p.keys_per_blk = pl.keys_per_blk;
-  p.row_tiles = pl.rows_per_cta ? (p.G + pl.rows_per_cta - 1) / pl.rows_per_cta : 1;
-  p.spans = 1;
-  if (pl.kernel == NV_SDPA_KERNEL_DECODE_MMA) p.spans = decode_spans(x, pl.nblk);
-  p.mask_kind = mask_kind;
-  p.has_sinks = sinks != nullptr;
-  p.scale = scale;
-  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  *p = Params{};
+  p->q = q; p->k = k; p->v = v;
+  p->mask = mask_kind == NV_SDPA_MASK_BOOL ? bool_mask : nullptr;
+  p->sinks = sinks; p->out = out; p->lse = lse;
+  p->B = x.B; p->Hq = x.Hq; p->Hkv = x.Hkv; p->Lq = x.Lq; p->Lk = x.Lk; p->d = x.d; p->dv = x.dv;
+  p->g = x.Hq / x.Hkv; p->G = p->g * x.Lq;
+  p->nblk = pl->nblk; p->keys_per_blk = pl->keys_per_blk;
+  p->row_tiles = pl->rows_per_cta ? (p->G + pl->rows_per_cta - 1) / pl->rows_per_cta : 1;
+  p->spans = pl->kernel == NV_SDPA_KERNEL_DECODE_MMA ? decode_spans(x, pl->nblk) : 1;
+  p->mask_kind = mask_kind;
+  p->has_sinks = sinks != nullptr;
+  p->scale = scale;
+  p->scale_log2 = (float)((double)scale * 1.4426950408889634);
   const uint64_t wl = g_wait_limit.load();
-  p.wait_limit = wl ? wl : kDefaultWaitLimit;
+  p->wait_limit = wl ? wl : kDefaultWaitLimit;
+  return NV_SDPA_OK;
+}
 
-  if (pl.path == NV_SDPA_PATH_NO_KEYS) {
-    ce = launch_fill_no_keys(dtype, p, cs);
-    return ce == cudaSuccess ? NV_SDPA_OK : NV_SDPA_ERR_CUDA;
-  }
-  void* scratch = nullptr;
-  if (pl.scratch_bytes) {
-    ce = pool_alloc(&scratch, (size_t)pl.scratch_bytes, cs);
-    if (ce != cudaSuccess) return NV_SDPA_ERR_CUDA;
-    const int64_t rows = x.B * x.Hq * x.Lq;
-    const int64_t o_bytes = (rows * pl.nblk * x.dv * 4 + 255) / 256 * 256;
+// Launches the kernels of a prepared call on `cs`.  `scratch` holds pl.scratch_bytes
+// (the split-KV partials, or the bit-packed boolean mask) or is null when none is needed.
+cudaError_t launch_plan(int dtype, const nv_sdpa_plan_t& pl, Params& p, void* scratch, cudaStream_t cs) {
+  cudaError_t ce;
+  p.status = status_ptr_for_current_device(&ce);
+  if (!p.status) return ce != cudaSuccess ? ce : cudaErrorUnknown;
+  if (pl.path == NV_SDPA_PATH_NO_KEYS) return launch_fill_no_keys(dtype, p, cs);
+  if (scratch) {
+    const int64_t rows = p.B * p.Hq * p.Lq;
+    const int64_t o_bytes = (rows * pl.nblk * p.dv * 4 + 255) / 256 * 256;
     p.part_o = static_cast<float*>(scratch);
     p.part_ml = reinterpret_cast<float*>(static_cast<char*>(scratch) + o_bytes);
   }
-  if (pl.kernel == NV_SDPA_KERNEL_PREFILL_TC) {
-    ce = launch_prefill_tc(dtype, p, static_cast<uint32_t*>(scratch), cs);
-  } else if (pl.kernel == NV_SDPA_KERNEL_DECODE_MMA) {
+  if (pl.kernel == NV_SDPA_KERNEL_PREFILL_TC) return launch_prefill_tc(dtype, p, static_cast<uint32_t*>(scratch), cs);
+  if (pl.kernel == NV_SDPA_KERNEL_DECODE_MMA) {
     ce = launch_decode_mma(dtype, p, cs);
-    if (ce == cudaSuccess && pl.nblk > 1) ce = launch_merge(dtype, p, cs);
   } else {
     ce = launch_tiled_simt(dtype, p, cs);
-    if (ce == cudaSuccess && pl.nblk > 1) ce = launch_merge(dtype, p, cs);
   }
+  if (ce == cudaSuccess && pl.nblk > 1) ce = launch_merge(dtype, p, cs);
+  return ce;
+}
+
+}  // namespace
+}  // namespace nvsdpa
+
+NV_SDPA_API int nv_sdpa(const void* q, const void* k, const void* v, const nv_sdpa_dims* dims,
+                        int mask_kind, const uint8_t* bool_mask, const void* sinks, float scale,
+                        void* out, float* lse, int dtype, void* stream) {
+  nv_sdpa_plan_t pl;
+  Params p;
+  int st = prepare_call(q, k, v, dims, mask_kind, bool_mask, sinks, scale, out, lse, dtype, &pl, &p);
+  if (st != NV_SDPA_OK || pl.path == NV_SDPA_PATH_NOOP) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  void* scratch = nullptr;
+  if (pl.scratch_bytes && pool_alloc(&scratch, (size_t)pl.scratch_bytes, cs) != cudaSuccess)
+    return NV_SDPA_ERR_CUDA;
+  cudaError_t ce = launch_plan(dtype, pl, p, scratch, cs);
   if (scratch) {
     cudaError_t fe = cudaFreeAsync(scratch, cs);
     if (ce == cudaSuccess) ce = fe;
@@ -563,68 +586,19 @@ void* static_scratch_for_current_device(cudaError_t* err) {
 NV_SDPA_API int nv_sdpa_noalloc(const void* q, const void* k, const void* v, const nv_sdpa_dims* dims,
                                 int mask_kind, const uint8_t* bool_mask, const void* sinks, float scale,
                                 void* out, float* lse, int dtype, void* stream) {
-  int st = check_dims(dims, mask_kind, dtype);
-  if (st != NV_SDPA_OK) return st;
-  if (!std::isfinite(scale)) return NV_SDPA_ERR_INVALID;
-  const nv_sdpa_dims& x = *dims;
   nv_sdpa_plan_t pl;
-  st = make_plan(x, mask_kind, sinks != nullptr, dtype, &pl);
-  if (st != NV_SDPA_OK) return st;
-  if (pl.path == NV_SDPA_PATH_NOOP) return NV_SDPA_OK;
+  Params p;
+  int st = prepare_call(q, k, v, dims, mask_kind, bool_mask, sinks, scale, out, lse, dtype, &pl, &p);
+  if (st != NV_SDPA_OK || pl.path == NV_SDPA_PATH_NOOP) return st;
   if (pl.scratch_bytes > (int64_t)NV_SDPA_STATIC_SCRATCH_BYTES) return NV_SDPA_ERR_UNSUPPORTED;
-  const int64_t e = elt_bytes(dtype);
-  if (!out || !aligned(out, 16)) return NV_SDPA_ERR_INVALID;
-  if (lse && !aligned(lse, 4)) return NV_SDPA_ERR_INVALID;
-  if (sinks && !aligned(sinks, (uintptr_t)e)) return NV_SDPA_ERR_INVALID;
-  if (pl.path != NV_SDPA_PATH_NO_KEYS) {
-    if (!q || !k || !v || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16)) return NV_SDPA_ERR_INVALID;
-    if (mask_kind == NV_SDPA_MASK_BOOL && !bool_mask) return NV_SDPA_ERR_INVALID;
-  }
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  cudaError_t ce;
-  Params p{};
-  p.q = q; p.k = k; p.v = v;
-  p.mask = mask_kind == NV_SDPA_MASK_BOOL ? bool_mask : nullptr;
-  p.sinks = sinks; p.out = out; p.lse = lse;
-  p.status = status_ptr_for_current_device(&ce);
-  if (!p.status) return NV_SDPA_ERR_CUDA;
+  cudaError_t ce = cudaSuccess;
   void* scratch = nullptr;
   if (pl.scratch_bytes) {
     scratch = static_scratch_for_current_device(&ce);
     if (!scratch) return NV_SDPA_ERR_CUDA;
   }
-  p.B = x.B; p.Hq = x.Hq; p.Hkv = x.Hkv; p.Lq = x.Lq; p.Lk = x.Lk; p.d = x.d; p.dv = x.dv;
-  p.g = x.Hq / x.Hkv; p.G = p.g * x.Lq;
-  p.nblk = pl.nblk; p.keys_per_blk = pl.keys_per_blk;
-  p.row_tiles = pl.rows_per_cta ? (p.G + pl.rows_per_cta - 1) / pl.rows_per_cta : 1;
-  p.spans = 1;
-  if (pl.kernel == NV_SDPA_KERNEL_DECODE_MMA) p.spans = decode_spans(x, pl.nblk);
-  p.mask_kind = mask_kind;
-  p.has_sinks = sinks != nullptr;
-  p.scale = scale;
-  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
-  const uint64_t wl = g_wait_limit.load();
-  p.wait_limit = wl ? wl : kDefaultWaitLimit;
-  if (pl.path == NV_SDPA_PATH_NO_KEYS) {
-    ce = launch_fill_no_keys(dtype, p, cs);
-    return ce == cudaSuccess ? NV_SDPA_OK : NV_SDPA_ERR_CUDA;
-  }
-  if (scratch) {
-    // every partial (and mask word) the merge pass reads is written by this call's first
-    // kernel, so the array's previous contents never need clearing
-    const int64_t rows = x.B * x.Hq * x.Lq;
-    const int64_t o_bytes = (rows * pl.nblk * x.dv * 4 + 255) / 256 * 256;
-    p.part_o = static_cast<float*>(scratch);
-    p.part_ml = reinterpret_cast<float*>(static_cast<char*>(scratch) + o_bytes);
-  }
-  if (pl.kernel == NV_SDPA_KERNEL_PREFILL_TC) {
-    ce = launch_prefill_tc(dtype, p, static_cast<uint32_t*>(scratch), cs);
-  } else if (pl.kernel == NV_SDPA_KERNEL_DECODE_MMA) {
-    ce = launch_decode_mma(dtype, p, cs);
-    if (ce == cudaSuccess && pl.nblk > 1) ce = launch_merge(dtype, p, cs);
-  } else {
-    ce = launch_tiled_simt(dtype, p, cs);
-    if (ce == cudaSuccess && pl.nblk > 1) ce = launch_merge(dtype, p, cs);
-  }
+  // every partial (and mask word) that a later kernel of the call reads is written by an
+  // earlier one, so the array's previous contents never need clearing
+  ce = launch_plan(dtype, pl, p, scratch, static_cast<cudaStream_t>(stream));
   return ce == cudaSuccess ? NV_SDPA_OK : NV_SDPA_ERR_CUDA;
 }

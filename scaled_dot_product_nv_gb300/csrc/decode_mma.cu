@@ -360,49 +360,12 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
   __syncwarp();
 }
 
-using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
-                                 CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                 CUtensorMapFloatOOBfill);
-
-EncodeTiled get_encode_dec() {
-  static EncodeTiled fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiled>(ptr);
-  }
-  return fn;
-}
-
-bool encode_kv(CUtensorMap* m, int dtype, const void* ptr, int64_t inner, int64_t rows, int64_t outer, int kt) {
-  EncodeTiled enc = get_encode_dec();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)outer};
-  cuuint64_t strides[2] = {(cuuint64_t)(inner * 2), (cuuint64_t)(inner * rows * 2)};
-  cuuint32_t box[3] = {64, (cuuint32_t)kt, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-             const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <typename T, int DMAX, int DV>
 cudaError_t launch_dec_t(const DecArgs& a, int64_t grid, cudaStream_t st) {
   using Sh = DecShape<DMAX, DV>;
-  static unsigned long long configured = 0;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<unsigned long long> configured{0};
+  cudaError_t e = set_max_dynamic_smem_once(configured, (const void*)sdpa_decode_mma<T, DMAX, DV>, Sh::kSmem);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !(configured >> dev & 1ull)) {
-    e = cudaFuncSetAttribute(sdpa_decode_mma<T, DMAX, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) configured |= 1ull << dev;
-  }
   sdpa_decode_mma<T, DMAX, DV><<<(unsigned)grid, Sh::WPC * 32, Sh::kSmem, st>>>(a);
   return cudaGetLastError();
 }
@@ -472,7 +435,7 @@ cudaError_t launch_decode_mma(int dtype, const Params& p, cudaStream_t st) {
   a.p = p;
   const int64_t BH = p.B * p.Hkv;
   const int kt = dec_info(p.d, p.dv).kt;
-  if (!kt || !encode_kv(&a.tmk, dtype, p.k, p.d, p.Lk, BH, kt) || !encode_kv(&a.tmv, dtype, p.v, p.dv, p.Lk, BH, kt))
+  if (!kt || !encode_3d(&a.tmk, dtype, p.k, p.d, p.Lk, BH, kt) || !encode_3d(&a.tmv, dtype, p.v, p.dv, p.Lk, BH, kt))
     return cudaErrorInvalidValue;
   a.n_rc = (int)((p.G + kRowsDec - 1) / kRowsDec);
   a.dpanels = (int)((p.d + 63) / 64);

@@ -2,13 +2,30 @@
 // tiling constants the planner needs from them.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace nvsdpa {
+
+// tensor_map.cu
+constexpr int kDefaultSmCount = 152;  // GB300 (2 dies x 76 SMs), when no device can be asked
+// SM count of the current device, read once per device (kDefaultSmCount if none).
+int device_sm_count();
+// A tiled TMA map of a 16-bit tensor of `rank` dims (innermost first, strides in elements
+// for dims 1..rank-1), boxes of 64 x box_rows x 1 ..., 128-byte swizzle, zero fill.
+bool encode_tiled_16bit(CUtensorMap* m, int dtype, const void* ptr, int rank, const int64_t* dims,
+                        const int64_t* strides_elems, int box_rows);
+// The contiguous [outer][rows][inner] case of encode_tiled_16bit.
+bool encode_3d(CUtensorMap* m, int dtype, const void* ptr, int64_t inner, int64_t rows, int64_t outer,
+               int box_rows);
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per device (thread-safe bitmask).
+cudaError_t set_max_dynamic_smem_once(std::atomic<unsigned long long>& configured, const void* fn, int bytes);
 
 // tiled_simt.cu
 size_t tiled_simt_smem_bytes(int64_t d, int64_t dv);

@@ -736,53 +736,11 @@ __global__ void sdpa_pack_mask_bits(const uint8_t* __restrict__ mask, int64_t Lq
 
 // ------------------------------------------------------------------------- host side
 
-using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
-                                 CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                 CUtensorMapFloatOOBfill);
-
-EncodeTiled get_encode() {
-  static EncodeTiled fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiled>(ptr);
-  }
-  return fn;
-}
-
-// [outer][rows][inner] 16-bit tensor, boxes of 64 x box_rows x 1 with 128-byte swizzle,
-// out-of-range elements read as zero.
-bool encode_3d(CUtensorMap* m, int dtype, const void* ptr, int64_t inner, int64_t rows, int64_t outer,
-               int box_rows) {
-  EncodeTiled enc = get_encode();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)outer};
-  cuuint64_t strides[2] = {(cuuint64_t)(inner * 2), (cuuint64_t)(inner * rows * 2)};
-  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-                   const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 template <typename T, int BN, int NQ>
 cudaError_t launch_tc_t(const TcArgs& a, size_t smem, int64_t grid, cudaStream_t st) {
-  static unsigned long long configured = 0;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<unsigned long long> configured{0};
+  cudaError_t e = set_max_dynamic_smem_once(configured, (const void*)sdpa_prefill_tc<T, BN, NQ>, (int)kTcMaxSmem);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !(configured >> dev & 1ull)) {
-    e = cudaFuncSetAttribute(sdpa_prefill_tc<T, BN, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kTcMaxSmem);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) configured |= 1ull << dev;
-  }
   sdpa_prefill_tc<T, BN, NQ><<<(unsigned)grid, tc_threads<NQ>(), smem, st>>>(a);
   return cudaGetLastError();
 }
@@ -862,7 +820,8 @@ cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, c
     a.mask_bits = mask_bits;
     const int64_t n = p.Lq * a.mask_words;
     int64_t g = (n + 255) / 256;
-    if (g > 152 * 8) g = 152 * 8;
+    const int64_t cap = (int64_t)device_sm_count() * 8;
+    if (g > cap) g = cap;
     sdpa_pack_mask_bits<<<(unsigned)(g > 0 ? g : 1), 256, 0, st>>>(p.mask, p.Lq, p.Lk, a.mask_words, mask_bits);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

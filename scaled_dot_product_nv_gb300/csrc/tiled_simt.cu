@@ -310,16 +310,10 @@ __global__ void sdpa_fill_no_keys(const Params p) {
 template <typename T>
 cudaError_t launch_simt_t(const Params& p, cudaStream_t st) {
   const size_t smem = tiled_simt_smem_bytes(p.d, p.dv);
-  static unsigned long long configured = 0;  // one bit per device ordinal < 64
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<unsigned long long> configured{0};
+  cudaError_t e = set_max_dynamic_smem_once(configured, (const void*)sdpa_tiled_simt<T>,
+                                            (int)tiled_simt_smem_bytes(256, 256));
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !(configured >> dev & 1ull)) {
-    e = cudaFuncSetAttribute(sdpa_tiled_simt<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)tiled_simt_smem_bytes(256, 256));
-    if (e != cudaSuccess) return e;
-    if (dev < 64) configured |= 1ull << dev;
-  }
   const int64_t grid = p.B * p.Hkv * p.nblk * p.row_tiles;
   sdpa_tiled_simt<T><<<(unsigned)grid, kThreads, smem, st>>>(p);
   return cudaGetLastError();
@@ -346,7 +340,8 @@ template <typename T>
 cudaError_t launch_fill_t(const Params& p, cudaStream_t st) {
   const int64_t n = p.B * p.Hq * p.Lq * p.dv;
   int64_t grid = (n + 255) / 256;
-  if (grid > 152 * 16) grid = 152 * 16;
+  const int64_t cap = (int64_t)device_sm_count() * 16;
+  if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
   sdpa_fill_no_keys<T><<<(unsigned)grid, 256, 0, st>>>(p);
   return cudaGetLastError();

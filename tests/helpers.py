@@ -75,16 +75,49 @@ def upload(case, x):
     return dev
 
 
+GUARD_BYTES = 4096   # canary band on each side of an output (a multiple of 256: keeps alignment)
+CANARY = 0xA5
+
+
+class Guarded:
+    """A CUDA tensor of `shape` inside a larger byte buffer whose bands before and after
+    it hold a canary pattern, so that a kernel writing past either end of its output is
+    caught (no memory checker runs on the GPU; these bands are the stand-in)."""
+
+    def __init__(self, shape, dtype):
+        import torch
+        self.shape = tuple(shape)
+        n = int(np.prod(self.shape)) if self.shape else 1
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        self.raw = torch.full((GUARD_BYTES + nbytes + GUARD_BYTES,), CANARY, dtype=torch.uint8,
+                              device="cuda")
+        self.nbytes = nbytes
+        self.tensor = self.raw[GUARD_BYTES:GUARD_BYTES + nbytes].view(dtype).view(self.shape)
+
+    def check(self, what):
+        head = self.raw[:GUARD_BYTES]
+        tail = self.raw[GUARD_BYTES + self.nbytes:]
+        bad_head = int((head != CANARY).sum())
+        bad_tail = int((tail != CANARY).sum())
+        assert bad_head == 0 and bad_tail == 0, \
+            f"{what}: {bad_head} bytes before and {bad_tail} bytes after the buffer were written"
+
+
 def run_gpu(case, x, dev=None):
-    """Runs the CUDA path; returns (out f64 [B,Hq,Lq,dv], lse f64 [B,Hq,Lq])."""
+    """Runs the CUDA path; returns (out f64 [B,Hq,Lq,dv], lse f64 [B,Hq,Lq]).  The output
+    and the log-sum-exp are written into canary-guarded buffers, checked after the call."""
     import torch
     nv = ensure_built()
     dev = dev or upload(case, x)
+    gout = Guarded((case.B, case.Hq, case.Lq, case.dv), torch_dtype(case.dtype))
+    glse = Guarded((case.B, case.Hq, case.Lq), torch.float32)
     out, lse = nv.sdpa(dev["q"], dev["k"], dev["v"], mask_kind=case.mask, scale=case.scale_f32,
-                       bool_mask=dev["mask"], sinks=dev["sinks"])
+                       bool_mask=dev["mask"], sinks=dev["sinks"], out=gout.tensor, lse=glse.tensor)
     torch.cuda.synchronize()
     st, detail = nv.nv_sdpa_device_status(0)
     assert st == nv.OK, f"device status {st} detail {detail:#x}"
+    gout.check("out")
+    glse.check("lse")
     return from_device(out, case.dtype), lse.cpu().numpy().astype(np.float64)
 
 

@@ -302,3 +302,71 @@ def test_pipeline_repeats_are_identical_and_correct(case):
         assert torch.equal(o.view(torch.int16), outs[0][0].view(torch.int16))
         assert torch.equal(l, outs[0][1])
     check_case(case, x)
+
+
+# ----------------------------------------------------------------------------- scales and mask bytes
+
+def _scale_cases():
+    """Every kernel under scale 0 (all scores equal: the mean of the visible V rows) and
+    under negative scales (the largest raw score is then the smallest scaled one, which
+    the prefill's unmasked fast path must not assume away).  The pages pass arbitrary f32
+    scales ("nuvec-core 0.5.0 tests/fast.rs": 0.3 in the fused-attention tests, 0.125 in
+    the window tests); here 0, -0.3 and -1/sqrt(d)."""
+    base = [
+        # (name, case, expected kernel, expected nblk > 1)
+        ("prefill_nq2", W.Case(1, 8, 2, 300, 500, 128, 128, "bf16", "none", True, None, "n0.5", seed=61),
+         "prefill_tc", False),
+        ("prefill_nq2_causal", W.Case(2, 4, 2, 257, 257, 64, 64, "f16", "causal", False, None, "u2", seed=62),
+         "prefill_tc", False),
+        ("prefill_nq1_d256", W.Case(1, 4, 2, 200, 300, 256, 256, "f16", "none", True, None, "n0.5", seed=63),
+         "prefill_tc", False),
+        ("prefill_nq1_d192_bool", W.Case(1, 4, 1, 100, 700, 192, 128, "bf16", "bool", False, None, "n0.5",
+                                         seed=64), "prefill_tc", False),
+        ("decode_split", W.Case(2, 8, 2, 1, 3000, 128, 128, "f16", "causal", True, None, "u2", seed=65),
+         "decode_mma", True),
+        ("decode_one_block", W.Case(1, 4, 4, 3, 200, 64, 64, "bf16", "none", False, None, "n0.5", seed=66),
+         "decode_mma", False),
+        ("decode_bool", W.Case(1, 8, 2, 5, 900, 128, 128, "bf16", "bool", True, None, "n0.5", seed=67),
+         "decode_mma", True),
+        ("f32_prefill", W.Case(1, 4, 2, 40, 700, 64, 64, "f32", "causal", True, None, "n0.5", seed=68),
+         "tiled_simt", True),
+        ("f32_decode", W.Case(2, 4, 2, 1, 3000, 64, 64, "f32", "none", False, None, "u0.25", seed=69),
+         "tiled_simt", True),
+    ]
+    out = []
+    for name, c, kern, split in base:
+        for sc in [0.0, -0.3, "-rsqrt"]:
+            s = -1.0 / np.sqrt(c.d) if sc == "-rsqrt" else sc
+            out.append((f"{name}_scale{sc}", c.with_(scale=s, name=f"{name}_scale{sc}"), kern, split))
+    return out
+
+
+SCALES = _scale_cases()
+
+
+@pytest.mark.parametrize("name,case,kernel,split", SCALES, ids=[s[0] for s in SCALES])
+def test_zero_and_negative_scales(name, case, kernel, split):
+    nv = ensure_built()
+    st, pl = nv.nv_sdpa_plan((case.B, case.Hq, case.Hkv, case.Lq, case.Lk, case.d, case.dv),
+                             nv.MASKS[case.mask], int(case.sinks), nv.DTYPES[case.dtype])
+    assert st == nv.OK and pl["kernel"] == kernel and (pl["nblk"] > 1) == split, pl
+    check_case(case, name=name)
+
+
+MASK_BYTES = [
+    W.Case(1, 8, 2, 300, 700, 128, 128, "bf16", "bool", True, None, "n0.5", seed=71, name="prefill_nq2"),
+    W.Case(1, 4, 2, 150, 333, 256, 256, "f16", "bool", False, None, "n0.5", seed=72, name="prefill_nq1"),
+    W.Case(2, 8, 2, 4, 2000, 128, 128, "f16", "bool", True, None, "u2", seed=73, name="decode"),
+    W.Case(1, 4, 2, 33, 400, 64, 64, "f32", "bool", False, None, "u0.25", seed=74, name="f32"),
+]
+
+
+@pytest.mark.parametrize("case", MASK_BYTES, ids=[c.name for c in MASK_BYTES])
+def test_boolean_mask_reads_any_nonzero_byte_as_attend(case):
+    """The mask is bytes, nonzero = attend: entries of 2, 128 and 255 must act like 1."""
+    x = W.make_inputs(case)
+    rng = np.random.RandomState(case.seed)
+    x["mask"] = (x["mask"] * rng.choice(np.array([1, 2, 128, 255], dtype=np.uint8),
+                                        size=x["mask"].shape)).astype(np.uint8)
+    assert set(np.unique(x["mask"])) == {0, 1, 2, 128, 255}
+    check_case(case, x)
