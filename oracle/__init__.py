@@ -11,4 +11,5 @@ and the readings taken where the pages are silent.  Every function here is pinne
 ``tests/test_oracle_pins.py`` (closed forms, a worked example printed on the pages,
 invariants and a high-precision brute force) -- no function is "parity unpinned".
 """
-from .attention import attend_rows, sdpa, sdpa_sampled, visible_mask  # noqa: F401
+from .attention import (attend_rows, paged_gather, sdpa, sdpa_paged, sdpa_sampled,  # noqa: F401
+                        visible_mask)
