@@ -117,6 +117,12 @@ def attend_rows(q_rows: np.ndarray, k_head: np.ndarray, v_head: np.ndarray,
     k_head = np.asarray(k_head, dtype=np.float64)
     v_head = np.asarray(v_head, dtype=np.float64)
     n, Lk, dv = q_rows.shape[0], k_head.shape[0], v_head.shape[1]
+    # The sums run over visible keys only: a key that no row sees takes no part at all,
+    # whatever its stored values (the pages fill such never-read cache blocks with NaN).
+    seen = np.asarray(vis).any(axis=0)
+    if not seen.all():
+        k_head = np.where(seen[:, None], k_head, 0.0)
+        v_head = np.where(seen[:, None], v_head, 0.0)
     # scores s_ij = scale * <q_i, k_j> (+ mask_ij), minus infinity where key j is not visible
     s = np.float64(scale) * (q_rows @ k_head.T) if Lk else np.zeros((n, 0))
     if add is not None:

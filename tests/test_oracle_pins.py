@@ -677,7 +677,30 @@ def pin_paged_empty_sequences(fn, fnp):
         fnp(q, kc, kc, table, np.array([3, 3]), mask_kind="bool", scale=0.5)
 
 
-PAGED_PINS = [pin_paged_equals_contiguous, pin_paged_hostile_tables_are_clamped, pin_paged_block_order,
+def pin_paged_never_reads_hidden_blocks(fn, fnp):
+    """Blocks wholly before every row's window, and every slot past a length, hold NaN:
+    the result equals the one with those slots zeroed, and is finite ("nuvec-core 0.5.0
+    tests/fast.rs", paged_windows_and_sinks_equal_contiguous_attention)."""
+    B, Hq, Hkv, Lq, N, d, bs, W = 2, 4, 2, 2, 12, 4, 3, 4
+    keys = rand((B, Hkv, N, d), 261)
+    vals = rand((B, Hkv, N, 3), 262)
+    q = rand((B, Hq, Lq, d), 263)
+    kc, vc, table = build_paged(keys, vals, bs, list(range(B * (-(-N // bs)))))
+    lens = np.array([12, 9])
+    clean_k, clean_v = np.nan_to_num(kc), np.nan_to_num(vc)
+    for s in range(B):
+        first = lens[s] - Lq - W + 1          # the earliest row's band starts here
+        for j in range(first // bs):
+            kc[table[s, j]] = np.nan
+            vc[table[s, j]] = np.nan
+    a, la = fnp(q, kc, vc, table, lens, mask_kind="causal", scale=0.5, window=W)
+    b, lb = fnp(q, clean_k, clean_v, table, lens, mask_kind="causal", scale=0.5, window=W)
+    assert np.all(np.isfinite(a))
+    np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(la, lb)
+
+
+PAGED_PINS = [pin_paged_never_reads_hidden_blocks, pin_paged_equals_contiguous, pin_paged_hostile_tables_are_clamped, pin_paged_block_order,
               pin_paged_empty_sequences]
 
 
