@@ -316,6 +316,119 @@ def steady_ms(torch, call, sets, stream, windows=5, per_window=50):
     return round(statistics.median(res), 5), [round(r, 5) for r in res]
 
 
+def window_pairs(Lq, Lk, W):
+    """Visible (query, key) pairs of one head under the causal mask with a window of W."""
+    pos = np.arange(Lq, dtype=np.int64) + (Lk - Lq)
+    hi = np.minimum(pos + 1, Lk)
+    lo = np.maximum(pos - W + 1, 0) if W else np.zeros(Lq, np.int64)
+    return float(np.maximum(hi - lo, 0).sum())
+
+
+def feature_lines(torch, nv, dev, stream, pk, pc, px, dc, dx, mc, mx, args):
+    """Throughput of the options beyond nv_sdpa() on the workloads' shapes: causal sliding
+    windows (prefill and decode), paged decode, an additive-mask prefill and a prefill with
+    every tensor a transposed [B, L, H, D] view.  Work counts only what the option leaves
+    visible: 2 (d + dv) FLOP per visible (query, key) pair, or the K+V bytes of the keys a
+    row can see."""
+    steps = max(30, min(args.steps, 100))
+
+    def up(a, dt):
+        if dt == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    def timed(call):
+        for _ in range(5):
+            call()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            call()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    def tc_line(name, flops, ms, extra=None):
+        tf = flops / (ms / 1e3) / 1e12
+        d = {"workload": name, "value": round(tf, 2), "unit": "TFLOP/s", "ms_per_call": round(ms, 5),
+             "flops_per_call": flops,
+             "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": pk["bf16_tflops"],
+                          "frac": round(tf / pk["bf16_tflops"], 4), "vs_nominal": vs_nominal(tf, "bf16_tflops")}}
+        d.update(extra or {})
+        return d
+
+    def hbm_line(name, nbytes, ms, extra=None):
+        gbs = nbytes / (ms / 1e3) / 1e9
+        d = {"workload": name, "value": round(gbs, 1), "unit": "GB/s", "ms_per_call": round(ms, 5),
+             "kv_bytes_per_call": nbytes,
+             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"],
+                          "frac": round(gbs / pk["hbm_gbs"], 4), "vs_nominal": vs_nominal(gbs, "hbm_gbs")}}
+        d.update(extra or {})
+        return d
+
+    out = {"steps": steps}
+    q, k, v = (up(px[n], pc.dtype) for n in ("q", "k", "v"))
+    o = torch.empty((pc.B, pc.Hq, pc.Lq, pc.dv), dtype=q.dtype, device=dev)
+    # causal sliding window on the 2x32/8 x 4096 prefill
+    Wp = 1024
+    fl = 2.0 * (pc.d + pc.dv) * pc.B * pc.Hq * window_pairs(pc.Lq, pc.Lk, Wp)
+    ms = timed(lambda: nv.sdpa(q, k, v, mask_kind="causal", scale=pc.scale_f32, window=Wp, out=o, want_lse=False))
+    out["window_prefill"] = tc_line(f"{pc.name}_window{Wp}", fl, ms)
+    # every tensor a transposed [B, L, H, D] view (read and written in place)
+    def tview(t):
+        buf = torch.empty((t.shape[0], t.shape[2], t.shape[1], t.shape[3]), dtype=t.dtype, device=dev)
+        buf.copy_(t.transpose(1, 2))
+        return buf.transpose(1, 2)
+    qt, kt, vt, ot = tview(q), tview(k), tview(v), tview(o)
+    ms = timed(lambda: nv.sdpa(qt, kt, vt, mask_kind="causal", scale=pc.scale_f32, out=ot, want_lse=False))
+    out["strided_prefill"] = tc_line(f"{pc.name}_bLhD_views", prefill_flops(pc), ms)
+    del q, k, v, o, qt, kt, vt, ot
+    # additive mask [1, Hq, Lq, Lk] on the 16/2-head, 1024 x 1801, head-256 prefill
+    mq, mk_, mv = (up(mx[n], mc.dtype) for n in ("q", "k", "v"))
+    ms_ = up(mx["sinks"], mc.dtype)
+    am = torch.randn((1, mc.Hq, mc.Lq, mc.Lk), dtype=mq.dtype, device=dev)
+    mo = torch.empty((mc.B, mc.Hq, mc.Lq, mc.dv), dtype=mq.dtype, device=dev)
+    ms = timed(lambda: nv.sdpa(mq, mk_, mv, mask_kind="add", scale=mc.scale_f32, add_mask=am, sinks=ms_,
+                               out=mo, want_lse=False))
+    out["additive_prefill"] = tc_line(mc.name.replace("bool", "additive"), prefill_flops(mc), ms,
+                                      {"mask_bytes_per_call": am.numel() * 2})
+    del mq, mk_, mv, am, mo
+    # decode: a window of 4096 over the 32769 keys, and the keys in a paged cache
+    dq, dk, dv_ = (up(dx[n], dc.dtype) for n in ("q", "k", "v"))
+    dsk = up(dx["sinks"], dc.dtype)
+    do = torch.empty((dc.B, dc.Hq, dc.Lq, dc.dv), dtype=dq.dtype, device=dev)
+    Wd = 4096
+    ms = timed(lambda: nv.sdpa(dq, dk, dv_, mask_kind="causal", scale=dc.scale_f32, window=Wd, sinks=dsk, out=do,
+                               want_lse=False))
+    out["window_decode"] = hbm_line(f"{dc.name}_window{Wd}", dc.B * dc.Hkv * Wd * (dc.d + dc.dv) * 2.0, ms)
+    bs = 16
+    per = -(-dc.Lk // bs)
+    nblocks = dc.B * per + 7
+    order = torch.randperm(nblocks, generator=torch.Generator().manual_seed(5))[:dc.B * per].to(dev)
+    def to_pages(t):
+        pad = torch.zeros((dc.B, dc.Hkv, per * bs, t.shape[3]), dtype=t.dtype, device=dev)
+        pad[:, :, :dc.Lk] = t
+        blocks = pad.view(dc.B, dc.Hkv, per, bs, t.shape[3]).permute(0, 2, 1, 3, 4).reshape(dc.B * per, dc.Hkv, bs,
+                                                                                         t.shape[3])
+        cache = torch.zeros((nblocks, dc.Hkv, bs, t.shape[3]), dtype=t.dtype, device=dev)
+        cache[order] = blocks
+        return cache
+    kc, vc = to_pages(dk), to_pages(dv_)
+    del dk, dv_
+    table = order.view(dc.B, per).to(torch.int32).contiguous()
+    lens = torch.full((dc.B,), dc.Lk, dtype=torch.int32, device=dev)
+    ms = timed(lambda: nv.sdpa_paged(dq, kc, vc, table, lens, mask_kind="causal", scale=dc.scale_f32, sinks=dsk,
+                                     out=do, want_lse=False))
+    _, ppl = nv.nv_sdpa_paged_plan((dc.B, dc.Hq, dc.Hkv, 1, dc.d, dc.dv, nblocks, bs, per), 1, 0, 0, 1,
+                                   W.DTYPE_CODES[dc.dtype])
+    out["paged_decode"] = hbm_line(f"{dc.name}_paged_bs{bs}", kv_bytes(dc), ms,
+                                   {"block_size": bs, "nblk": ppl["nblk"], "loads": "16-byte cp.async per key row"})
+    del kc, vc, dq, do
+    torch.cuda.synchronize()
+    return out
+
+
 def run_ours(args):
     import torch
     import scaled_dot_product_nv_gb300 as nv
@@ -449,6 +562,9 @@ def run_ours(args):
                      "traffic": recorded_traffic("prefill:" + mc.name)},
     }
 
+    # --------------------------------------------------------------- the options beyond nv_sdpa()
+    features = feature_lines(torch, nv, dev, stream, pk, pc, px, dc, dx, mc, mx, args)
+
     # --------------------------------------------------------------- end to end (host buffers)
     e2e_steps = min(args.steps, 10)
     pin = {n: torch.from_numpy(np.ascontiguousarray(px[n]).view(np.int16)).pin_memory()
@@ -513,6 +629,7 @@ def run_ours(args):
                      "traffic": recorded_traffic("prefill:" + pc.name)},
         "decode": decode,
         "prefill_mask": prefill_mask,
+        "features": features,
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "api": "nv_sdpa_host (pinned host buffers; copies, device alloc, sync inside)"},

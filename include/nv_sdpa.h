@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define NV_SDPA_ABI_VERSION 1
+#define NV_SDPA_ABI_VERSION 2
 
 /* Element types of q, k, v, sinks and out. */
 typedef enum { NV_SDPA_F32 = 0, NV_SDPA_F16 = 1, NV_SDPA_BF16 = 2 } nv_sdpa_dtype;
@@ -51,8 +51,16 @@ typedef enum { NV_SDPA_F32 = 0, NV_SDPA_F16 = 1, NV_SDPA_BF16 = 2 } nv_sdpa_dtyp
  * j <= i + (Lk - Lq) ("nuvec-core 0.5.0 tests/fast.rs", the direct-formula test's
  * visible count i + lk - lq + 1).  With Lq > Lk the first Lq - Lk rows see no key.
  * BOOL reads bool_mask[i * Lk + j] ("nuvec-core 0.5.0 tests/fast.rs", the boolean
- * mask of shape [lq, lk] in the fused-attention tests). */
-typedef enum { NV_SDPA_MASK_NONE = 0, NV_SDPA_MASK_CAUSAL = 1, NV_SDPA_MASK_BOOL = 2 } nv_sdpa_mask;
+ * mask of shape [lq, lk] in the fused-attention tests).  ADD (nv_sdpa_ex only) adds a
+ * float mask in the input dtype to the scaled scores, softmax(scale * q.k + mask)
+ * (same page, the "additive" mask amask of shape [1, hq, lq, lk]); an entry of -inf
+ * hides its key like a false boolean entry. */
+typedef enum {
+  NV_SDPA_MASK_NONE = 0,
+  NV_SDPA_MASK_CAUSAL = 1,
+  NV_SDPA_MASK_BOOL = 2,
+  NV_SDPA_MASK_ADD = 3
+} nv_sdpa_mask;
 
 typedef enum {
   NV_SDPA_OK = 0,
@@ -128,6 +136,94 @@ int nv_sdpa(const void* q, const void* k, const void* v, const nv_sdpa_dims* dim
  * status for them.  `plan` is a host pointer, written on success. */
 int nv_sdpa_plan(const nv_sdpa_dims* dims, int mask_kind, int has_sinks, int dtype,
                  nv_sdpa_plan_t* plan);
+
+/* Optional arguments of nv_sdpa_ex() / nv_sdpa_plan_ex().  Zero-initialise the struct and
+ * set what is used: an all-zero struct (or a NULL pointer) is exactly nv_sdpa().
+ *
+ *   has_window, window  A causal sliding window ("nuvec-core 0.5.0 tests/fast.rs", band /
+ *             window_mask and windows_run_fused_and_equal_the_boolean_mask): with
+ *             has_window = 1, the query at absolute position p = i + Lk - Lq sees key j iff
+ *             p - window < j <= p.  Needs mask_kind CAUSAL and window >= 1; anything else
+ *             is NV_SDPA_ERR_INVALID (window_errors_empty_inputs_and_full_windows: a
+ *             window of 0, or a window without the causal mask, is an error).  A window of
+ *             at least Lk is plain causal attention, bit for bit.  Key blocks and tiles
+ *             wholly outside every row's band are never read; a one-query (Lq = 1)
+ *             f16/bf16 decode cuts its key blocks from the band's first key, so each row
+ *             gets the bits of an unmasked call over exactly its window's keys.
+ *   add_mask, add_mask_b, add_mask_h  mask_kind ADD: device pointer to the mask, dtype,
+ *             contiguous [add_mask_b, add_mask_h, Lq, Lk] with add_mask_b in {1, B} and
+ *             add_mask_h in {1, Hq} (a dimension of 1 is shared by every batch item / query
+ *             head; 0 reads as 1).  Not multiplied by scale.  Must be NULL for other kinds.
+ *   q_strides, k_strides, v_strides, out_strides  Element strides of q, k, v and out
+ *             along their first three dimensions [B, H, L] (the head dimension is always
+ *             contiguous, stride 1).  All three 0 = the contiguous layout.  This covers
+ *             "transposed views of [B, L, H, D]" (strides {L*H*D, D, H*D}) and keys and
+ *             values sliced out of a longer cache ("nuvec-core 0.5.0 tests/fast.rs",
+ *             attention_kernels_match_the_fallback and the windowed-kernel tests), with
+ *             no copy: the tensor-core kernels read them through stride-aware TMA tensor
+ *             maps.  Strides must be >= 0; for f16/bf16 every stride must be a multiple
+ *             of 8 elements (16 bytes, a TMA rule), else NV_SDPA_ERR_UNSUPPORTED.  The
+ *             output must not overlap the inputs; lse stays contiguous [B, Hq, Lq]. */
+typedef struct {
+  int32_t has_window;
+  int32_t reserved0;       /* must be 0 */
+  int64_t window;
+  const void* add_mask;
+  int64_t add_mask_b;
+  int64_t add_mask_h;
+  int64_t q_strides[3];
+  int64_t k_strides[3];
+  int64_t v_strides[3];
+  int64_t out_strides[3];
+} nv_sdpa_options;
+
+/* nv_sdpa_ex: nv_sdpa() with the options above (`opt` is a host pointer, read during the
+ * call only; NULL = no options).  Same ownership, scratch and error behaviour. */
+int nv_sdpa_ex(const void* q, const void* k, const void* v, const nv_sdpa_dims* dims,
+               int mask_kind, const uint8_t* bool_mask, const void* sinks, float scale,
+               const nv_sdpa_options* opt, void* out, float* lse, int dtype, void* stream);
+
+/* nv_sdpa_plan_ex: nv_sdpa_plan() for nv_sdpa_ex(): the same checks (those that need no
+ * device pointer) and the same status. */
+int nv_sdpa_plan_ex(const nv_sdpa_dims* dims, int mask_kind, int has_sinks, int dtype,
+                    const nv_sdpa_options* opt, nv_sdpa_plan_t* plan);
+
+/* Paged key/value caches ("nuvec-core 0.5.0 tests/fast.rs", paged and
+ * paged_attention_equals_contiguous_attention): sizes of nv_sdpa_paged(). */
+typedef struct {
+  int64_t B, Hq, Hkv, Lq, d, dv;
+  int64_t num_blocks;   /* blocks in each cache, >= 1 */
+  int64_t block_size;   /* key positions per block, >= 1 (a multiple of 8 for f16/bf16) */
+  int64_t max_blocks;   /* columns of the block table, >= 1 */
+} nv_sdpa_paged_dims;
+
+/* nv_sdpa_paged: decode attention (Lq <= 8) over paged caches.
+ *   q            device [B, Hq, Lq, d], dtype, contiguous.
+ *   k_cache      device [num_blocks, Hkv, block_size, d], dtype, contiguous.
+ *   v_cache      device [num_blocks, Hkv, block_size, dv], dtype, contiguous.
+ *   block_table  device [B, max_blocks] int32: key j of sequence s is position
+ *                j % block_size of block block_table[s, j / block_size].
+ *   seq_lens     device [B] int32: sequence s has seq_lens[s] keys.
+ *   mask_kind    NONE or CAUSAL (bottom-right against each sequence's own length);
+ *                BOOL and ADD are NV_SDPA_ERR_INVALID, as in the pages' paged tests.
+ *   has_window, window  as in nv_sdpa_options (CAUSAL only; window >= 1).  Blocks wholly
+ *                before a sequence's band are never read.
+ *   sinks, scale, out [B, Hq, Lq, dv], lse [B, Hq, Lq]: as in nv_sdpa().
+ * The result of sequence s equals contiguous attention over its first seq_lens[s] keys
+ * with the same options.  Hostile device inputs are clamped, never dereferenced out of
+ * range ("nuvec-core 0.5.0 tests/fast.rs", paged_attention_clamps_hostile_tables_and_lengths):
+ * a length to [0, max_blocks * block_size], a block id to [0, num_blocks - 1].  Keys past
+ * a sequence's length are never read, whatever the cache holds there.  Lq > 8 is
+ * NV_SDPA_ERR_UNSUPPORTED.  Scratch (split-KV partials, sized from the table's capacity)
+ * comes from the library's pool on `stream`, as in nv_sdpa(). */
+int nv_sdpa_paged(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                  const int32_t* seq_lens, const nv_sdpa_paged_dims* dims, int mask_kind,
+                  int has_window, int64_t window, const void* sinks, float scale, void* out,
+                  float* lse, int dtype, void* stream);
+
+/* nv_sdpa_paged_plan: the plan nv_sdpa_paged() follows (checks that need no pointer). */
+int nv_sdpa_paged_plan(const nv_sdpa_paged_dims* dims, int mask_kind, int has_window, int64_t window,
+                       int has_sinks, int dtype, nv_sdpa_plan_t* plan);
 
 /* nv_sdpa_host: the same operation on HOST buffers (same layouts), for callers without
  * device memory of their own.  Takes one device block from the library's pool (as nv_sdpa

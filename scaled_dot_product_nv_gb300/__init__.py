@@ -5,10 +5,14 @@ module converts Python arguments to C ones and raises on a non-OK status.  There
 no CPU path: if the library is missing, loading it raises.
 
 Raw entry points (same names as the C functions, pointers as ints):
-    nv_sdpa, nv_sdpa_plan, nv_sdpa_host, nv_sdpa_noalloc, nv_sdpa_device_status,
-    nv_sdpa_set_wait_limit, nv_sdpa_status_string, nv_sdpa_abi_version
+    nv_sdpa, nv_sdpa_ex, nv_sdpa_plan, nv_sdpa_plan_ex, nv_sdpa_paged, nv_sdpa_paged_plan,
+    nv_sdpa_host, nv_sdpa_noalloc, nv_sdpa_device_status, nv_sdpa_set_wait_limit,
+    nv_sdpa_status_string, nv_sdpa_abi_version
 Torch convenience (torch tensors for device memory and the current stream):
-    sdpa(q, k, v, mask_kind=..., scale=..., bool_mask=None, sinks=None)
+    sdpa(q, k, v, mask_kind=..., scale=..., bool_mask=None, sinks=None, window=None,
+         add_mask=None)         -- q, k, v, out may be strided views (head dim contiguous)
+    sdpa_paged(q, k_cache, v_cache, block_table, seq_lens, mask_kind=..., scale=...,
+               sinks=None, window=None)
 """
 from __future__ import annotations
 
@@ -21,7 +25,7 @@ LIB_PATH = os.path.join(_PKG, "libnvsdpa.so")
 
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_TIMEOUT = 0, 1, 2, 3, 4
 DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
-MASKS = {"none": 0, "causal": 1, "bool": 2}
+MASKS = {"none": 0, "causal": 1, "bool": 2, "add": 3}
 PATHS = {0: "noop", 1: "no_keys", 2: "prefill", 3: "decode"}
 KERNELS = {0: "none", 1: "fill", 2: "prefill_tc", 3: "tiled_simt", 4: "decode_mma"}
 
@@ -41,6 +45,34 @@ class Plan(ctypes.Structure):
         d["path"] = PATHS.get(self.path, self.path)
         d["kernel"] = KERNELS.get(self.kernel, self.kernel)
         return d
+
+
+class Options(ctypes.Structure):
+    """nv_sdpa_options: window, additive mask, strides (zero = unused / contiguous)."""
+    _fields_ = [("has_window", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+                ("window", ctypes.c_int64), ("add_mask", ctypes.c_void_p),
+                ("add_mask_b", ctypes.c_int64), ("add_mask_h", ctypes.c_int64),
+                ("q_strides", ctypes.c_int64 * 3), ("k_strides", ctypes.c_int64 * 3),
+                ("v_strides", ctypes.c_int64 * 3), ("out_strides", ctypes.c_int64 * 3)]
+
+
+class PagedDims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("B", "Hq", "Hkv", "Lq", "d", "dv", "num_blocks",
+                                              "block_size", "max_blocks")]
+
+
+def make_options(window=None, add_mask=0, add_mask_b=0, add_mask_h=0, q_strides=None,
+                 k_strides=None, v_strides=None, out_strides=None) -> Options:
+    o = Options()
+    if window is not None:
+        o.has_window, o.window = 1, int(window)
+    o.add_mask = add_mask or None
+    o.add_mask_b, o.add_mask_h = int(add_mask_b), int(add_mask_h)
+    for name, st in (("q_strides", q_strides), ("k_strides", k_strides), ("v_strides", v_strides),
+                     ("out_strides", out_strides)):
+        if st is not None:
+            getattr(o, name)[:] = [int(x) for x in st]
+    return o
 
 
 class NvSdpaError(RuntimeError):
@@ -72,6 +104,19 @@ def lib() -> ctypes.CDLL:
         L.nv_sdpa_plan.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                    ctypes.POINTER(Plan)]
         L.nv_sdpa_plan.restype = ctypes.c_int
+        L.nv_sdpa_ex.argtypes = sig[:8] + [ctypes.POINTER(Options)] + sig[8:]
+        L.nv_sdpa_ex.restype = ctypes.c_int
+        L.nv_sdpa_plan_ex.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      ctypes.POINTER(Options), ctypes.POINTER(Plan)]
+        L.nv_sdpa_plan_ex.restype = ctypes.c_int
+        L.nv_sdpa_paged.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(PagedDims), ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_int64, vp, ctypes.c_float, vp, vp,
+                                    ctypes.c_int, vp]
+        L.nv_sdpa_paged.restype = ctypes.c_int
+        L.nv_sdpa_paged_plan.argtypes = [ctypes.POINTER(PagedDims), ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                         ctypes.POINTER(Plan)]
+        L.nv_sdpa_paged_plan.restype = ctypes.c_int
         L.nv_sdpa_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
         L.nv_sdpa_device_status.restype = ctypes.c_int
         L.nv_sdpa_set_wait_limit.argtypes = [ctypes.c_uint64]
@@ -95,6 +140,47 @@ def nv_sdpa(q, k, v, dims, mask_kind, bool_mask, sinks, scale, out, lse, dtype, 
     return lib().nv_sdpa(q, k, v, ctypes.byref(dims), int(mask_kind), bool_mask or None,
                          sinks or None, ctypes.c_float(scale), out, lse or None, int(dtype),
                          stream or None)
+
+
+def nv_sdpa_ex(q, k, v, dims, mask_kind, bool_mask, sinks, scale, options, out, lse, dtype,
+               stream) -> int:
+    """The C call with options (an Options, or None)."""
+    if not isinstance(dims, Dims):
+        dims = _dims(*dims)
+    return lib().nv_sdpa_ex(q, k, v, ctypes.byref(dims), int(mask_kind), bool_mask or None,
+                            sinks or None, ctypes.c_float(scale),
+                            ctypes.byref(options) if options is not None else None, out,
+                            lse or None, int(dtype), stream or None)
+
+
+def nv_sdpa_plan_ex(dims, mask_kind, has_sinks, dtype, options=None):
+    if not isinstance(dims, Dims):
+        dims = _dims(*dims)
+    pl = Plan()
+    st = lib().nv_sdpa_plan_ex(ctypes.byref(dims), int(mask_kind), int(has_sinks), int(dtype),
+                               ctypes.byref(options) if options is not None else None,
+                               ctypes.byref(pl))
+    return st, (pl.as_dict() if st == OK else None)
+
+
+def _paged_dims(dims) -> PagedDims:
+    return dims if isinstance(dims, PagedDims) else PagedDims(*dims)
+
+
+def nv_sdpa_paged(q, k_cache, v_cache, block_table, seq_lens, dims, mask_kind, has_window, window,
+                  sinks, scale, out, lse, dtype, stream) -> int:
+    """The C call; dims a PagedDims or (B, Hq, Hkv, Lq, d, dv, num_blocks, block_size, max_blocks)."""
+    return lib().nv_sdpa_paged(q, k_cache, v_cache, block_table, seq_lens,
+                               ctypes.byref(_paged_dims(dims)), int(mask_kind), int(has_window),
+                               int(window), sinks or None, ctypes.c_float(scale), out, lse or None,
+                               int(dtype), stream or None)
+
+
+def nv_sdpa_paged_plan(dims, mask_kind, has_window, window, has_sinks, dtype):
+    pl = Plan()
+    st = lib().nv_sdpa_paged_plan(ctypes.byref(_paged_dims(dims)), int(mask_kind), int(has_window),
+                                  int(window), int(has_sinks), int(dtype), ctypes.byref(pl))
+    return st, (pl.as_dict() if st == OK else None)
 
 
 def nv_sdpa_host(q, k, v, dims, mask_kind, bool_mask, sinks, scale, out, lse, dtype, stream) -> int:
@@ -169,17 +255,29 @@ def _torch_dtype_code(t):
     return m[t.dtype]
 
 
+def _bhl_strides(t):
+    """Element strides of a 4-D tensor along [B, H, L]; its last dim must be contiguous."""
+    if t.stride(3) != 1 and t.shape[3] > 1:
+        raise ValueError("the head dimension must be contiguous")
+    return tuple(int(x) for x in t.stride()[:3])
+
+
 def sdpa(q, k, v, *, mask_kind: str = "none", scale: Optional[float] = None, bool_mask=None,
-         sinks=None, out=None, lse=None, want_lse: bool = True, stream=None):
+         sinks=None, out=None, lse=None, want_lse: bool = True, stream=None, window=None,
+         add_mask=None):
     """Attention forward on CUDA tensors q [B,Hq,Lq,d], k [B,Hkv,Lk,d], v [B,Hkv,Lk,dv].
 
-    Allocates out (and lse, float32) with torch when not given, launches on the current
-    torch stream (or `stream`, a torch.cuda.Stream), and returns (out, lse or None).
+    q, k, v (and a given out) may be strided views whose last dimension is contiguous
+    (transposed [B, L, H, D] layouts, slices of longer caches); they are read in place.
+    window: a causal sliding window (mask_kind "causal").  add_mask: the additive mask
+    [1|B, 1|Hq, Lq, Lk] of mask_kind "add", in the input dtype.  Allocates out (and lse,
+    float32) with torch when not given, launches on the current torch stream (or `stream`,
+    a torch.cuda.Stream), and returns (out, lse or None).
     """
     import torch
     for t in (q, k, v):
-        if not (t.is_cuda and t.is_contiguous()):
-            raise ValueError("q, k, v must be contiguous CUDA tensors")
+        if not t.is_cuda:
+            raise ValueError("q, k, v must be CUDA tensors")
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("q, k, v must be 4-D")
     B, Hq, Lq, d = q.shape
@@ -191,14 +289,67 @@ def sdpa(q, k, v, *, mask_kind: str = "none", scale: Optional[float] = None, boo
         out = torch.empty((B, Hq, Lq, dv), dtype=q.dtype, device=q.device)
     if lse is None and want_lse:
         lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
+    if lse is not None and not lse.is_contiguous():
+        raise ValueError("lse must be contiguous")
     mk = MASKS[mask_kind] if isinstance(mask_kind, str) else int(mask_kind)
     if bool_mask is not None and bool_mask.dtype != torch.uint8:
         bool_mask = bool_mask.to(torch.uint8)
     st = (stream or torch.cuda.current_stream(q.device)).cuda_stream
-    status = nv_sdpa(q.data_ptr(), k.data_ptr(), v.data_ptr(), (B, Hq, Hkv, Lq, Lk, d, dv), mk,
-                     bool_mask.data_ptr() if (bool_mask is not None and mk == 2) else 0,
-                     sinks.data_ptr() if sinks is not None else 0, float(scale), out.data_ptr(),
-                     lse.data_ptr() if lse is not None else 0, dt, st)
+    plain = (all(t.is_contiguous() for t in (q, k, v, out)) and window is None and add_mask is None
+             and mk != MASKS["add"])
+    if plain:
+        status = nv_sdpa(q.data_ptr(), k.data_ptr(), v.data_ptr(), (B, Hq, Hkv, Lq, Lk, d, dv), mk,
+                         bool_mask.data_ptr() if (bool_mask is not None and mk == 2) else 0,
+                         sinks.data_ptr() if sinks is not None else 0, float(scale), out.data_ptr(),
+                         lse.data_ptr() if lse is not None else 0, dt, st)
+    else:
+        am = 0
+        mb = mh = 0
+        if add_mask is not None:
+            if not add_mask.is_contiguous() or add_mask.dim() != 4:
+                raise ValueError("add_mask must be a contiguous [1|B, 1|Hq, Lq, Lk] tensor")
+            am, mb, mh = add_mask.data_ptr(), add_mask.shape[0], add_mask.shape[1]
+        opts = make_options(window=window, add_mask=am, add_mask_b=mb, add_mask_h=mh,
+                            q_strides=_bhl_strides(q), k_strides=_bhl_strides(k),
+                            v_strides=_bhl_strides(v), out_strides=_bhl_strides(out))
+        status = nv_sdpa_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), (B, Hq, Hkv, Lq, Lk, d, dv), mk,
+                            bool_mask.data_ptr() if (bool_mask is not None and mk == 2) else 0,
+                            sinks.data_ptr() if sinks is not None else 0, float(scale), opts,
+                            out.data_ptr(), lse.data_ptr() if lse is not None else 0, dt, st)
+    if status != OK:
+        raise NvSdpaError(status)
+    return out, lse
+
+
+def sdpa_paged(q, k_cache, v_cache, block_table, seq_lens, *, mask_kind: str = "causal",
+               scale: Optional[float] = None, sinks=None, window=None, out=None, lse=None,
+               want_lse: bool = True, stream=None):
+    """Decode attention over paged caches: q [B,Hq,Lq<=8,d], k_cache [num_blocks,Hkv,bs,d],
+    v_cache [num_blocks,Hkv,bs,dv], block_table [B,max_blocks] int32, seq_lens [B] int32
+    (all CUDA, contiguous).  Returns (out, lse or None)."""
+    import torch
+    for t in (q, k_cache, v_cache, block_table, seq_lens):
+        if not (t.is_cuda and t.is_contiguous()):
+            raise ValueError("paged inputs must be contiguous CUDA tensors")
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_table and seq_lens must be int32")
+    B, Hq, Lq, d = q.shape
+    nb, Hkv, bs, _ = k_cache.shape
+    dv = v_cache.shape[3]
+    dt = _torch_dtype_code(q)
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty((B, Hq, Lq, dv), dtype=q.dtype, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
+    mk = MASKS[mask_kind] if isinstance(mask_kind, str) else int(mask_kind)
+    st = (stream or torch.cuda.current_stream(q.device)).cuda_stream
+    status = nv_sdpa_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
+                           seq_lens.data_ptr(), (B, Hq, Hkv, Lq, d, dv, nb, bs, block_table.shape[1]),
+                           mk, window is not None, int(window or 0),
+                           sinks.data_ptr() if sinks is not None else 0, float(scale), out.data_ptr(),
+                           lse.data_ptr() if lse is not None else 0, dt, st)
     if status != OK:
         raise NvSdpaError(status)
     return out, lse

@@ -92,7 +92,8 @@ int check_dims(const nv_sdpa_dims* dm, int mask_kind, int dtype) {
   if (!dm) return NV_SDPA_ERR_INVALID;
   const nv_sdpa_dims& x = *dm;
   if (dtype != NV_SDPA_F32 && dtype != NV_SDPA_F16 && dtype != NV_SDPA_BF16) return NV_SDPA_ERR_INVALID;
-  if (mask_kind != NV_SDPA_MASK_NONE && mask_kind != NV_SDPA_MASK_CAUSAL && mask_kind != NV_SDPA_MASK_BOOL)
+  if (mask_kind != NV_SDPA_MASK_NONE && mask_kind != NV_SDPA_MASK_CAUSAL && mask_kind != NV_SDPA_MASK_BOOL &&
+      mask_kind != NV_SDPA_MASK_ADD)
     return NV_SDPA_ERR_INVALID;
   if (x.B < 0 || x.Hq < 0 || x.Lq < 0 || x.Lk < 0 || x.Hkv < 1 || x.d < 1 || x.dv < 1)
     return NV_SDPA_ERR_INVALID;
@@ -110,16 +111,119 @@ int check_dims(const nv_sdpa_dims* dm, int mask_kind, int dtype) {
   return NV_SDPA_OK;
 }
 
+// The options of one call, resolved: strides (contiguous when not given), the window
+// and the additive mask's broadcast.
+struct Resolved {
+  int64_t qs[3], ks[3], vs[3], os[3];  // element strides along [B, H, L]
+  int64_t window;                      // 0 = none
+  const void* amask;
+  int64_t am_sb, am_sh;
+  bool qo_packed;                      // q and out contiguous
+};
+
+// Strides of one tensor [n0, n1, n2, width]: contiguous when all three are 0.  Checks that
+// the largest offset is representable and, for 16-bit types, the 16-byte rule of TMA.
+int resolve_strides(const int64_t* given, int64_t n0, int64_t n1, int64_t n2, int64_t width, int dtype,
+                    int64_t* out, bool* contiguous) {
+  const bool none = !given || (given[0] == 0 && given[1] == 0 && given[2] == 0);
+  if (none) {
+    out[2] = width;
+    out[1] = n2 * width;
+    out[0] = n1 * n2 * width;
+    *contiguous = true;
+    return NV_SDPA_OK;
+  }
+  for (int k = 0; k < 3; ++k)
+    if (given[k] < 0) return NV_SDPA_ERR_INVALID;
+  int64_t span = width, t;
+  const int64_t n[3] = {n0, n1, n2};
+  for (int k = 0; k < 3; ++k) {
+    if (n[k] == 0) continue;
+    if (!mul_ok(given[k], n[k] - 1, &t) || __builtin_add_overflow(span, t, &span) || span > (int64_t(1) << 60))
+      return NV_SDPA_ERR_INVALID;
+  }
+  for (int k = 0; k < 3; ++k) out[k] = given[k];
+  *contiguous = out[2] == width && out[1] == n2 * width && out[0] == n1 * n2 * width;
+  if (dtype != NV_SDPA_F32)
+    for (int k = 0; k < 3; ++k)
+      if (out[k] % 8 != 0) return NV_SDPA_ERR_UNSUPPORTED;
+  return NV_SDPA_OK;
+}
+
+int resolve_options(const nv_sdpa_dims& x, int mask_kind, int dtype, const nv_sdpa_options* opt, Resolved* r) {
+  nv_sdpa_options zero;
+  std::memset(&zero, 0, sizeof(zero));
+  const nv_sdpa_options& o = opt ? *opt : zero;
+  std::memset(r, 0, sizeof(*r));
+  if (o.reserved0 != 0 || (o.has_window != 0 && o.has_window != 1)) return NV_SDPA_ERR_INVALID;
+  if (o.has_window) {
+    // "nuvec-core 0.5.0 tests/fast.rs", window_errors_empty_inputs_and_full_windows: a window
+    // of 0, or a window without the causal mask, is an error
+    if (o.window < 1 || mask_kind != NV_SDPA_MASK_CAUSAL) return NV_SDPA_ERR_INVALID;
+    r->window = o.window;
+  } else if (o.window != 0) {
+    return NV_SDPA_ERR_INVALID;
+  }
+  if (mask_kind == NV_SDPA_MASK_ADD) {
+    const int64_t mb = o.add_mask_b ? o.add_mask_b : 1, mh = o.add_mask_h ? o.add_mask_h : 1;
+    if ((mb != 1 && mb != x.B) || (mh != 1 && mh != x.Hq)) return NV_SDPA_ERR_INVALID;
+    int64_t t;
+    if (!mul_ok(x.Lq, x.Lk, &t) || !mul_ok(t, x.Hq, &t) || !mul_ok(t, x.B, &t)) return NV_SDPA_ERR_INVALID;
+    r->amask = o.add_mask;
+    r->am_sh = mh == 1 ? 0 : x.Lq * x.Lk;
+    r->am_sb = mb == 1 ? 0 : mh * x.Lq * x.Lk;
+  } else if (o.add_mask || o.add_mask_b || o.add_mask_h) {
+    return NV_SDPA_ERR_INVALID;
+  }
+  bool qc, kc, vc, oc;
+  int st;
+  if ((st = resolve_strides(o.q_strides, x.B, x.Hq, x.Lq, x.d, dtype, r->qs, &qc)) != NV_SDPA_OK) return st;
+  if ((st = resolve_strides(o.k_strides, x.B, x.Hkv, x.Lk, x.d, dtype, r->ks, &kc)) != NV_SDPA_OK) return st;
+  if ((st = resolve_strides(o.v_strides, x.B, x.Hkv, x.Lk, x.dv, dtype, r->vs, &vc)) != NV_SDPA_OK) return st;
+  if ((st = resolve_strides(o.out_strides, x.B, x.Hq, x.Lq, x.dv, dtype, r->os, &oc)) != NV_SDPA_OK) return st;
+  r->qo_packed = qc && oc;
+  return NV_SDPA_OK;
+}
+
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// What the router needs to know about one call beyond its sizes.
+struct CallShape {
+  nv_sdpa_dims x;   // (paged: Lk = the table's capacity)
+  int64_t span;     // keys one row tile's blocks cover: Lk, or the window's reach
+  bool qo_packed;   // q and out contiguous
+  bool paged;
+};
+
+CallShape call_shape(const nv_sdpa_dims& x, const Resolved& r) {
+  CallShape c{x, x.Lk, r.qo_packed, false};
+  // rows of one tile are at most Lq positions apart: their bands together cover at most
+  // window + Lq - 1 keys
+  if (r.window > 0 && r.window < x.Lk) c.span = std::min<int64_t>(x.Lk, r.window + std::max<int64_t>(x.Lq, 1) - 1);
+  return c;
+}
+
+// The decode key split: blocks of keys_per_blk (a multiple of `quantum`) over `span`
+// keys, enough of them that one batch item alone keeps 2 x (SM count) warps streaming,
+// each at least 256 keys.  Depends on the head shape and the span alone, never on B.
+void split_keys(int64_t span, int64_t units_per_item, int64_t quantum, int64_t* nblk_out, int64_t* kpb_out) {
+  const int64_t sms = device_sm_count();
+  int64_t nblk = cdiv(2 * sms, std::max<int64_t>(1, units_per_item));
+  nblk = std::min(nblk, cdiv(span, 256));
+  nblk = std::max<int64_t>(1, std::min(nblk, merge_max_blocks()));
+  const int64_t kpb = cdiv(cdiv(span, nblk), quantum) * quantum;
+  *kpb_out = kpb;
+  *nblk_out = std::max<int64_t>(1, cdiv(span, kpb));
+}
+
 // The router.  Pure for a given device: depends on its arguments and the current
-// device's SM count only.  The key-block count depends on Lk and the per-batch-item work
-// (Hkv x row tiles), never on B, so that a batch item gets the bits of the same item run
-// alone.
-int make_plan(const nv_sdpa_dims& x, int mask_kind, int has_sinks, int dtype, nv_sdpa_plan_t* pl) {
+// device's SM count only.  The key-block count depends on the span of keys and the
+// per-batch-item work (Hkv x row tiles), never on B, so that a batch item gets the bits
+// of the same item run alone.
+int make_plan(const CallShape& cs, int mask_kind, int has_sinks, int dtype, nv_sdpa_plan_t* pl) {
   (void)has_sinks;
+  const nv_sdpa_dims& x = cs.x;
   std::memset(pl, 0, sizeof(*pl));
-  const int64_t kNumSms = device_sm_count();
   pl->nblk = 1;
   if (x.B == 0 || x.Hq == 0 || x.Lq == 0) {
     pl->path = NV_SDPA_PATH_NOOP;
@@ -135,15 +239,18 @@ int make_plan(const nv_sdpa_dims& x, int mask_kind, int has_sinks, int dtype, nv
     return NV_SDPA_OK;
   }
   pl->path = x.Lq > 8 ? NV_SDPA_PATH_PREFILL : NV_SDPA_PATH_DECODE;
+  if (cs.paged && pl->path != NV_SDPA_PATH_DECODE) return NV_SDPA_ERR_UNSUPPORTED;
+  // the tensor-core kernels index keys and rows in 32 bits (as TMA coordinates are)
+  const bool fits32 = x.Lk < (int64_t(1) << 31) - 1024 && G < (int64_t(1) << 31) - 1024;
+  if (!fits32 && dtype != NV_SDPA_F32) return NV_SDPA_ERR_UNSUPPORTED;
   if (pl->path == NV_SDPA_PATH_PREFILL && prefill_tc_supported(dtype, x.d, x.dv)) {
     // tcgen05 kernel: one CTA per 128 or 256 rows of one KV head, all keys (no split)
+    const PrefillGeom geo = prefill_tc_geometry(x.B, x.Hkv, g, x.Lq, x.d, x.dv, cs.qo_packed);
     pl->kernel = NV_SDPA_KERNEL_PREFILL_TC;
-    pl->rows_per_cta = prefill_tc_rows_per_cta(x.d, x.dv, G);
+    pl->rows_per_cta = 128 * geo.nq;
     pl->keys_per_blk = x.Lk;
-    int64_t grid;
-    if (!mul_ok(x.B * x.Hkv, cdiv(G, pl->rows_per_cta), &grid) || grid > 0x7fffffff)
-      return NV_SDPA_ERR_UNSUPPORTED;
-    pl->grid = grid;
+    if (geo.grid > 0x7fffffff || geo.n_it > 0x7fffffff / 128) return NV_SDPA_ERR_UNSUPPORTED;
+    pl->grid = geo.grid;
     pl->launches = 1;
     if (mask_kind == NV_SDPA_MASK_BOOL) {  // bit-packed copy of the mask
       pl->launches = 2;
@@ -153,34 +260,27 @@ int make_plan(const nv_sdpa_dims& x, int mask_kind, int has_sinks, int dtype, nv
   }
   if (pl->path == NV_SDPA_PATH_DECODE && decode_mma_supported(dtype, x.d, x.dv)) {
     // Tensor-core decode.  The keys of each KV head are cut into blocks that depend on
-    // the head shape and Lk alone, never on B: enough of them that one batch item alone
-    // keeps 2 x 152 warps streaming, each at least 256 keys.  Every block's partial is
-    // computed the same way whichever warp computes it, so a batch item gets the bits
-    // it would get alone.  How many warps share a (b, KV head, 16-row tile)'s blocks
-    // (each walking a contiguous run of them) is free, and is chosen so that all warps
-    // run as one wave: fewer, longer streams read K and V best (measured: one wave at
-    // 85-95 % of the slots beats two full waves, and far beats eight).
+    // the head shape and the span alone, never on B.  Every block's partial is computed
+    // the same way whichever warp computes it, so a batch item gets the bits it would get
+    // alone.  How many warps share a (b, KV head, 16-row tile)'s blocks (each walking a
+    // contiguous run of them) is free, and is chosen so that all warps run as one wave:
+    // fewer, longer streams read K and V best (measured: one wave at 85-95 % of the slots
+    // beats two full waves, and far beats eight).
     pl->kernel = NV_SDPA_KERNEL_DECODE_MMA;
     pl->rows_per_cta = decode_mma_rows_per_warp();
     const int64_t rc = cdiv(G, pl->rows_per_cta);
-    int64_t nblk = cdiv(2 * kNumSms, x.Hkv * rc);
-    nblk = std::min(nblk, cdiv(x.Lk, 256));
-    nblk = std::max<int64_t>(1, std::min(nblk, merge_max_blocks()));
-    const int64_t kpb = cdiv(cdiv(x.Lk, nblk), 64) * 64;  // whole key tiles
-    nblk = cdiv(x.Lk, kpb);
-    pl->nblk = nblk;
-    pl->keys_per_blk = kpb;
+    split_keys(cs.span, x.Hkv * rc, 64, &pl->nblk, &pl->keys_per_blk);
     int64_t units, warp_units;
-    if (!mul_ok(x.B * x.Hkv, rc, &units) || !mul_ok(units, decode_spans(x, nblk), &warp_units))
+    if (!mul_ok(x.B * x.Hkv, rc, &units) || !mul_ok(units, decode_spans(x, pl->nblk), &warp_units))
       return NV_SDPA_ERR_UNSUPPORTED;
     const int64_t grid = decode_mma_grid(warp_units, x.d, x.dv);
     if (grid > 0x7fffffff) return NV_SDPA_ERR_UNSUPPORTED;
     pl->grid = grid;
-    pl->launches = nblk > 1 ? 2 : 1;
-    if (nblk > 1) {
+    pl->launches = pl->nblk > 1 ? 2 : 1;
+    if (pl->nblk > 1) {
       const int64_t rows = x.B * x.Hq * x.Lq;
       if (rows > 0x7fffffff) return NV_SDPA_ERR_UNSUPPORTED;  // the merge grid: one CTA per row
-      pl->scratch_bytes = cdiv(rows * nblk * x.dv * 4, 256) * 256 + rows * nblk * 2 * 4;
+      pl->scratch_bytes = cdiv(rows * pl->nblk * x.dv * 4, 256) * 256 + rows * pl->nblk * 2 * 4;
     }
     return NV_SDPA_OK;
   }
@@ -189,26 +289,17 @@ int make_plan(const nv_sdpa_dims& x, int mask_kind, int has_sinks, int dtype, nv
   pl->kernel = NV_SDPA_KERNEL_TILED_SIMT;
   pl->rows_per_cta = tiled_simt_rows_per_cta();
   const int64_t row_tiles = cdiv(G, pl->rows_per_cta);
-  const int64_t units = x.Hkv * row_tiles;     // CTAs per batch item with one block
-  const int64_t kMinKeys = 256;                  // keys per block, at least
-  const int64_t kTargetCtas = 2 * kNumSms;       // per batch item
-  int64_t nblk = cdiv(kTargetCtas, units);
-  nblk = std::min(nblk, cdiv(x.Lk, kMinKeys));
-  nblk = std::max<int64_t>(1, std::min(nblk, merge_max_blocks()));
-  int64_t kpb = cdiv(cdiv(x.Lk, nblk), 128) * 128;  // multiple of every key tile
-  nblk = cdiv(x.Lk, kpb);
-  pl->nblk = nblk;
-  pl->keys_per_blk = kpb;
+  split_keys(cs.span, x.Hkv * row_tiles, 128, &pl->nblk, &pl->keys_per_blk);
   int64_t grid;
-  if (!mul_ok(x.B * x.Hkv, row_tiles, &grid) || !mul_ok(grid, nblk, &grid) || grid > 0x7fffffff)
+  if (!mul_ok(x.B * x.Hkv, row_tiles, &grid) || !mul_ok(grid, pl->nblk, &grid) || grid > 0x7fffffff)
     return NV_SDPA_ERR_UNSUPPORTED;
   pl->grid = grid;
-  pl->launches = nblk > 1 ? 2 : 1;
-  if (nblk > 1) {
+  pl->launches = pl->nblk > 1 ? 2 : 1;
+  if (pl->nblk > 1) {
     const int64_t rows = x.B * x.Hq * x.Lq;
     if (rows > 0x7fffffff) return NV_SDPA_ERR_UNSUPPORTED;  // the merge grid: one CTA per row
-    const int64_t o_bytes = cdiv(rows * nblk * x.dv * 4, 256) * 256;
-    pl->scratch_bytes = o_bytes + rows * nblk * 2 * 4;
+    const int64_t o_bytes = cdiv(rows * pl->nblk * x.dv * 4, 256) * 256;
+    pl->scratch_bytes = o_bytes + rows * pl->nblk * 2 * 4;
   }
   return NV_SDPA_OK;
 }
@@ -248,12 +339,37 @@ NV_SDPA_API const char* nv_sdpa_status_string(int s) {
   }
 }
 
-NV_SDPA_API int nv_sdpa_plan(const nv_sdpa_dims* dims, int mask_kind, int has_sinks, int dtype,
-                             nv_sdpa_plan_t* plan) {
-  if (!plan) return NV_SDPA_ERR_INVALID;
+namespace nvsdpa {
+namespace {
+// Every check of a (non-paged) call that needs no device pointer; on success *r holds the
+// resolved options and *cs the router's view of the call.  The entry points without
+// options take no additive mask.
+int check_call(const nv_sdpa_dims* dims, int mask_kind, int dtype, const nv_sdpa_options* opt, Resolved* r,
+               CallShape* cs) {
   int st = check_dims(dims, mask_kind, dtype);
   if (st != NV_SDPA_OK) return st;
-  return make_plan(*dims, mask_kind, has_sinks, dtype, plan);
+  if (mask_kind == NV_SDPA_MASK_ADD && (!opt || !opt->add_mask)) return NV_SDPA_ERR_INVALID;
+  st = resolve_options(*dims, mask_kind, dtype, opt, r);
+  if (st != NV_SDPA_OK) return st;
+  *cs = call_shape(*dims, *r);
+  return NV_SDPA_OK;
+}
+}  // namespace
+}  // namespace nvsdpa
+
+NV_SDPA_API int nv_sdpa_plan_ex(const nv_sdpa_dims* dims, int mask_kind, int has_sinks, int dtype,
+                                const nv_sdpa_options* opt, nv_sdpa_plan_t* plan) {
+  if (!plan) return NV_SDPA_ERR_INVALID;
+  Resolved r;
+  CallShape cs;
+  int st = check_call(dims, mask_kind, dtype, opt, &r, &cs);
+  if (st != NV_SDPA_OK) return st;
+  return make_plan(cs, mask_kind, has_sinks, dtype, plan);
+}
+
+NV_SDPA_API int nv_sdpa_plan(const nv_sdpa_dims* dims, int mask_kind, int has_sinks, int dtype,
+                             nv_sdpa_plan_t* plan) {
+  return nv_sdpa_plan_ex(dims, mask_kind, has_sinks, dtype, nullptr, plan);
 }
 
 NV_SDPA_API int nv_sdpa_set_wait_limit(uint64_t spins) {
@@ -264,17 +380,36 @@ NV_SDPA_API int nv_sdpa_set_wait_limit(uint64_t spins) {
 namespace nvsdpa {
 namespace {
 
-// Everything nv_sdpa() and nv_sdpa_noalloc() check before launching, and the launch
-// parameters of the call's plan.  Returns NV_SDPA_OK (with *pl and *p filled) or the
+// Launch parameters common to every call: sizes, the split, the scale and the wait budget.
+void fill_common(Params* p, const nv_sdpa_dims& x, const nv_sdpa_plan_t& pl, int mask_kind, const void* sinks,
+                 float scale) {
+  p->B = x.B; p->Hq = x.Hq; p->Hkv = x.Hkv; p->Lq = x.Lq; p->Lk = x.Lk; p->d = x.d; p->dv = x.dv;
+  p->g = x.Hq / x.Hkv; p->G = p->g * x.Lq;
+  p->nblk = pl.nblk; p->keys_per_blk = pl.keys_per_blk;
+  p->row_tiles = pl.rows_per_cta ? (p->G + pl.rows_per_cta - 1) / pl.rows_per_cta : 1;
+  p->spans = pl.kernel == NV_SDPA_KERNEL_DECODE_MMA ? decode_spans(x, pl.nblk) : 1;
+  p->mask_kind = mask_kind;
+  p->sinks = sinks;
+  p->has_sinks = sinks != nullptr;
+  p->scale = scale;
+  p->scale_log2 = (float)((double)scale * 1.4426950408889634);
+  const uint64_t wl = g_wait_limit.load();
+  p->wait_limit = wl ? wl : kDefaultWaitLimit;
+}
+
+// Everything nv_sdpa_ex(), nv_sdpa() and nv_sdpa_noalloc() check before launching, and the
+// launch parameters of the call's plan.  Returns NV_SDPA_OK (with *pl and *p filled) or the
 // status to return; nothing has been launched or allocated either way.
 int prepare_call(const void* q, const void* k, const void* v, const nv_sdpa_dims* dims, int mask_kind,
-                 const uint8_t* bool_mask, const void* sinks, float scale, void* out, float* lse, int dtype,
-                 nv_sdpa_plan_t* pl, Params* p) {
-  int st = check_dims(dims, mask_kind, dtype);
+                 const uint8_t* bool_mask, const void* sinks, float scale, const nv_sdpa_options* opt, void* out,
+                 float* lse, int dtype, nv_sdpa_plan_t* pl, Params* p) {
+  Resolved r;
+  CallShape cs;
+  int st = check_call(dims, mask_kind, dtype, opt, &r, &cs);
   if (st != NV_SDPA_OK) return st;
   if (!std::isfinite(scale)) return NV_SDPA_ERR_INVALID;
   const nv_sdpa_dims& x = *dims;
-  st = make_plan(x, mask_kind, sinks != nullptr, dtype, pl);
+  st = make_plan(cs, mask_kind, sinks != nullptr, dtype, pl);
   if (st != NV_SDPA_OK) return st;
   if (pl->path == NV_SDPA_PATH_NOOP) return NV_SDPA_OK;
   // pointers: required ones present and aligned
@@ -285,22 +420,22 @@ int prepare_call(const void* q, const void* k, const void* v, const nv_sdpa_dims
   if (pl->path != NV_SDPA_PATH_NO_KEYS) {
     if (!q || !k || !v || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16)) return NV_SDPA_ERR_INVALID;
     if (mask_kind == NV_SDPA_MASK_BOOL && !bool_mask) return NV_SDPA_ERR_INVALID;
+    if (mask_kind == NV_SDPA_MASK_ADD && !aligned(r.amask, 16)) return NV_SDPA_ERR_INVALID;
   }
   *p = Params{};
   p->q = q; p->k = k; p->v = v;
   p->mask = mask_kind == NV_SDPA_MASK_BOOL ? bool_mask : nullptr;
-  p->sinks = sinks; p->out = out; p->lse = lse;
-  p->B = x.B; p->Hq = x.Hq; p->Hkv = x.Hkv; p->Lq = x.Lq; p->Lk = x.Lk; p->d = x.d; p->dv = x.dv;
-  p->g = x.Hq / x.Hkv; p->G = p->g * x.Lq;
-  p->nblk = pl->nblk; p->keys_per_blk = pl->keys_per_blk;
-  p->row_tiles = pl->rows_per_cta ? (p->G + pl->rows_per_cta - 1) / pl->rows_per_cta : 1;
-  p->spans = pl->kernel == NV_SDPA_KERNEL_DECODE_MMA ? decode_spans(x, pl->nblk) : 1;
-  p->mask_kind = mask_kind;
-  p->has_sinks = sinks != nullptr;
-  p->scale = scale;
-  p->scale_log2 = (float)((double)scale * 1.4426950408889634);
-  const uint64_t wl = g_wait_limit.load();
-  p->wait_limit = wl ? wl : kDefaultWaitLimit;
+  p->out = out; p->lse = lse;
+  fill_common(p, x, *pl, mask_kind, sinks, scale);
+  p->q_sb = r.qs[0]; p->q_sh = r.qs[1]; p->q_sl = r.qs[2];
+  p->k_sb = r.ks[0]; p->k_sh = r.ks[1]; p->k_sl = r.ks[2];
+  p->v_sb = r.vs[0]; p->v_sh = r.vs[1]; p->v_sl = r.vs[2];
+  p->o_sb = r.os[0]; p->o_sh = r.os[1]; p->o_sl = r.os[2];
+  p->qo_packed = r.qo_packed ? 1 : 0;
+  p->window = r.window;
+  p->amask = r.amask;
+  p->am_sb = r.am_sb;
+  p->am_sh = r.am_sh;
   return NV_SDPA_OK;
 }
 
@@ -330,13 +465,10 @@ cudaError_t launch_plan(int dtype, const nv_sdpa_plan_t& pl, Params& p, void* sc
 }  // namespace
 }  // namespace nvsdpa
 
-NV_SDPA_API int nv_sdpa(const void* q, const void* k, const void* v, const nv_sdpa_dims* dims,
-                        int mask_kind, const uint8_t* bool_mask, const void* sinks, float scale,
-                        void* out, float* lse, int dtype, void* stream) {
-  nv_sdpa_plan_t pl;
-  Params p;
-  int st = prepare_call(q, k, v, dims, mask_kind, bool_mask, sinks, scale, out, lse, dtype, &pl, &p);
-  if (st != NV_SDPA_OK || pl.path == NV_SDPA_PATH_NOOP) return st;
+namespace nvsdpa {
+namespace {
+// Runs a prepared call with its scratch from the library's pool on `stream`.
+int run_pooled(int dtype, const nv_sdpa_plan_t& pl, Params& p, void* stream) {
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   void* scratch = nullptr;
   if (pl.scratch_bytes && pool_alloc(&scratch, (size_t)pl.scratch_bytes, cs) != cudaSuccess)
@@ -347,6 +479,102 @@ NV_SDPA_API int nv_sdpa(const void* q, const void* k, const void* v, const nv_sd
     if (ce == cudaSuccess) ce = fe;
   }
   return ce == cudaSuccess ? NV_SDPA_OK : NV_SDPA_ERR_CUDA;
+}
+}  // namespace
+}  // namespace nvsdpa
+
+NV_SDPA_API int nv_sdpa_ex(const void* q, const void* k, const void* v, const nv_sdpa_dims* dims,
+                           int mask_kind, const uint8_t* bool_mask, const void* sinks, float scale,
+                           const nv_sdpa_options* opt, void* out, float* lse, int dtype, void* stream) {
+  nv_sdpa_plan_t pl;
+  Params p;
+  int st = prepare_call(q, k, v, dims, mask_kind, bool_mask, sinks, scale, opt, out, lse, dtype, &pl, &p);
+  if (st != NV_SDPA_OK || pl.path == NV_SDPA_PATH_NOOP) return st;
+  return run_pooled(dtype, pl, p, stream);
+}
+
+NV_SDPA_API int nv_sdpa(const void* q, const void* k, const void* v, const nv_sdpa_dims* dims,
+                        int mask_kind, const uint8_t* bool_mask, const void* sinks, float scale,
+                        void* out, float* lse, int dtype, void* stream) {
+  return nv_sdpa_ex(q, k, v, dims, mask_kind, bool_mask, sinks, scale, nullptr, out, lse, dtype, stream);
+}
+
+namespace nvsdpa {
+namespace {
+// Checks of a paged call that need no device pointer; fills the router's view (Lk = the
+// table's capacity).
+int check_paged(const nv_sdpa_paged_dims* pd, int mask_kind, int has_window, int64_t window, int dtype,
+                nv_sdpa_dims* x, CallShape* cs) {
+  if (!pd) return NV_SDPA_ERR_INVALID;
+  if (mask_kind != NV_SDPA_MASK_NONE && mask_kind != NV_SDPA_MASK_CAUSAL) return NV_SDPA_ERR_INVALID;
+  if (has_window != 0 && has_window != 1) return NV_SDPA_ERR_INVALID;
+  if (has_window && (window < 1 || mask_kind != NV_SDPA_MASK_CAUSAL)) return NV_SDPA_ERR_INVALID;
+  if (pd->num_blocks < 1 || pd->block_size < 1 || pd->max_blocks < 1) return NV_SDPA_ERR_INVALID;
+  int64_t cap, t;
+  if (!mul_ok(pd->max_blocks, pd->block_size, &cap) || cap > 0x7fffffff) return NV_SDPA_ERR_INVALID;
+  if (!mul_ok(pd->B, pd->max_blocks, &t)) return NV_SDPA_ERR_INVALID;
+  const int64_t e = elt_bytes(dtype);
+  if (pd->Hkv < 1 || !mul_ok(pd->num_blocks, pd->Hkv, &t) || !mul_ok(t, pd->block_size, &t) ||
+      !mul_ok(t, std::max(pd->d, pd->dv), &t) || !mul_ok(t, e, &t))
+    return NV_SDPA_ERR_INVALID;
+  *x = nv_sdpa_dims{pd->B, pd->Hq, pd->Hkv, pd->Lq, cap, pd->d, pd->dv};
+  int st = check_dims(x, mask_kind, dtype);
+  if (st != NV_SDPA_OK) return st;
+  if (x->Lq > 8) return NV_SDPA_ERR_UNSUPPORTED;  // paged caches serve the decode path
+  cs->x = *x;
+  cs->span = cap;
+  if (has_window && window < cap) cs->span = std::min<int64_t>(cap, window + std::max<int64_t>(x->Lq, 1) - 1);
+  cs->qo_packed = true;
+  cs->paged = true;
+  return NV_SDPA_OK;
+}
+}  // namespace
+}  // namespace nvsdpa
+
+NV_SDPA_API int nv_sdpa_paged_plan(const nv_sdpa_paged_dims* dims, int mask_kind, int has_window, int64_t window,
+                                   int has_sinks, int dtype, nv_sdpa_plan_t* plan) {
+  if (!plan) return NV_SDPA_ERR_INVALID;
+  nv_sdpa_dims x;
+  CallShape cs;
+  int st = check_paged(dims, mask_kind, has_window, window, dtype, &x, &cs);
+  if (st != NV_SDPA_OK) return st;
+  return make_plan(cs, mask_kind, has_sinks, dtype, plan);
+}
+
+NV_SDPA_API int nv_sdpa_paged(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                              const int32_t* seq_lens, const nv_sdpa_paged_dims* dims, int mask_kind,
+                              int has_window, int64_t window, const void* sinks, float scale, void* out,
+                              float* lse, int dtype, void* stream) {
+  nv_sdpa_dims x;
+  CallShape cs;
+  int st = check_paged(dims, mask_kind, has_window, window, dtype, &x, &cs);
+  if (st != NV_SDPA_OK) return st;
+  if (!std::isfinite(scale)) return NV_SDPA_ERR_INVALID;
+  nv_sdpa_plan_t pl;
+  st = make_plan(cs, mask_kind, sinks != nullptr, dtype, &pl);
+  if (st != NV_SDPA_OK || pl.path == NV_SDPA_PATH_NOOP) return st;
+  const int64_t e = elt_bytes(dtype);
+  if (!q || !k_cache || !v_cache || !out || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(out, 16))
+    return NV_SDPA_ERR_INVALID;
+  if (!block_table || !seq_lens || !aligned(block_table, 4) || !aligned(seq_lens, 4)) return NV_SDPA_ERR_INVALID;
+  if (lse && !aligned(lse, 4)) return NV_SDPA_ERR_INVALID;
+  if (sinks && !aligned(sinks, (uintptr_t)e)) return NV_SDPA_ERR_INVALID;
+  Params p{};
+  p.q = q; p.k = k_cache; p.v = v_cache;
+  p.out = out; p.lse = lse;
+  fill_common(&p, x, pl, mask_kind, sinks, scale);
+  p.q_sl = x.d; p.q_sh = x.Lq * x.d; p.q_sb = x.Hq * x.Lq * x.d;
+  p.o_sl = x.dv; p.o_sh = x.Lq * x.dv; p.o_sb = x.Hq * x.Lq * x.dv;
+  p.qo_packed = 1;
+  p.window = has_window ? window : 0;
+  p.paged = 1;
+  p.table = block_table;
+  p.lens = seq_lens;
+  p.page = dims->block_size;
+  p.max_pages = dims->max_blocks;
+  p.num_pages = dims->num_blocks;
+  return run_pooled(dtype, pl, p, stream);
 }
 
 NV_SDPA_API int nv_sdpa_device_status(void* stream, uint32_t* detail) {
@@ -436,7 +664,9 @@ std::vector<HostChunk> host_chunks(const nv_sdpa_dims& x, int kernel, size_t h2d
 NV_SDPA_API int nv_sdpa_host(const void* q, const void* k, const void* v, const nv_sdpa_dims* dims,
                              int mask_kind, const uint8_t* bool_mask, const void* sinks, float scale,
                              void* out, float* lse, int dtype, void* stream) {
-  int st = check_dims(dims, mask_kind, dtype);
+  Resolved r;
+  CallShape shape;
+  int st = check_call(dims, mask_kind, dtype, nullptr, &r, &shape);
   if (st != NV_SDPA_OK) return st;
   if (!std::isfinite(scale)) return NV_SDPA_ERR_INVALID;
   const nv_sdpa_dims& x = *dims;
@@ -447,7 +677,7 @@ NV_SDPA_API int nv_sdpa_host(const void* q, const void* k, const void* v, const 
   if ((nq && !q) || (nk && !k) || (nv && !v) || (no && !out)) return NV_SDPA_ERR_INVALID;
   if (mask_kind == NV_SDPA_MASK_BOOL && nm && !bool_mask) return NV_SDPA_ERR_INVALID;
   nv_sdpa_plan_t pl;
-  st = make_plan(x, mask_kind, sinks != nullptr, dtype, &pl);
+  st = make_plan(shape, mask_kind, sinks != nullptr, dtype, &pl);
   if (st != NV_SDPA_OK) return st;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const bool use_mask = mask_kind == NV_SDPA_MASK_BOOL && nm;
@@ -588,7 +818,7 @@ NV_SDPA_API int nv_sdpa_noalloc(const void* q, const void* k, const void* v, con
                                 void* out, float* lse, int dtype, void* stream) {
   nv_sdpa_plan_t pl;
   Params p;
-  int st = prepare_call(q, k, v, dims, mask_kind, bool_mask, sinks, scale, out, lse, dtype, &pl, &p);
+  int st = prepare_call(q, k, v, dims, mask_kind, bool_mask, sinks, scale, nullptr, out, lse, dtype, &pl, &p);
   if (st != NV_SDPA_OK || pl.path == NV_SDPA_PATH_NOOP) return st;
   if (pl.scratch_bytes > (int64_t)NV_SDPA_STATIC_SCRATCH_BYTES) return NV_SDPA_ERR_UNSUPPORTED;
   cudaError_t ce = cudaSuccess;

@@ -135,59 +135,121 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
   const int64_t rc = unit % a.n_rc;
   const int64_t bh = unit / a.n_rc;
   const int64_t b = bh / p.Hkv, hkv = bh % p.Hkv;
+  const int64_t Lkb = seq_keys(p, b);
+  const int64_t rows_here = (p.G - rc * kRowsDec < kRowsDec) ? p.G - rc * kRowsDec : kRowsDec;
+
+  // The keys any row of the tile may see, [u_lo, u_hi): the blocks of the plan's split are
+  // cut from u_lo (with a window, the band's first key), so that a one-query row's blocks
+  // are those of a call over exactly its band.
+  const int64_t r0 = rc * kRowsDec, r1 = r0 + rows_here - 1;
+  const bool one_head = r0 / p.Lq == r1 / p.Lq;
+  const int64_t imin = one_head ? r0 % p.Lq : 0, imax = one_head ? r1 % p.Lq : p.Lq - 1;
+  const int64_t u_lo = row_key_lo(p, imin + Lkb - p.Lq);
+  const int64_t u_hi = row_key_hi(p, imax + Lkb - p.Lq, Lkb);
   const int64_t c_begin = span * p.nblk / p.spans, c_end = (span + 1) * p.nblk / p.spans;
-  const int64_t key_begin = c_begin * p.keys_per_blk;
-  const int64_t key_end = (c_end * p.keys_per_blk < p.Lk) ? c_end * p.keys_per_blk : p.Lk;
-  const int n_tiles = (int)((key_end - key_begin + kKT - 1) / kKT);
+  const int64_t key_begin = u_lo + c_begin * p.keys_per_blk;
+  int64_t key_end = u_lo + c_end * p.keys_per_blk;
+  if (key_end > u_hi) key_end = u_hi;
+  const int n_tiles = key_end > key_begin ? (int)((key_end - key_begin + kKT - 1) / kKT) : 0;
   const int tpb = (int)(p.keys_per_blk / kKT);  // tiles per (full) key block
   const uint64_t limit = p.wait_limit;
 
-  // tile i of the run into ring slot i % ST (lane 0)
+  // tile i of the run into ring slot i % ST: by TMA (lane 0), or for paged caches by
+  // 16-byte copies of every lane, key row by key row through the page table (rows outside
+  // [key_begin, key_end) and columns past the head are zero-filled, never read)
+  const T* kg = reinterpret_cast<const T*>(p.k);
+  const T* vg = reinterpret_cast<const T*>(p.v);
+  const int ck = (int)(p.d / 8), cv = (int)(p.dv / 8);   // 16-byte chunks of a K / V row
+  const int pk = a.dpanels * 8, pv = a.dvpanels * 8;     // chunks of a panelled smem row
   auto issue = [&](int i) {
     const int s = i % ST;
-    mbar_arrive_expect_tx(full(s), stage_bytes);
-    const int key0 = (int)(key_begin + (int64_t)i * kKT);
-    for (int pn = 0; pn < a.dpanels; ++pn)
-      tma_load_3d(ring + s * stage_bytes + pn * kKT * 128, &a.tmk, full(s), pn * 64, key0, (int)bh);
-    for (int pn = 0; pn < a.dvpanels; ++pn)
-      tma_load_3d(ring + s * stage_bytes + k_bytes + pn * kKT * 128, &a.tmv, full(s), pn * 64, key0, (int)bh);
+    const int64_t key0 = key_begin + (int64_t)i * kKT;
+    if (!p.paged) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(full(s), stage_bytes);
+        for (int pn = 0; pn < a.dpanels; ++pn)
+          tma_load_4d(ring + s * stage_bytes + pn * kKT * 128, &a.tmk, full(s), pn * 64, (int)key0, (int)hkv, (int)b);
+        for (int pn = 0; pn < a.dvpanels; ++pn)
+          tma_load_4d(ring + s * stage_bytes + k_bytes + pn * kKT * 128, &a.tmv, full(s), pn * 64, (int)key0,
+                      (int)hkv, (int)b);
+      }
+      return;
+    }
+    const int per_row = pk + pv;
+    for (int e = lane; e < kKT * per_row; e += 32) {
+      const int r = e / per_row, cc = e - r * per_row;
+      const int64_t j = key0 + r;
+      const bool is_k = cc < pk;
+      const int ch = is_k ? cc : cc - pk;               // chunk within the K or V row
+      const bool in = j < key_end && ch < (is_k ? ck : cv);
+      const T* src = kg;
+      if (in)
+        src = is_k ? kg + kv_offset(p, b, hkv, j, 0, 0, 0, p.d) + ch * 8
+                   : vg + kv_offset(p, b, hkv, j, 0, 0, 0, p.dv) + ch * 8;
+      const uint32_t panel = ring + s * stage_bytes + (is_k ? 0u : k_bytes) + (ch >> 3) * kKT * 128;
+      cp_async16_zfill(sw128(panel, r, ch & 7), src, in ? 16u : 0u);
+    }
+  };
+  // waits until tile i has landed in its slot (bounded for TMA; the paged copies are this
+  // warp's own and always complete)
+  auto landed = [&](int i) -> bool {
+    if (!p.paged) return __all_sync(0xffffffffu, mbar_wait(full(i % ST), (i / ST) & 1, limit, nullptr));
+    __syncwarp();
+    return true;
   };
   int issued = n_tiles < ST ? n_tiles : ST;
-  if (lane == 0) {
+  if (!p.paged && lane == 0) {
     tma_prefetch_desc(&a.tmk);
     tma_prefetch_desc(&a.tmv);
-    for (int i = 0; i < issued; ++i) issue(i);
+  }
+  for (int i = 0; i < ST; ++i) {
+    if (i < issued) issue(i);
+    if (p.paged) cp_async_commit();  // one group per slot, empty ones included
   }
 
-  // This lane's two query rows (gid and gid + 8 of the row tile).
-  const int64_t rows_here = (p.G - rc * kRowsDec < kRowsDec) ? p.G - rc * kRowsDec : kRowsDec;
-  int64_t ri[2], last[2];
+  // This lane's two query rows (gid and gid + 8 of the row tile): the keys [lo, hi) each
+  // may see (32-bit: the planner sends no longer sequence here) and its mask row (boolean
+  // bytes or additive values, by mask kind).
+  int lo[2], hi[2];
   bool rok[2];
-  const uint8_t* mrow[2];
+  const void* mk[2];
+  const bool bool_mask = p.mask_kind == kMaskBool, add_mask = p.mask_kind == kMaskAdd;
 #pragma unroll
   for (int hrow = 0; hrow < 2; ++hrow) {
     const int r = gid + 8 * hrow;
     rok[hrow] = r < rows_here;
-    const int64_t rho = rc * kRowsDec + r;
-    ri[hrow] = rok[hrow] ? rho % p.Lq : 0;
-    last[hrow] = (p.mask_kind == kMaskCausal) ? causal_last_key(p, ri[hrow]) : p.Lk - 1;
-    mrow[hrow] = (p.mask_kind == kMaskBool) ? p.mask + ri[hrow] * p.Lk : nullptr;
+    const int64_t rho = rc * kRowsDec + (rok[hrow] ? r : 0);
+    const int64_t i = rho % p.Lq, h = hkv * p.g + rho / p.Lq;
+    const int64_t pos = i + Lkb - p.Lq;
+    lo[hrow] = (int)row_key_lo(p, pos);
+    hi[hrow] = (int)row_key_hi(p, pos, Lkb);
+    mk[hrow] = bool_mask ? static_cast<const void*>(p.mask + i * p.Lk)
+                         : (add_mask ? static_cast<const void*>(reinterpret_cast<const T*>(p.amask) + b * p.am_sb +
+                                                                h * p.am_sh + i * p.Lk)
+                                     : nullptr);
   }
 
   // Q fragments (A operand, row-major m16 x k16 per k-block), straight from global memory.
   constexpr int kKB = DMAX / 16;  // k-blocks of the d bucket
   const int nkb = (int)((p.d + 15) / 16);
   uint32_t qa[kKB][4];
-  const T* qbase = reinterpret_cast<const T*>(p.q) + (bh * p.G + rc * kRowsDec) * p.d;
+  {
+    const T* qrow[2];
 #pragma unroll
-  for (int kb = 0; kb < kKB; ++kb) {
+    for (int hrow = 0; hrow < 2; ++hrow) {
+      const int64_t rho = rc * kRowsDec + (rok[hrow] ? gid + 8 * hrow : 0);
+      qrow[hrow] = reinterpret_cast<const T*>(p.q) + q_offset(p, b, hkv * p.g + rho / p.Lq, rho % p.Lq);
+    }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int r = gid + 8 * (e & 1);
-      const int c = kb * 16 + 2 * tig + 8 * (e >> 1);
-      uint32_t v = 0;
-      if (kb < nkb && r < rows_here && c < p.d) v = *reinterpret_cast<const uint32_t*>(qbase + r * p.d + c);
-      qa[kb][e] = v;
+    for (int kb = 0; kb < kKB; ++kb) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int hrow = e & 1;
+        const int c = kb * 16 + 2 * tig + 8 * (e >> 1);
+        uint32_t v = 0;
+        if (kb < nkb && rok[hrow] && c < p.d) v = *reinterpret_cast<const uint32_t*>(qrow[hrow] + c);
+        qa[kb][e] = v;
+      }
     }
   }
 
@@ -199,15 +261,71 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
   int consumed = 0;
 
+  // The partial of key block c from this warp's running (m, l, o) -- or, with a single
+  // block, the final output -- and a fresh start for the next block.
+  auto flush = [&](int64_t c) {
+    float L[2];
+#pragma unroll
+    for (int hrow = 0; hrow < 2; ++hrow) {
+      L[hrow] = l[hrow] + __shfl_xor_sync(0xffffffffu, l[hrow], 1);
+      L[hrow] += __shfl_xor_sync(0xffffffffu, L[hrow], 2);
+    }
+#pragma unroll
+    for (int hrow = 0; hrow < 2; ++hrow) {
+      if (!rok[hrow]) continue;
+      const int64_t rho = rc * kRowsDec + gid + 8 * hrow;
+      const int64_t ri = rho % p.Lq, hr = hkv * p.g + rho / p.Lq;
+      const int64_t row_global = (b * p.Hq + hr) * p.Lq + ri;
+      const float M = m[hrow];
+      if (p.nblk == 1) {
+        const float sk = sink_log2<T>(p, hr);
+        const float Mf = fmaxf(M, sk);
+        float f = 0.f, Lf = 0.f;
+        if (Mf != -INFINITY) {
+          const float am = (M == -INFINITY) ? 0.f : ex2(M - Mf);
+          Lf = L[hrow] * am + ex2(sk - Mf);
+          f = am / Lf;
+        }
+        T* orow = reinterpret_cast<T*>(p.out) + o_offset(p, b, hr, ri);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          const int cc = j * 8 + 2 * tig;
+          if (cc < dv)
+            *reinterpret_cast<uint32_t*>(orow + cc) = MmaOp<T>::pack(o[j][2 * hrow] * f, o[j][2 * hrow + 1] * f);
+        }
+        if (tig == 0 && p.lse) p.lse[row_global] = (Mf == -INFINITY) ? -INFINITY : (Mf + log2f(Lf)) * kLn2;
+      } else {
+        float* po = p.part_o + (row_global * p.nblk + c) * p.dv;
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          const int cc = j * 8 + 2 * tig;
+          if (cc < dv) *reinterpret_cast<float2*>(po + cc) = make_float2(o[j][2 * hrow], o[j][2 * hrow + 1]);
+        }
+        if (tig == 0) {
+          p.part_ml[(row_global * p.nblk + c) * 2 + 0] = M;
+          p.part_ml[(row_global * p.nblk + c) * 2 + 1] = L[hrow];
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    m[0] = m[1] = -INFINITY;
+    l[0] = l[1] = 0.f;
+  };
+
+  bool ok = true;
   for (int gt = 0; gt < n_tiles; ++gt) {
     const int s = gt % ST;
-    if (!__all_sync(0xffffffffu, mbar_wait(full(s), (gt / ST) & 1, limit, nullptr))) {
+    if (p.paged) cp_async_wait<ST - 1>();
+    if (!landed(gt)) {
       if (lane == 0) record_status(p, kStatTimeoutTmaFull);
+      ok = false;
       break;
     }
     consumed = gt + 1;
     const int64_t c = c_begin + gt / tpb;  // key block of this tile
-    const int64_t j_end = ((c + 1) * p.keys_per_blk < p.Lk) ? (c + 1) * p.keys_per_blk : p.Lk;
+    const int64_t jb_end = u_lo + (c + 1) * p.keys_per_blk;
+    const int j_end = (int)(jb_end < key_end ? jb_end : key_end);
     const uint32_t kst = ring + s * stage_bytes, vst = kst + k_bytes;
     // ---- S = Q K^T over the tile's keys (n-tiles of 8 keys)
     constexpr int NS = kKT / 8;  // n-tiles of S
@@ -229,17 +347,19 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
       }
     }
     // ---- mask, online softmax (rows gid / gid + 8; keys spread over the lane quad)
-    const int64_t jt = key_begin + (int64_t)gt * kKT;
+    const int jt = (int)(key_begin + (int64_t)gt * kKT);
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
     for (int nt = 0; nt < NS; ++nt) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int hrow = e >> 1;
-        const int64_t j = jt + nt * 8 + 2 * tig + (e & 1);
-        bool vis = rok[hrow] && j < j_end && j <= last[hrow];
-        if (mrow[hrow] && vis) vis = mrow[hrow][j] != 0;
-        const float v = vis ? sc[nt][e] * p.scale_log2 : -INFINITY;
+        const int j = jt + nt * 8 + 2 * tig + (e & 1);
+        bool vis = rok[hrow] && j < j_end && j >= lo[hrow] && j < hi[hrow];
+        if (bool_mask && vis) vis = static_cast<const uint8_t*>(mk[hrow])[j] != 0;
+        float v = -INFINITY;
+        if (vis) v = add_mask ? fmaf(sc[nt][e], p.scale_log2, to_f32<T>(static_cast<const T*>(mk[hrow])[j]) * kLog2e)
+                              : sc[nt][e] * p.scale_log2;
         sc[nt][e] = v;
         mx[hrow] = fmaxf(mx[hrow], v);
       }
@@ -296,67 +416,27 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
     // ---- the slot is read: refill it with tile gt + ST (the async proxy's write must
     // follow this warp's reads of the slot)
     __syncwarp();
-    if (lane == 0 && gt + ST < n_tiles) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (gt + ST < n_tiles) {
+      if (!p.paged && lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       issue(gt + ST);
+      issued = gt + ST + 1;
     }
-    if (gt + ST < n_tiles) issued = gt + ST + 1;
+    if (p.paged) cp_async_commit();
 
     // ---- end of a key block: write its partial (or the output when it is the only one)
-    if ((gt + 1) % tpb == 0 || gt + 1 == n_tiles) {
-      float L[2];
-#pragma unroll
-      for (int hrow = 0; hrow < 2; ++hrow) {
-        L[hrow] = l[hrow] + __shfl_xor_sync(0xffffffffu, l[hrow], 1);
-        L[hrow] += __shfl_xor_sync(0xffffffffu, L[hrow], 2);
-      }
-#pragma unroll
-      for (int hrow = 0; hrow < 2; ++hrow) {
-        const int r = gid + 8 * hrow;
-        if (!rok[hrow]) continue;
-        const int64_t rho = rc * kRowsDec + r;
-        const int64_t row_global = (b * p.Hq + hkv * p.g + rho / p.Lq) * p.Lq + rho % p.Lq;
-        const float M = m[hrow];
-        if (p.nblk == 1) {
-          const int64_t h = hkv * p.g + rho / p.Lq;
-          const float sk = sink_log2<T>(p, h);
-          const float Mf = fmaxf(M, sk);
-          float f = 0.f, Lf = 0.f;
-          if (Mf != -INFINITY) {
-            const float am = (M == -INFINITY) ? 0.f : ex2(M - Mf);
-            Lf = L[hrow] * am + ex2(sk - Mf);
-            f = am / Lf;
-          }
-          T* orow = reinterpret_cast<T*>(p.out) + row_global * p.dv;
-#pragma unroll
-          for (int j = 0; j < NT; ++j) {
-            const int cc = j * 8 + 2 * tig;
-            if (cc < dv)
-              *reinterpret_cast<uint32_t*>(orow + cc) = MmaOp<T>::pack(o[j][2 * hrow] * f, o[j][2 * hrow + 1] * f);
-          }
-          if (tig == 0 && p.lse) p.lse[row_global] = (Mf == -INFINITY) ? -INFINITY : (Mf + log2f(Lf)) * kLn2;
-        } else {
-          float* po = p.part_o + (row_global * p.nblk + c) * p.dv;
-#pragma unroll
-          for (int j = 0; j < NT; ++j) {
-            const int cc = j * 8 + 2 * tig;
-            if (cc < dv) *reinterpret_cast<float2*>(po + cc) = make_float2(o[j][2 * hrow], o[j][2 * hrow + 1]);
-          }
-          if (tig == 0) {
-            p.part_ml[(row_global * p.nblk + c) * 2 + 0] = M;
-            p.part_ml[(row_global * p.nblk + c) * 2 + 1] = L[hrow];
-          }
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-      m[0] = m[1] = -INFINITY;
-      l[0] = l[1] = 0.f;
-    }
+    if ((gt + 1) % tpb == 0 || gt + 1 == n_tiles) flush(c);
+  }
+  if (ok) {
+    // key blocks of this run that hold no key of this tile's rows (past a sequence's
+    // length, outside a window) still get their (empty) partial, or the final output
+    for (int64_t c = c_begin + (n_tiles + tpb - 1) / tpb; c < c_end; ++c) flush(c);
   }
   // a wait that gave up leaves copies in flight: they land before the warp leaves
-  if (lane == 0)
+  if (p.paged) {
+    cp_async_wait<0>();
+  } else if (lane == 0) {
     for (int i = consumed; i < issued; ++i) mbar_wait(full(i % ST), (i / ST) & 1, kDrainLimitDec, nullptr);
+  }
   __syncwarp();
 }
 
@@ -435,8 +515,15 @@ cudaError_t launch_decode_mma(int dtype, const Params& p, cudaStream_t st) {
   a.p = p;
   const int64_t BH = p.B * p.Hkv;
   const int kt = dec_info(p.d, p.dv).kt;
-  if (!kt || !encode_3d(&a.tmk, dtype, p.k, p.d, p.Lk, BH, kt) || !encode_3d(&a.tmv, dtype, p.v, p.dv, p.Lk, BH, kt))
-    return cudaErrorInvalidValue;
+  if (!kt) return cudaErrorInvalidValue;
+  if (!p.paged) {
+    // K and V as 4-D [B][Hkv][Lk][d] views with the caller's strides (a slice of a longer
+    // cache or a transposed [B, L, H, D] layout reads in place)
+    const int64_t kd[4] = {p.d, p.Lk, p.Hkv, p.B}, ks[3] = {p.k_sl, p.k_sh, p.k_sb};
+    const int64_t vd[4] = {p.dv, p.Lk, p.Hkv, p.B}, vs[3] = {p.v_sl, p.v_sh, p.v_sb};
+    if (!encode_tiled_16bit(&a.tmk, dtype, p.k, 4, kd, ks, kt) || !encode_tiled_16bit(&a.tmv, dtype, p.v, 4, vd, vs, kt))
+      return cudaErrorInvalidValue;
+  }
   a.n_rc = (int)((p.G + kRowsDec - 1) / kRowsDec);
   a.dpanels = (int)((p.d + 63) / 64);
   a.dvpanels = (int)((p.dv + 63) / 64);

@@ -43,6 +43,14 @@ int prefill_tc_q_tiles(int64_t d, int64_t dv, int64_t G);
 size_t prefill_tc_smem_bytes(int64_t d, int64_t dv, int bn, int nq);
 int64_t prefill_tc_rows_per_cta(int64_t d, int64_t dv, int64_t G);
 size_t prefill_tc_mask_words(int64_t Lk);
+// How a tensor-core prefill call is tiled: key tile, Q tiles per CTA, packed rows or
+// head-local tiles (strided q / out go through 5-D maps), and the grid.
+struct PrefillGeom {
+  int bn, nq, head_local, qo5;
+  int64_t n_it, n_rt, grid;
+};
+PrefillGeom prefill_tc_geometry(int64_t B, int64_t Hkv, int64_t g, int64_t Lq, int64_t d, int64_t dv,
+                                bool qo_packed);
 cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, cudaStream_t st);
 
 // decode_mma.cu

@@ -64,8 +64,11 @@ struct TcArgs {
   int ksteps_qk;     // ceil(d / 16)
   int n_pv;          // dv rounded up to 16 (MMA N of P V)
   int itile_order;   // Lq % (NQ x 128) == 0: launch the late (heavier, causal) blocks first
-  int head_pairs;    // NQ = 2, g even, Lq % 128 == 0: the two Q tiles are the same positions
-                     // of two query heads (equal key extents), late positions first
+  int head_local;    // each Q tile is 128 positions of one query head (NQ = 2: the same
+                     // positions of two heads, equal key extents), late positions first
+  int qo5;           // Q and out are read / written through 5-D [B][Hkv][g][Lq][D] maps
+                     // (strided layouts); otherwise 3-D [B*Hkv][G][D] maps of packed rows
+  int n_it;          // head_local: 128-position blocks per head
   int tma_out;       // the output tile fits the Q tile's shared memory: store it by TMA
 };
 
@@ -93,44 +96,77 @@ template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, f
   return pack_bf16(lo, hi);
 }
 
-// Last key row i may see (causal: bottom-right diagonal; otherwise the last key).
-__device__ __forceinline__ int64_t row_last_key(const Params& p, int64_t i) {
-  return p.mask_kind == kMaskCausal ? causal_last_key(p, i) : p.Lk - 1;
-}
-
-// Key tiles of BN keys that rows [r0, r0 + 128) of a KV head need (0 past the last row).
-template <int BN>
-__device__ __forceinline__ int tiles_for_rows(const Params& p, int64_t r0) {
-  if (r0 >= p.G) return 0;
-  int64_t kend = p.Lk;
-  if (p.mask_kind == kMaskCausal) {
-    const int64_t r1 = (r0 + kBM < p.G ? r0 + kBM : p.G) - 1;
-    const int64_t imax = (r0 / p.Lq == r1 / p.Lq) ? r1 % p.Lq : p.Lq - 1;
-    const int64_t lim = causal_last_key(p, imax) + 1;
-    if (lim < kend) kend = lim;
+// The positions [imin, imax] of a Q tile's valid rows, or false if it has none.  Packed:
+// rows [r0, r0 + 128) of the KV head's G rows (head-major; a tile spanning two heads
+// covers every position).  Head-local: positions [i0, i0 + 128) of one query head.
+__device__ __forceinline__ bool tile_positions(const TcArgs& a, int r0, int i0, int64_t& imin,
+                                               int64_t& imax) {
+  const Params& p = a.p;
+  if (a.head_local) {
+    if (i0 >= p.Lq) return false;
+    imin = i0;
+    imax = (i0 + kBM < p.Lq ? i0 + kBM : p.Lq) - 1;
+    return true;
   }
-  return kend > 0 ? (int)((kend + BN - 1) / BN) : 0;
+  if (r0 >= p.G) return false;
+  const int64_t r1 = (r0 + kBM < p.G ? r0 + kBM : p.G) - 1;
+  const bool one = r0 / p.Lq == r1 / p.Lq;
+  imin = one ? r0 % p.Lq : 0;
+  imax = one ? r1 % p.Lq : p.Lq - 1;
+  return true;
 }
 
-// One query row's softmax step on key tile t.  tS / tO: TMEM addresses (lane base
-// included) of this tile's S columns and of O; mrow: this row's bit-packed mask words
-// (or null).  PF: the tile's words were loaded ahead by the caller into mw.  Returns
-// false if a wait gave up.
-template <typename T, int BN, bool PF>
-__device__ __forceinline__ bool softmax_tile(const TcArgs& a, int t, uint32_t tS, uint32_t tO,
-                                             bool row_ok, int64_t last_key, const uint32_t* mrow,
+// Key tiles of BN keys [first, end) that a Q tile needs: the causal bound of its last
+// position and the window band of its first (end = first = 0 when it needs none).
+template <int BN>
+__device__ __forceinline__ void tile_key_range(const TcArgs& a, int r0, int i0, int& first, int& end) {
+  const Params& p = a.p;
+  int64_t imin, imax;
+  first = end = 0;
+  if (!tile_positions(a, r0, i0, imin, imax)) return;
+  const int64_t hi = row_key_hi(p, imax + p.Lk - p.Lq, p.Lk);
+  const int64_t lo = row_key_lo(p, imin + p.Lk - p.Lq);
+  if (hi <= lo) return;
+  first = (int)(lo / BN);
+  end = (int)((hi + BN - 1) / BN);
+}
+
+// The 32-bit visibility word of columns [c0, c0 + 32) of a row that sees columns
+// [lo, hi) of the tile.
+__device__ __forceinline__ uint32_t col_bound(int c0, int lo, int hi) {
+  const int a = lo - c0, b = hi - c0;
+  const uint32_t below_hi = b >= 32 ? 0xffffffffu : (b <= 0 ? 0u : (1u << b) - 1u);
+  const uint32_t below_lo = a >= 32 ? 0xffffffffu : (a <= 0 ? 0u : (1u << a) - 1u);
+  return below_hi & ~below_lo;
+}
+
+// Mask handling of a prefill kernel instantiation: the key bounds alone (none, causal,
+// window), a bit-packed boolean mask, or an additive mask.
+enum { kMmBounds = 0, kMmBits = 1, kMmAdd = 2 };
+
+// One query row's softmax step on its t-th key tile, key tile kt of the sequence.  tS /
+// tO: TMEM addresses (lane base included) of this tile's S columns and of O; the row
+// sees keys [first_key, last_key]; mrow: its mask row (MM = kMmBits: bit-packed words,
+// kMmAdd: the additive row in T), unused otherwise.  PF: the tile's words were loaded
+// ahead by the caller into mw.  Returns false if a wait gave up.
+template <typename T, int BN, int MM, bool PF>
+__device__ __forceinline__ bool softmax_tile(const TcArgs& a, int t, int kt, uint32_t tS, uint32_t tO,
+                                             bool row_ok, int first_key, int last_key, const void* mrow_any,
                                              const uint32_t (&mw)[BN / 32], float& m_run, float& l_run,
                                              uint32_t pv_bar, bool wait_pv, uint64_t limit,
                                              volatile int* abort) {
   const Params& p = a.p;
+  const uint32_t* mrow = static_cast<const uint32_t*>(mrow_any);
+  const T* arow = static_cast<const T*>(mrow_any);
   uint32_t sr[BN];
   if constexpr (BN == 128) tmem_ld128_sync(tS, sr);
   else tmem_ld64_sync(tS, sr);
-  const int64_t j0 = (int64_t)t * BN;
-  // columns [0, vis_cols) pass the causal / key-count bound for this row
-  const int64_t vc = last_key - j0 + 1;
-  const int vis_cols = vc < 0 ? 0 : (vc > BN ? BN : (int)vc);
-  const bool masked = !row_ok || mrow != nullptr || vis_cols < BN;
+  const int j0 = kt * BN;
+  // columns [vis_lo, vis_hi) pass the causal / key-count bound and the window band
+  const int vh = last_key - j0 + 1, vl = first_key - j0;
+  const int vis_hi = vh < 0 ? 0 : (vh > BN ? BN : vh);
+  const int vis_lo = vl < 0 ? 0 : (vl > BN ? BN : vl);
+  const bool masked = !row_ok || MM != kMmBounds || vis_hi < BN || vis_lo > 0;
   // warp-uniform fast path: nothing masked and scale >= 0, so the maximum of the raw
   // scores gives the scaled maximum and 2^(s*c - m) is one FFMA and one MUFU op
   const bool fast = !__any_sync(0xffffffffu, masked) && p.scale_log2 >= 0.f;
@@ -169,10 +205,9 @@ __device__ __forceinline__ bool softmax_tile(const TcArgs& a, int t, uint32_t tS
       }
       tmem_st32(tS + c2i * 32, pk);
     }
-    float a0, a1, b0, b1, c0, c1, d0, d1;
+    float a0, a1, b0, b1;
     f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
     f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
-    (void)c0; (void)c1; (void)d0; (void)d1;
     l_run = l_run * alpha + ((a0 + a1) + (b0 + b1));
   } else {
     float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -180,16 +215,29 @@ __device__ __forceinline__ bool softmax_tile(const TcArgs& a, int t, uint32_t tS
 #pragma unroll
     for (int c = 0; c < BN / 32; ++c) {
       uint32_t bits = 0xffffffffu;
-      if (mrow) bits = PF ? mw[c] : (row_ok ? __ldg(mrow + j0 / 32 + c) : 0u);
-      // the visible columns of this word: mask bits, causal / key-count bound, the row
-      const int lim = vis_cols - c * 32;
-      const uint32_t bound = lim >= 32 ? 0xffffffffu : (lim <= 0 ? 0u : (1u << lim) - 1u);
-      const uint32_t vb = row_ok ? (bits & bound) : 0u;
+      if constexpr (MM == kMmBits) bits = PF ? mw[c] : (row_ok ? __ldg(mrow + j0 / 32 + c) : 0u);
+      // the visible columns of this word: mask bits, causal / key-count bound, window
+      // band, the row
+      const uint32_t vb = row_ok ? (bits & col_bound(c * 32, vis_lo, vis_hi)) : 0u;
 #pragma unroll
       for (int e = 0; e < 32; e += 2) {
         const int col = c * 32 + e;
         float x0, x1;
         f2_unpack(f2_mul(f2_pack(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])), c2), x0, x1);
+        if (MM == kMmAdd && (vb & (3u << e))) {
+          // the additive term, in log2 units (a pair of 16-bit values where aligned)
+          float a0, a1;
+          if ((p.Lk & 1) == 0) {
+            const uint32_t w = __ldg(reinterpret_cast<const unsigned int*>(arow + j0 + col));
+            a0 = to_f32<T>(*reinterpret_cast<const T*>(&w));
+            a1 = to_f32<T>(*(reinterpret_cast<const T*>(&w) + 1));
+          } else {
+            a0 = (vb & (1u << e)) ? to_f32<T>(arow[j0 + col]) : 0.f;
+            a1 = (vb & (2u << e)) ? to_f32<T>(arow[j0 + col + 1]) : 0.f;
+          }
+          x0 = fmaf(a0, kLog2e, x0);
+          x1 = fmaf(a1, kLog2e, x1);
+        }
         x0 = (vb & (1u << e)) ? x0 : -INFINITY;
         x1 = (vb & (2u << e)) ? x1 : -INFINITY;
         sr[col] = __float_as_uint(x0);
@@ -255,7 +303,7 @@ __device__ __forceinline__ bool softmax_tile(const TcArgs& a, int t, uint32_t tS
 // Final output of one query row: sink folded in, one division, one rounding; lse.
 template <typename T>
 __device__ __forceinline__ void epilogue_row(const Params& p, uint32_t tO, bool have_o, bool row_ok,
-                                             int64_t out_row, int64_t h, float m_run, float l_run) {
+                                             int64_t b, int64_t h, int64_t i, float m_run, float l_run) {
   const float sk = sink_log2<T>(p, h);
   const float M = fmaxf(m_run, sk);
   float f = 0.f, L = 0.f;
@@ -264,7 +312,8 @@ __device__ __forceinline__ void epilogue_row(const Params& p, uint32_t tO, bool 
     L = l_run * am + ex2(sk - M);
     f = am / L;
   }
-  T* orow = reinterpret_cast<T*>(p.out) + out_row * p.dv;
+  T* orow = reinterpret_cast<T*>(p.out) + o_offset(p, b, h, i);
+  const int64_t lse_row = (b * p.Hq + h) * p.Lq + i;
   const int dv = (int)p.dv;
   // 128 columns of O per TMEM load (the O region is 128-column aligned and inside the
   // allocation for every head this kernel takes)
@@ -291,7 +340,7 @@ __device__ __forceinline__ void epilogue_row(const Params& p, uint32_t tO, bool 
       }
     }
   }
-  if (row_ok && p.lse) p.lse[out_row] = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
+  if (row_ok && p.lse) p.lse[lse_row] = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
 }
 
 // The same, for a TMA store of the whole tile: the row is written (scaled and rounded)
@@ -300,7 +349,7 @@ __device__ __forceinline__ void epilogue_row(const Params& p, uint32_t tO, bool 
 // (c ^ (r mod 8)) * 16); the log-sum-exp is written directly.
 template <typename T>
 __device__ __forceinline__ void epilogue_row_smem(const Params& p, uint32_t tO, bool have_o, bool row_ok,
-                                                  int64_t out_row, int64_t h, float m_run, float l_run,
+                                                  int64_t b, int64_t h, int64_t i, float m_run, float l_run,
                                                   uint8_t* stage, int r) {
   const float sk = sink_log2<T>(p, h);
   const float M = fmaxf(m_run, sk);
@@ -333,13 +382,13 @@ __device__ __forceinline__ void epilogue_row_smem(const Params& p, uint32_t tO, 
       }
     }
   }
-  if (row_ok && p.lse) p.lse[out_row] = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
+  if (row_ok && p.lse) p.lse[(b * p.Hq + h) * p.Lq + i] = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
 }
 
 template <int NQ>
 constexpr int tc_threads() { return (2 + 4 * NQ) * 32; }
 
-template <typename T, int BN, int NQ>
+template <typename T, int BN, int NQ, int MM>
 __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __grid_constant__ TcArgs a) {
   static_assert(NQ == 1 || NQ == 2, "one or two Q tiles per CTA");
   static_assert(NQ == 1 || BN == 128, "the two-tile variant uses 128-key tiles");
@@ -360,38 +409,58 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_holder + 1);
   auto bar = [&](int i) { return smem_addr(bars + i); };
 
-  // ---- which rows and keys this CTA owns: (b, kv head) and the first of the 128 rows
-  // (among the G rows of that KV head) of each Q tile
-  const int64_t BH = p.B * p.Hkv;
-  int64_t bh, row0[NQ];
-  if (NQ == 2 && a.head_pairs) {
-    const int64_t hp = p.g / 2, kpt = p.Lq / kBM;
-    int64_t x = blockIdx.x;
-    const int64_t pr = x % hp; x /= hp;
+  // ---- which rows and keys this CTA owns: (b, kv head) and, per Q tile, either the first
+  // of its 128 packed rows (among the G rows of that KV head) or its query head and first
+  // position (head-local tiles)
+  // (32-bit: the planner sends no call whose rows, keys or CTAs do not fit)
+  const int BH = (int)(p.B * p.Hkv);
+  int bh, row0[NQ], i0[NQ], hhq[NQ];
+  if (a.head_local) {
+    const int per = (int)(p.g / NQ);  // Q-tile groups (heads or head pairs) per KV head
+    int x = (int)blockIdx.x;
+    const int pr = x % per; x /= per;
     bh = x % BH;
-    const int64_t k = kpt - 1 - x / BH;
-    row0[0] = 2 * pr * p.Lq + k * kBM;
-    row0[NQ - 1] = row0[0] + p.Lq;
+    const int it = a.n_it - 1 - x / BH;  // late (heavier, causal) positions first
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      hhq[q] = pr * NQ + q;
+      i0[q] = it * kBM;
+      row0[q] = hhq[q] * (int)p.Lq + i0[q];
+    }
   } else {
-    int64_t rb;  // row block of NQ x 128 consecutive rows
+    int rb;  // row block of NQ x 128 consecutive rows
     if (a.itile_order) {
-      const int64_t ipt = p.Lq / (kBM * NQ);  // row blocks per head
-      int64_t x = blockIdx.x;
-      const int64_t hh = x % p.g; x /= p.g;
+      const int ipt = (int)(p.Lq / (kBM * NQ));  // row blocks per head
+      int x = (int)blockIdx.x;
+      const int hh = x % (int)p.g; x /= (int)p.g;
       bh = x % BH;
-      const int64_t it = ipt - 1 - x / BH;
+      const int it = ipt - 1 - x / BH;
       rb = hh * ipt + it;
     } else {
-      rb = blockIdx.x % a.n_rt;
-      bh = blockIdx.x / a.n_rt;
+      rb = (int)blockIdx.x % a.n_rt;
+      bh = (int)blockIdx.x / a.n_rt;
     }
 #pragma unroll
-    for (int q = 0; q < NQ; ++q) row0[q] = (rb * NQ + q) * kBM;
+    for (int q = 0; q < NQ; ++q) {
+      row0[q] = (rb * NQ + q) * kBM;
+      hhq[q] = 0;
+      i0[q] = 0;
+    }
   }
-  const int64_t hkv = bh % p.Hkv;
+  const int hkv = bh % (int)p.Hkv, bb = bh / (int)p.Hkv;
+  // key tiles: the CTA walks tiles kt0 + t, t < n_max; Q tile q uses t < n_q[q] (its tiles
+  // before kt0 + n_q[q]; a tile of the walk wholly outside a row's band is masked for it)
+  int first_q[NQ], end_q[NQ];
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) tile_key_range<BN>(a, row0[q], i0[q], first_q[q], end_q[q]);
+  int kt0 = 0x7fffffff;
+#pragma unroll
+  for (int q = 0; q < NQ; ++q)
+    if (end_q[q] > first_q[q] && first_q[q] < kt0) kt0 = first_q[q];
+  if (kt0 == 0x7fffffff) kt0 = 0;
   int n_q[NQ];
 #pragma unroll
-  for (int q = 0; q < NQ; ++q) n_q[q] = tiles_for_rows<BN>(p, row0[q]);
+  for (int q = 0; q < NQ; ++q) n_q[q] = end_q[q] > first_q[q] ? end_q[q] - kt0 : 0;
   int n_max = 0;
 #pragma unroll
   for (int q = 0; q < NQ; ++q) n_max = n_q[q] > n_max ? n_q[q] : n_max;
@@ -442,8 +511,13 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
       mbar_arrive_expect_tx(bar(kBarQ), q_tx);
       for (int q = 0; q < NQ; ++q)
         if (n_q[q] > 0)
-          for (int pn = 0; pn < a.dpanels; ++pn)
-            tma_load_3d(sQ + q * q_bytes + pn * kBM * 128, &a.tmq, bar(kBarQ), pn * 64, (int)row0[q], (int)bh);
+          for (int pn = 0; pn < a.dpanels; ++pn) {
+            if (a.qo5)
+              tma_load_5d(sQ + q * q_bytes + pn * kBM * 128, &a.tmq, bar(kBarQ), pn * 64, (int)i0[q], hhq[q],
+                          (int)hkv, (int)bb);
+            else
+              tma_load_3d(sQ + q * q_bytes + pn * kBM * 128, &a.tmq, bar(kBarQ), pn * 64, (int)row0[q], (int)bh);
+          }
       // one ring slot: wait until its previous tile is released, then load tile t into it
       auto load = [&](int full, int empty, uint32_t ring, uint32_t bytes, const CUtensorMap* tm1, int panels1,
                       uint32_t ring2, const CUtensorMap* tm2, int panels2, int t) {
@@ -454,9 +528,11 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
         }
         mbar_arrive_expect_tx(bar(full + s), bytes);
         for (int pn = 0; pn < panels1; ++pn)
-          tma_load_3d(ring + s * (panels1 * BN * 128) + pn * BN * 128, tm1, bar(full + s), pn * 64, t * BN, (int)bh);
+          tma_load_4d(ring + s * (panels1 * BN * 128) + pn * BN * 128, tm1, bar(full + s), pn * 64, (kt0 + t) * BN,
+                      (int)hkv, (int)bb);
         for (int pn = 0; pn < panels2; ++pn)
-          tma_load_3d(ring2 + s * (panels2 * BN * 128) + pn * BN * 128, tm2, bar(full + s), pn * 64, t * BN, (int)bh);
+          tma_load_4d(ring2 + s * (panels2 * BN * 128) + pn * BN * 128, tm2, bar(full + s), pn * 64, (kt0 + t) * BN,
+                      (int)hkv, (int)bb);
         return true;
       };
       int k_issued = 0, v_issued = 0;
@@ -470,9 +546,11 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
           }
           mbar_arrive_expect_tx(bar(kBarKvFull + s), k_bytes + v_bytes);
           for (int pn = 0; pn < a.dpanels; ++pn)
-            tma_load_3d(sK + s * k_bytes + pn * BN * 128, &a.tmk, bar(kBarKvFull + s), pn * 64, t * BN, (int)bh);
+            tma_load_4d(sK + s * k_bytes + pn * BN * 128, &a.tmk, bar(kBarKvFull + s), pn * 64, (kt0 + t) * BN,
+                        (int)hkv, (int)bb);
           for (int pn = 0; pn < a.dvpanels; ++pn)
-            tma_load_3d(sV + s * v_bytes + pn * BN * 128, &a.tmv, bar(kBarKvFull + s), pn * 64, t * BN, (int)bh);
+            tma_load_4d(sV + s * v_bytes + pn * BN * 128, &a.tmv, bar(kBarKvFull + s), pn * 64, (kt0 + t) * BN,
+                        (int)hkv, (int)bb);
           k_issued = v_issued = t + 1;
         }
       } else {
@@ -615,12 +693,29 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
     const int q4 = warp & 3;       // TMEM lane quarter this warp may access
     const int row = q4 * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-    const int64_t rho = (q == 0 ? row0[0] : row0[NQ - 1]) + row;
-    const bool row_ok = rho < p.G;
-    const int64_t i = row_ok ? rho % p.Lq : 0;
-    const int64_t h = hkv * p.g + (row_ok ? rho / p.Lq : 0);
-    const int64_t last_key = row_last_key(p, i);
-    const uint32_t* mrow = a.mask_bits ? a.mask_bits + i * a.mask_words : nullptr;
+    const int qi = q == 0 ? 0 : NQ - 1;
+    bool row_ok;
+    int i, hh;
+    if (a.head_local) {
+      i = i0[qi] + row;
+      row_ok = i < p.Lq;
+      hh = hhq[qi];
+      if (!row_ok) i = 0;
+    } else {
+      const int rho = row0[qi] + row;
+      row_ok = rho < p.G;
+      i = row_ok ? rho % (int)p.Lq : 0;
+      hh = row_ok ? rho / (int)p.Lq : 0;
+    }
+    const int h = hkv * (int)p.g + hh;
+    // the keys [first_key, last_key] this row may see (key indices fit 32 bits: the
+    // planner sends no longer sequence here)
+    const int64_t pos = i + p.Lk - p.Lq;
+    const int first_key = (int)row_key_lo(p, pos), last_key = (int)row_key_hi(p, pos, p.Lk) - 1;
+    const uint32_t* mrow = MM == kMmBits ? a.mask_bits + (int64_t)i * a.mask_words : nullptr;
+    const void* mrow_any = mrow;
+    if constexpr (MM == kMmAdd)
+      mrow_any = reinterpret_cast<const T*>(p.amask) + bb * p.am_sb + h * p.am_sh + (int64_t)i * p.Lk;
     const int n_tiles = n_q[q];
     const uint32_t tO = tmem + lane_base + tO_col(q);
     float m_run = -INFINITY, l_run = 0.f;
@@ -637,8 +732,9 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
         // S of this tile was issued after P_{t-1} V_{t-1} of the same Q tile, and a commit
         // tracks every earlier MMA of the issuing thread, so s_full already implies that O
         // holds P_{t-1} V_{t-1}
-        ok = softmax_tile<T, BN, false>(a, t, tmem + lane_base + tS_col(q), tO, row_ok, last_key, mrow, no_words,
-                                        m_run, l_run, bar(kBarPvDone + q), false, limit, abort);
+        ok = softmax_tile<T, BN, MM, false>(a, t, kt0 + t, tmem + lane_base + tS_col(q), tO, row_ok, first_key,
+                                            last_key, mrow_any, no_words, m_run, l_run, bar(kBarPvDone + q), false,
+                                            limit, abort);
         if (!ok) {
           fail(p, abort, kStatTimeoutMma);
           break;
@@ -652,7 +748,8 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
       uint32_t mw[BN / 32];
       auto load_mw = [&](int t, uint32_t (&dst)[BN / 32]) {
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) dst[c] = (mrow && row_ok) ? __ldg(mrow + (t * BN) / 32 + c) : 0u;
+        for (int c = 0; c < BN / 32; ++c)
+          dst[c] = (MM == kMmBits && row_ok) ? __ldg(mrow + ((kt0 + t) * BN) / 32 + c) : 0u;
       };
       if (n_tiles > 0) load_mw(0, mw);
       for (int t = 0; t < n_tiles; ++t) {
@@ -666,8 +763,9 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
         }
         tc_fence_after();
         // S_t was issued before P_{t-1} V_{t-1}: the softmax waits for that product
-        ok = softmax_tile<T, BN, true>(a, t, tmem + lane_base + tS_col(slot), tO, row_ok, last_key, mrow, mw,
-                                       m_run, l_run, bar(kBarPvDone + q), true, limit, abort);
+        ok = softmax_tile<T, BN, MM, true>(a, t, kt0 + t, tmem + lane_base + tS_col(slot), tO, row_ok, first_key,
+                                           last_key, mrow_any, mw, m_run, l_run, bar(kBarPvDone + q), true, limit,
+                                           abort);
         if (!ok) {
           fail(p, abort, kStatTimeoutMma);
           break;
@@ -693,17 +791,22 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
       // loaded at all when the tile sees no key.  Every thread of the warpgroup reaches
       // the barrier, whatever happened before it.
       uint8_t* stage = base + q * q_bytes;
-      if (ok) epilogue_row_smem<T>(p, tO, n_tiles > 0, row_ok, bh * p.G + rho, h, m_run, l_run, stage, row);
+      if (ok) epilogue_row_smem<T>(p, tO, n_tiles > 0, row_ok, bb, h, i, m_run, l_run, stage, row);
       fence_proxy_async_smem();
       const bool all_ok = bar_and(1 + q, 128, ok);
       if (all_ok && warp == 2 + 4 * q && lane == 0) {
-        for (int pn = 0; pn < a.dvpanels; ++pn)
-          tma_store_3d(&a.tmo, smem_addr(stage + pn * (kBM * 128)), pn * 64, (int)(q == 0 ? row0[0] : row0[NQ - 1]), (int)bh);
+        for (int pn = 0; pn < a.dvpanels; ++pn) {
+          if (a.qo5)
+            tma_store_5d(&a.tmo, smem_addr(stage + pn * (kBM * 128)), pn * 64, (int)i0[qi], hhq[qi], (int)hkv,
+                         (int)bb);
+          else
+            tma_store_3d(&a.tmo, smem_addr(stage + pn * (kBM * 128)), pn * 64, (int)row0[qi], (int)bh);
+        }
         bulk_commit_group();
         bulk_wait_read_all();  // the stage must stay intact until the copy has read it
       }
     } else if (ok) {
-      epilogue_row<T>(p, tO, n_tiles > 0, row_ok, bh * p.G + rho, h, m_run, l_run);
+      epilogue_row<T>(p, tO, n_tiles > 0, row_ok, bb, h, i, m_run, l_run);
     }
   }
 
@@ -736,19 +839,27 @@ __global__ void sdpa_pack_mask_bits(const uint8_t* __restrict__ mask, int64_t Lq
 
 // ------------------------------------------------------------------------- host side
 
-template <typename T, int BN, int NQ>
+template <typename T, int BN, int NQ, int MM>
 cudaError_t launch_tc_t(const TcArgs& a, size_t smem, int64_t grid, cudaStream_t st) {
   static std::atomic<unsigned long long> configured{0};
-  cudaError_t e = set_max_dynamic_smem_once(configured, (const void*)sdpa_prefill_tc<T, BN, NQ>, (int)kTcMaxSmem);
+  cudaError_t e =
+      set_max_dynamic_smem_once(configured, (const void*)sdpa_prefill_tc<T, BN, NQ, MM>, (int)kTcMaxSmem);
   if (e != cudaSuccess) return e;
-  sdpa_prefill_tc<T, BN, NQ><<<(unsigned)grid, tc_threads<NQ>(), smem, st>>>(a);
+  sdpa_prefill_tc<T, BN, NQ, MM><<<(unsigned)grid, tc_threads<NQ>(), smem, st>>>(a);
   return cudaGetLastError();
+}
+
+template <typename T, int MM>
+cudaError_t launch_tc_mm(int bn, int nq, const TcArgs& a, size_t smem, int64_t grid, cudaStream_t st) {
+  if (nq == 2) return launch_tc_t<T, 128, 2, MM>(a, smem, grid, st);
+  return bn == 128 ? launch_tc_t<T, 128, 1, MM>(a, smem, grid, st) : launch_tc_t<T, 64, 1, MM>(a, smem, grid, st);
 }
 
 template <typename T>
 cudaError_t launch_tc_cfg(int bn, int nq, const TcArgs& a, size_t smem, int64_t grid, cudaStream_t st) {
-  if (nq == 2) return launch_tc_t<T, 128, 2>(a, smem, grid, st);
-  return bn == 128 ? launch_tc_t<T, 128, 1>(a, smem, grid, st) : launch_tc_t<T, 64, 1>(a, smem, grid, st);
+  if (a.p.mask_kind == kMaskBool) return launch_tc_mm<T, kMmBits>(bn, nq, a, smem, grid, st);
+  if (a.p.mask_kind == kMaskAdd) return launch_tc_mm<T, kMmAdd>(bn, nq, a, smem, grid, st);
+  return launch_tc_mm<T, kMmBounds>(bn, nq, a, smem, grid, st);
 }
 
 size_t smem_need(int64_t d, int64_t dv, int bn, int nq) {
@@ -795,26 +906,59 @@ size_t prefill_tc_mask_words(int64_t Lk) {
   return (size_t)((Lk + 127) / 128 * 4);
 }
 
+PrefillGeom prefill_tc_geometry(int64_t B, int64_t Hkv, int64_t g, int64_t Lq, int64_t d, int64_t dv,
+                                bool qo_packed) {
+  PrefillGeom r{};
+  r.bn = prefill_tc_bn(d, dv);
+  const int64_t G = g * Lq;
+  r.nq = prefill_tc_q_tiles(d, dv, G);
+  // strided q / out: Q tiles of one query head each (pairs of heads need an even group)
+  if (!qo_packed && g % 2 != 0) r.nq = 1;
+  r.qo5 = qo_packed ? 0 : 1;
+  // Packed rows with two Q tiles, an even group and whole 128-position blocks: the two
+  // tiles are the same positions of two heads (equal key extents).  Strided: always
+  // head-local tiles.
+  r.head_local = (!qo_packed || (r.nq == 2 && g % 2 == 0 && Lq % kBM == 0)) ? 1 : 0;
+  r.n_it = (Lq + kBM - 1) / kBM;
+  r.n_rt = (G + kBM * r.nq - 1) / (kBM * r.nq);
+  r.grid = r.head_local ? B * Hkv * (g / r.nq) * r.n_it : B * Hkv * r.n_rt;
+  return r;
+}
+
 cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, cudaStream_t st) {
   TcArgs a;
   memset(&a, 0, sizeof(a));
   a.p = p;
-  const int bn = prefill_tc_bn(p.d, p.dv);
+  const PrefillGeom geo = prefill_tc_geometry(p.B, p.Hkv, p.g, p.Lq, p.d, p.dv, p.qo_packed != 0);
+  const int bn = geo.bn, nq = geo.nq;
   if (!bn) return cudaErrorInvalidValue;
-  const int nq = prefill_tc_q_tiles(p.d, p.dv, p.G);
   const int64_t BH = p.B * p.Hkv;
-  if (!encode_3d(&a.tmq, dtype, p.q, p.d, p.G, BH, kBM) || !encode_3d(&a.tmk, dtype, p.k, p.d, p.Lk, BH, bn) ||
-      !encode_3d(&a.tmv, dtype, p.v, p.dv, p.Lk, BH, bn))
+  // K and V as 4-D [B][Hkv][Lk][d] views with the caller's strides
+  const int64_t kd[4] = {p.d, p.Lk, p.Hkv, p.B}, ks[3] = {p.k_sl, p.k_sh, p.k_sb};
+  const int64_t vd[4] = {p.dv, p.Lk, p.Hkv, p.B}, vs[3] = {p.v_sl, p.v_sh, p.v_sb};
+  if (!encode_tiled_16bit(&a.tmk, dtype, p.k, 4, kd, ks, bn) || !encode_tiled_16bit(&a.tmv, dtype, p.v, 4, vd, vs, bn))
     return cudaErrorInvalidValue;
-  // the output as [B*Hkv][G][dv]: the rows of one KV head are contiguous, as for Q
-  a.tma_out = ((p.dv + 63) / 64 <= (p.d + 63) / 64 && encode_3d(&a.tmo, dtype, p.out, p.dv, p.G, BH, kBM)) ? 1 : 0;
-  a.n_rt = (int)((p.G + kBM * nq - 1) / (kBM * nq));
+  const bool out_fits = (p.dv + 63) / 64 <= (p.d + 63) / 64;  // the output tile fits the Q tile's buffer
+  if (geo.qo5) {
+    // q and out as 5-D [B][Hkv][g][Lq][D] views: query head h = hkv * g + hh
+    const int64_t qd[5] = {p.d, p.Lq, p.g, p.Hkv, p.B}, qs[4] = {p.q_sl, p.q_sh, p.g * p.q_sh, p.q_sb};
+    const int64_t od[5] = {p.dv, p.Lq, p.g, p.Hkv, p.B}, os[4] = {p.o_sl, p.o_sh, p.g * p.o_sh, p.o_sb};
+    if (!encode_tiled_16bit(&a.tmq, dtype, p.q, 5, qd, qs, kBM)) return cudaErrorInvalidValue;
+    a.tma_out = (out_fits && encode_tiled_16bit(&a.tmo, dtype, p.out, 5, od, os, kBM)) ? 1 : 0;
+  } else {
+    // the packed layout: [B*Hkv][G][D], the rows of one KV head contiguous
+    if (!encode_3d(&a.tmq, dtype, p.q, p.d, p.G, BH, kBM)) return cudaErrorInvalidValue;
+    a.tma_out = (out_fits && encode_3d(&a.tmo, dtype, p.out, p.dv, p.G, BH, kBM)) ? 1 : 0;
+  }
+  a.n_rt = (int)geo.n_rt;
+  a.n_it = (int)geo.n_it;
+  a.qo5 = geo.qo5;
   a.dpanels = (int)((p.d + 63) / 64);
   a.dvpanels = (int)((p.dv + 63) / 64);
   a.ksteps_qk = (int)((p.d + 15) / 16);
   a.n_pv = (int)((p.dv + 15) / 16 * 16);
   a.itile_order = (p.Lq % (kBM * nq) == 0) ? 1 : 0;
-  a.head_pairs = (nq == 2 && p.g % 2 == 0 && p.Lq % kBM == 0) ? 1 : 0;
+  a.head_local = geo.head_local;
   if (p.mask_kind == kMaskBool) {
     a.mask_words = (int64_t)prefill_tc_mask_words(p.Lk);
     a.mask_bits = mask_bits;
@@ -826,7 +970,7 @@ cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, c
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  const int64_t grid = BH * a.n_rt;
+  const int64_t grid = geo.grid;
   const size_t smem = prefill_tc_smem_bytes(p.d, p.dv, bn, nq);
   if (dtype == 1) return launch_tc_cfg<__half>(bn, nq, a, smem, grid, st);
   return launch_tc_cfg<__nv_bfloat16>(bn, nq, a, smem, grid, st);

@@ -46,44 +46,43 @@ sdpa_tiled_simt(const Params p) {
   const int64_t blk = x % p.nblk;
   const int64_t bh = x / p.nblk;  // b * Hkv + hkv
   const int64_t b = bh / p.Hkv, hkv = bh % p.Hkv;
+  const int64_t Lkb = seq_keys(p, b);  // keys of this sequence
+  const T* Kg = reinterpret_cast<const T*>(p.k);
+  const T* Vg = reinterpret_cast<const T*>(p.v);
+  const T* Qg = reinterpret_cast<const T*>(p.q);
 
-  const T* Kg = reinterpret_cast<const T*>(p.k) + bh * p.Lk * p.d;
-  const T* Vg = reinterpret_cast<const T*>(p.v) + bh * p.Lk * p.dv;
-
-  // This lane's query row.
+  // This lane's query row, its absolute position and the keys [lo, hi) it may see.
   const int64_t rho = rt * kRows + lane;
   const bool row_ok = rho < p.G;
   const int64_t hh = row_ok ? rho / p.Lq : 0, i = row_ok ? rho % p.Lq : 0;
   const int64_t h = hkv * p.g + hh;
   const int64_t row_global = (b * p.Hq + h) * p.Lq + i;
+  const int64_t pos = i + Lkb - p.Lq;
+  const int64_t my_lo = row_key_lo(p, pos), my_hi = row_key_hi(p, pos, Lkb);
 
   // Stage the 32 query rows (zeros past the last row).
   for (int idx = tid; idx < kRows * d; idx += kThreads) {
     const int r = idx / d, c = idx % d;
     const int64_t rr = rt * kRows + r;
     float val = 0.f;
-    if (rr < p.G) {
-      const int64_t qh = hkv * p.g + rr / p.Lq, qi = rr % p.Lq;
-      val = to_f32<T>(reinterpret_cast<const T*>(p.q)[((b * p.Hq + qh) * p.Lq + qi) * p.d + c]);
-    }
+    if (rr < p.G) val = to_f32<T>(Qg[q_offset(p, b, hkv * p.g + rr / p.Lq, rr % p.Lq) + c]);
     Qs[r * ldq + c] = val;
   }
 
-  // Keys of this block, cut at the last key any row of the tile may see.
-  const int64_t j_begin = blk * p.keys_per_blk;
+  // The keys any row of the tile may see, [tile_lo, tile_hi): block blk of the plan's
+  // split starts keys_per_blk * blk keys after tile_lo (rows wrap at Lq when a tile spans
+  // heads, so the tile's positions are those of its first and last rows, or all of them).
+  const int64_t r0 = rt * kRows;
+  const int64_t r1 = (r0 + kRows - 1 < p.G - 1) ? r0 + kRows - 1 : p.G - 1;
+  const bool one_head = r0 / p.Lq == r1 / p.Lq;
+  const int64_t imin = one_head ? r0 % p.Lq : 0, imax = one_head ? r1 % p.Lq : p.Lq - 1;
+  const int64_t tile_lo = row_key_lo(p, imin + Lkb - p.Lq);
+  const int64_t tile_hi = row_key_hi(p, imax + Lkb - p.Lq, Lkb);
+  const int64_t j_begin = tile_lo + blk * p.keys_per_blk;
   int64_t j_end = j_begin + p.keys_per_blk;
-  if (j_end > p.Lk) j_end = p.Lk;
-  if (p.mask_kind == kMaskCausal) {
-    // the largest i among this tile's rows (rows wrap at Lq when a tile spans heads)
-    const int64_t r0 = rt * kRows;
-    int64_t r1 = r0 + kRows - 1;
-    if (r1 > p.G - 1) r1 = p.G - 1;
-    int64_t imax = (r0 / p.Lq == r1 / p.Lq) ? r1 % p.Lq : p.Lq - 1;
-    const int64_t lim = causal_last_key(p, imax) + 1;
-    if (j_end > lim) j_end = lim;
-  }
-  const int64_t my_last = causal_last_key(p, i);
+  if (j_end > tile_hi) j_end = tile_hi;
   const uint8_t* mrow = (p.mask_kind == kMaskBool) ? p.mask + i * p.Lk : nullptr;
+  const bool add = p.mask_kind == kMaskAdd;
 
   float m = -INFINITY, l = 0.f;
   float o[kMaxDvPerThread];
@@ -95,12 +94,12 @@ sdpa_tiled_simt(const Params p) {
     for (int idx = tid; idx < kKeys * d; idx += kThreads) {
       const int r = idx / d, c = idx % d;
       const int64_t j = j0 + r;
-      Ks[r * ldq + c] = j < j_end ? to_f32<T>(Kg[j * p.d + c]) : 0.f;
+      Ks[r * ldq + c] = j < j_end ? to_f32<T>(Kg[kv_offset(p, b, hkv, j, p.k_sb, p.k_sh, p.k_sl, p.d) + c]) : 0.f;
     }
     for (int idx = tid; idx < kKeys * dv; idx += kThreads) {
       const int r = idx / dv, c = idx % dv;
       const int64_t j = j0 + r;
-      Vs[r * dv + c] = j < j_end ? to_f32<T>(Vg[j * p.dv + c]) : 0.f;
+      Vs[r * dv + c] = j < j_end ? to_f32<T>(Vg[kv_offset(p, b, hkv, j, p.v_sb, p.v_sh, p.v_sl, p.dv) + c]) : 0.f;
     }
     __syncthreads();
 
@@ -119,10 +118,11 @@ sdpa_tiled_simt(const Params p) {
 #pragma unroll
     for (int jj = 0; jj < 8; ++jj) {
       const int64_t j = j0 + warp * 8 + jj;
-      bool vis = row_ok && j < j_end;
-      if (p.mask_kind == kMaskCausal) vis = vis && j <= my_last;
-      else if (p.mask_kind == kMaskBool) vis = vis && mrow[j] != 0;
-      s[jj] = vis ? s[jj] * p.scale_log2 : -INFINITY;
+      bool vis = row_ok && j < j_end && j >= my_lo && j < my_hi;
+      if (mrow) vis = vis && mrow[j] != 0;
+      float sv = -INFINITY;
+      if (vis) sv = add ? fmaf(s[jj], p.scale_log2, amask_log2<T>(p, b, h, i, j)) : s[jj] * p.scale_log2;
+      s[jj] = sv;
       tmax = fmaxf(tmax, s[jj]);
     }
     red_max[warp * 32 + lane] = tmax;
@@ -165,7 +165,7 @@ sdpa_tiled_simt(const Params p) {
   if (p.nblk == 1) {
     const float sk = sink_log2<T>(p, h);
     const float M = fmaxf(m, sk);
-    T* orow = reinterpret_cast<T*>(p.out) + row_global * p.dv;
+    T* orow = reinterpret_cast<T*>(p.out) + o_offset(p, b, h, i);
     if (M == -INFINITY) {
 #pragma unroll
       for (int kk = 0; kk < kMaxDvPerThread; ++kk) {
@@ -250,7 +250,7 @@ sdpa_merge_partials(const Params p) {
   __syncthreads();
 #pragma unroll
   for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, red[w]);
-  T* orow = reinterpret_cast<T*>(p.out) + row * p.dv;
+  T* orow = reinterpret_cast<T*>(p.out) + o_offset(p, row / (p.Lq * p.Hq), h, row % p.Lq);
   if (M == -INFINITY) {
     for (int c = threadIdx.x; c < dv; c += kMergeWarps * 32) orow[c] = from_f32<T>(0.f);
     if (threadIdx.x == 0 && p.lse) p.lse[row] = -INFINITY;
@@ -299,11 +299,11 @@ __global__ void sdpa_fill_no_keys(const Params p) {
   T* out = reinterpret_cast<T*>(p.out);
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
        e += (int64_t)gridDim.x * blockDim.x) {
-    out[e] = from_f32<T>(0.f);
-    if (p.lse && e % p.dv == 0) {
-      const int64_t row = e / p.dv, h = (row / p.Lq) % p.Hq;
+    const int64_t row = e / p.dv, c = e % p.dv;
+    const int64_t i = row % p.Lq, h = (row / p.Lq) % p.Hq, b = row / (p.Lq * p.Hq);
+    out[o_offset(p, b, h, i) + c] = from_f32<T>(0.f);
+    if (p.lse && c == 0)
       p.lse[row] = p.has_sinks ? to_f32<T>(reinterpret_cast<const T*>(p.sinks)[h]) : -INFINITY;
-    }
   }
 }
 

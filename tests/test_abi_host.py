@@ -51,7 +51,7 @@ def test_only_abi_symbols_are_exported(nv):
 
 
 def test_abi_version_and_status_strings(nv):
-    assert nv.nv_sdpa_abi_version() == 1
+    assert nv.nv_sdpa_abi_version() == 2
     for s in range(5):
         assert nv.nv_sdpa_status_string(s) and "unknown" not in nv.nv_sdpa_status_string(s)
     assert "unknown" in nv.nv_sdpa_status_string(99)
