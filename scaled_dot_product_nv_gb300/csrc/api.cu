@@ -523,7 +523,9 @@ int check_paged(const nv_sdpa_paged_dims* pd, int mask_kind, int has_window, int
   if (x->Lq > 8) return NV_SDPA_ERR_UNSUPPORTED;  // paged caches serve the decode path
   cs->x = *x;
   cs->span = cap;
-  if (has_window && window < cap) cs->span = std::min<int64_t>(cap, window + std::max<int64_t>(x->Lq, 1) - 1);
+  // (+ one key tile: paged tiles start on a tile boundary at or before the band)
+  if (has_window && window < cap)
+    cs->span = std::min<int64_t>(cap, window + std::max<int64_t>(x->Lq, 1) - 1 + decode_mma_key_tile());
   cs->qo_packed = true;
   cs->paged = true;
   return NV_SDPA_OK;

@@ -22,477 +22,11 @@
 //   on the accumulator fragments (row max over a lane quad), P re-packed in registers as
 //   the A operand of O += P V with V read by ldmatrix.trans.  Tensor-core math keeps the
 //   SMs far from the ALU limit that FP32 dot products would hit at 8 query rows per key.
-#include <cuda.h>
-
-#include "common.cuh"
-#include "kernels.h"
-#include "sm100_ptx.cuh"
+#include "decode_kernel.cuh"
 
 namespace nvsdpa {
-namespace {
 
-using namespace sm100;
-
-constexpr int kRowsDec = 16;     // query rows per warp (the M of m16n8k16)
-constexpr int kKTMax = 32;       // the largest key tile of any bucket (key blocks are multiples of 64)
-constexpr float kRescaleLog2Dec = 8.0f;
-constexpr uint64_t kDrainLimitDec = 1ull << 18;  // polls of <= ~10 us each
-
-struct DecArgs {
-  CUtensorMap tmk, tmv;
-  Params p;
-  int n_rc;       // row tiles of 16 rows per KV head
-  int dpanels, dvpanels;
-};
-
-template <typename T> struct MmaOp;
-template <> struct MmaOp<__half> {
-  __device__ static __forceinline__ void run(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  }
-  __device__ static __forceinline__ uint32_t pack(float lo, float hi) { return pack_f16(lo, hi); }
-};
-template <> struct MmaOp<__nv_bfloat16> {
-  __device__ static __forceinline__ void run(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  }
-  __device__ static __forceinline__ uint32_t pack(float lo, float hi) { return pack_bf16(lo, hi); }
-};
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-// Byte address of (row, 16-byte chunk) in a [rows][128 B] panel written by TMA with the
-// 128-byte swizzle (chunk index XOR row mod 8).
-__device__ __forceinline__ uint32_t sw128(uint32_t panel, int row, int chunk) {
-  return panel + row * 128 + ((chunk ^ (row & 7)) << 4);
-}
-
-// Shape of each (d, dv) bucket's kernel: keys per tile, warps per CTA and ring stages
-// per warp, so that about 192 KB of loads are in flight per SM.  The per-warp mma.sync
-// work is what bounds the stream, so heads up to 128 run 8 warps (two per scheduler) on
-// 16-key tiles; larger heads, whose accumulators would not fit 8 warps' registers, run
-// 3-4 warps on 32-key tiles.  (Measured on the 8 x 32/4 x 32769-key f16 decode: 4 warps
-// of 32-key tiles 4430 GB/s, 8 warps of 16-key tiles 5390 GB/s; 6, 7, 10 or 12 warps
-// lose to an uneven share of key blocks or to register spills.)
-template <int DMAX, int DV> struct DecShape {
-  static constexpr bool kSmallHead = DMAX <= 128 && DV <= 128;
-  static constexpr int KT = kSmallHead ? 16 : 32;
-  static constexpr int kStageBytes = (DMAX / 64 + DV / 64) * KT * 128;
-  static constexpr int WPC = kSmallHead ? 8 : (DMAX >= 256) ? 3 : 4;
-  static constexpr int ST = (WPC * 3 * kStageBytes <= 192 * 1024) ? 3 : 2;
-  static constexpr int kSmem = WPC * ST * kStageBytes + 1024 + WPC * ST * 8 + 64;
-  static constexpr int kCtasPerSm = (kSmem <= 113 * 1024) ? 2 : 1;
-};
-
-template <typename T, int DMAX, int DV>
-__global__ void __launch_bounds__(DecShape<DMAX, DV>::WPC * 32, DecShape<DMAX, DV>::kCtasPerSm)
-sdpa_decode_mma(const __grid_constant__ DecArgs a) {
-  using Sh = DecShape<DMAX, DV>;
-  constexpr int ST = Sh::ST;
-  constexpr int kKT = Sh::KT;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const Params& p = a.p;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gid = lane >> 2, tig = lane & 3;
-
-  const uint32_t k_bytes = a.dpanels * kKT * 128, v_bytes = a.dvpanels * kKT * 128;
-  const uint32_t stage_bytes = k_bytes + v_bytes;
-  const uint32_t ring = smem_addr(base) + warp * ST * stage_bytes;  // this warp's stages
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + Sh::WPC * ST * stage_bytes);
-  auto full = [&](int s) { return smem_addr(bars + warp * ST + s); };
-
-  // the merge pass may be scheduled once every CTA of this grid is running
-  asm volatile("griddepcontrol.launch_dependents;");
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < Sh::WPC * ST; ++i) mbar_init(smem_addr(bars + i), 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  // ---- this warp's work: (b, KV head, row tile) and a contiguous run of its key blocks
-  const int64_t gw = (int64_t)blockIdx.x * Sh::WPC + warp;
-  if (gw >= p.B * p.Hkv * a.n_rc * p.spans) return;
-  const int64_t span = gw % p.spans;
-  const int64_t unit = gw / p.spans;
-  const int64_t rc = unit % a.n_rc;
-  const int64_t bh = unit / a.n_rc;
-  const int64_t b = bh / p.Hkv, hkv = bh % p.Hkv;
-  const int64_t Lkb = seq_keys(p, b);
-  const int64_t rows_here = (p.G - rc * kRowsDec < kRowsDec) ? p.G - rc * kRowsDec : kRowsDec;
-
-  // The keys any row of the tile may see, [u_lo, u_hi): the blocks of the plan's split are
-  // cut from u_lo (with a window, the band's first key), so that a one-query row's blocks
-  // are those of a call over exactly its band.
-  const int64_t r0 = rc * kRowsDec, r1 = r0 + rows_here - 1;
-  const bool one_head = r0 / p.Lq == r1 / p.Lq;
-  const int64_t imin = one_head ? r0 % p.Lq : 0, imax = one_head ? r1 % p.Lq : p.Lq - 1;
-  const int64_t u_lo = row_key_lo(p, imin + Lkb - p.Lq);
-  const int64_t u_hi = row_key_hi(p, imax + Lkb - p.Lq, Lkb);
-  const int64_t c_begin = span * p.nblk / p.spans, c_end = (span + 1) * p.nblk / p.spans;
-  const int64_t key_begin = u_lo + c_begin * p.keys_per_blk;
-  int64_t key_end = u_lo + c_end * p.keys_per_blk;
-  if (key_end > u_hi) key_end = u_hi;
-  const int n_tiles = key_end > key_begin ? (int)((key_end - key_begin + kKT - 1) / kKT) : 0;
-  const int tpb = (int)(p.keys_per_blk / kKT);  // tiles per (full) key block
-  const uint64_t limit = p.wait_limit;
-
-  // tile i of the run into ring slot i % ST: by TMA (lane 0), or for paged caches by
-  // 16-byte copies of every lane, key row by key row through the page table (rows outside
-  // [key_begin, key_end) and columns past the head are zero-filled, never read)
-  const T* kg = reinterpret_cast<const T*>(p.k);
-  const T* vg = reinterpret_cast<const T*>(p.v);
-  const int ck = (int)(p.d / 8), cv = (int)(p.dv / 8);   // 16-byte chunks of a K / V row
-  const int pk = a.dpanels * 8, pv = a.dvpanels * 8;     // chunks of a panelled smem row
-  auto issue = [&](int i) {
-    const int s = i % ST;
-    const int64_t key0 = key_begin + (int64_t)i * kKT;
-    if (!p.paged) {
-      if (lane == 0) {
-        mbar_arrive_expect_tx(full(s), stage_bytes);
-        for (int pn = 0; pn < a.dpanels; ++pn)
-          tma_load_4d(ring + s * stage_bytes + pn * kKT * 128, &a.tmk, full(s), pn * 64, (int)key0, (int)hkv, (int)b);
-        for (int pn = 0; pn < a.dvpanels; ++pn)
-          tma_load_4d(ring + s * stage_bytes + k_bytes + pn * kKT * 128, &a.tmv, full(s), pn * 64, (int)key0,
-                      (int)hkv, (int)b);
-      }
-      return;
-    }
-    const int per_row = pk + pv;
-    for (int e = lane; e < kKT * per_row; e += 32) {
-      const int r = e / per_row, cc = e - r * per_row;
-      const int64_t j = key0 + r;
-      const bool is_k = cc < pk;
-      const int ch = is_k ? cc : cc - pk;               // chunk within the K or V row
-      const bool in = j < key_end && ch < (is_k ? ck : cv);
-      const T* src = kg;
-      if (in)
-        src = is_k ? kg + kv_offset(p, b, hkv, j, 0, 0, 0, p.d) + ch * 8
-                   : vg + kv_offset(p, b, hkv, j, 0, 0, 0, p.dv) + ch * 8;
-      const uint32_t panel = ring + s * stage_bytes + (is_k ? 0u : k_bytes) + (ch >> 3) * kKT * 128;
-      cp_async16_zfill(sw128(panel, r, ch & 7), src, in ? 16u : 0u);
-    }
-  };
-  // waits until tile i has landed in its slot (bounded for TMA; the paged copies are this
-  // warp's own and always complete)
-  auto landed = [&](int i) -> bool {
-    if (!p.paged) return __all_sync(0xffffffffu, mbar_wait(full(i % ST), (i / ST) & 1, limit, nullptr));
-    __syncwarp();
-    return true;
-  };
-  int issued = n_tiles < ST ? n_tiles : ST;
-  if (!p.paged && lane == 0) {
-    tma_prefetch_desc(&a.tmk);
-    tma_prefetch_desc(&a.tmv);
-  }
-  for (int i = 0; i < ST; ++i) {
-    if (i < issued) issue(i);
-    if (p.paged) cp_async_commit();  // one group per slot, empty ones included
-  }
-
-  // This lane's two query rows (gid and gid + 8 of the row tile): the keys [lo, hi) each
-  // may see (32-bit: the planner sends no longer sequence here) and its mask row (boolean
-  // bytes or additive values, by mask kind).
-  int lo[2], hi[2];
-  bool rok[2];
-  const void* mk[2];
-  const bool bool_mask = p.mask_kind == kMaskBool, add_mask = p.mask_kind == kMaskAdd;
-#pragma unroll
-  for (int hrow = 0; hrow < 2; ++hrow) {
-    const int r = gid + 8 * hrow;
-    rok[hrow] = r < rows_here;
-    const int64_t rho = rc * kRowsDec + (rok[hrow] ? r : 0);
-    const int64_t i = rho % p.Lq, h = hkv * p.g + rho / p.Lq;
-    const int64_t pos = i + Lkb - p.Lq;
-    lo[hrow] = (int)row_key_lo(p, pos);
-    hi[hrow] = (int)row_key_hi(p, pos, Lkb);
-    mk[hrow] = bool_mask ? static_cast<const void*>(p.mask + i * p.Lk)
-                         : (add_mask ? static_cast<const void*>(reinterpret_cast<const T*>(p.amask) + b * p.am_sb +
-                                                                h * p.am_sh + i * p.Lk)
-                                     : nullptr);
-  }
-
-  // Q fragments (A operand, row-major m16 x k16 per k-block), straight from global memory.
-  constexpr int kKB = DMAX / 16;  // k-blocks of the d bucket
-  const int nkb = (int)((p.d + 15) / 16);
-  uint32_t qa[kKB][4];
-  {
-    const T* qrow[2];
-#pragma unroll
-    for (int hrow = 0; hrow < 2; ++hrow) {
-      const int64_t rho = rc * kRowsDec + (rok[hrow] ? gid + 8 * hrow : 0);
-      qrow[hrow] = reinterpret_cast<const T*>(p.q) + q_offset(p, b, hkv * p.g + rho / p.Lq, rho % p.Lq);
-    }
-#pragma unroll
-    for (int kb = 0; kb < kKB; ++kb) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int hrow = e & 1;
-        const int c = kb * 16 + 2 * tig + 8 * (e >> 1);
-        uint32_t v = 0;
-        if (kb < nkb && rok[hrow] && c < p.d) v = *reinterpret_cast<const uint32_t*>(qrow[hrow] + c);
-        qa[kb][e] = v;
-      }
-    }
-  }
-
-  constexpr int NT = DV / 8;  // n-tiles of the output
-  const int dv = (int)p.dv;
-  float o[NT][4];
-#pragma unroll
-  for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-  int consumed = 0;
-
-  // The partial of key block c from this warp's running (m, l, o) -- or, with a single
-  // block, the final output -- and a fresh start for the next block.
-  auto flush = [&](int64_t c) {
-    float L[2];
-#pragma unroll
-    for (int hrow = 0; hrow < 2; ++hrow) {
-      L[hrow] = l[hrow] + __shfl_xor_sync(0xffffffffu, l[hrow], 1);
-      L[hrow] += __shfl_xor_sync(0xffffffffu, L[hrow], 2);
-    }
-#pragma unroll
-    for (int hrow = 0; hrow < 2; ++hrow) {
-      if (!rok[hrow]) continue;
-      const int64_t rho = rc * kRowsDec + gid + 8 * hrow;
-      const int64_t ri = rho % p.Lq, hr = hkv * p.g + rho / p.Lq;
-      const int64_t row_global = (b * p.Hq + hr) * p.Lq + ri;
-      const float M = m[hrow];
-      if (p.nblk == 1) {
-        const float sk = sink_log2<T>(p, hr);
-        const float Mf = fmaxf(M, sk);
-        float f = 0.f, Lf = 0.f;
-        if (Mf != -INFINITY) {
-          const float am = (M == -INFINITY) ? 0.f : ex2(M - Mf);
-          Lf = L[hrow] * am + ex2(sk - Mf);
-          f = am / Lf;
-        }
-        T* orow = reinterpret_cast<T*>(p.out) + o_offset(p, b, hr, ri);
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          const int cc = j * 8 + 2 * tig;
-          if (cc < dv)
-            *reinterpret_cast<uint32_t*>(orow + cc) = MmaOp<T>::pack(o[j][2 * hrow] * f, o[j][2 * hrow + 1] * f);
-        }
-        if (tig == 0 && p.lse) p.lse[row_global] = (Mf == -INFINITY) ? -INFINITY : (Mf + log2f(Lf)) * kLn2;
-      } else {
-        float* po = p.part_o + (row_global * p.nblk + c) * p.dv;
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          const int cc = j * 8 + 2 * tig;
-          if (cc < dv) *reinterpret_cast<float2*>(po + cc) = make_float2(o[j][2 * hrow], o[j][2 * hrow + 1]);
-        }
-        if (tig == 0) {
-          p.part_ml[(row_global * p.nblk + c) * 2 + 0] = M;
-          p.part_ml[(row_global * p.nblk + c) * 2 + 1] = L[hrow];
-        }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-    m[0] = m[1] = -INFINITY;
-    l[0] = l[1] = 0.f;
-  };
-
-  bool ok = true;
-  for (int gt = 0; gt < n_tiles; ++gt) {
-    const int s = gt % ST;
-    if (p.paged) cp_async_wait<ST - 1>();
-    if (!landed(gt)) {
-      if (lane == 0) record_status(p, kStatTimeoutTmaFull);
-      ok = false;
-      break;
-    }
-    consumed = gt + 1;
-    const int64_t c = c_begin + gt / tpb;  // key block of this tile
-    const int64_t jb_end = u_lo + (c + 1) * p.keys_per_blk;
-    const int j_end = (int)(jb_end < key_end ? jb_end : key_end);
-    const uint32_t kst = ring + s * stage_bytes, vst = kst + k_bytes;
-    // ---- S = Q K^T over the tile's keys (n-tiles of 8 keys)
-    constexpr int NS = kKT / 8;  // n-tiles of S
-    float sc[NS][4];
-#pragma unroll
-    for (int nt = 0; nt < NS; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-#pragma unroll
-    for (int kb = 0; kb < kKB; ++kb) {
-      if (kb < nkb) {
-        const int chunk = (kb & 3) * 2 + ((lane >> 3) & 1);
-#pragma unroll
-        for (int h16 = 0; h16 < kKT / 16; ++h16) {
-          uint32_t b0, b1, b2, b3;
-          const int krow = h16 * 16 + (lane >> 4) * 8 + (lane & 7);
-          ldsm_x4(sw128(kst + (kb >> 2) * kKT * 128, krow, chunk), b0, b1, b2, b3);
-          MmaOp<T>::run(sc[2 * h16], qa[kb], b0, b1);
-          MmaOp<T>::run(sc[2 * h16 + 1], qa[kb], b2, b3);
-        }
-      }
-    }
-    // ---- mask, online softmax (rows gid / gid + 8; keys spread over the lane quad)
-    const int jt = (int)(key_begin + (int64_t)gt * kKT);
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int nt = 0; nt < NS; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int hrow = e >> 1;
-        const int j = jt + nt * 8 + 2 * tig + (e & 1);
-        bool vis = rok[hrow] && j < j_end && j >= lo[hrow] && j < hi[hrow];
-        if (bool_mask && vis) vis = static_cast<const uint8_t*>(mk[hrow])[j] != 0;
-        float v = -INFINITY;
-        if (vis) v = add_mask ? fmaf(sc[nt][e], p.scale_log2, to_f32<T>(static_cast<const T*>(mk[hrow])[j]) * kLog2e)
-                              : sc[nt][e] * p.scale_log2;
-        sc[nt][e] = v;
-        mx[hrow] = fmaxf(mx[hrow], v);
-      }
-    }
-    float alpha[2];
-#pragma unroll
-    for (int hrow = 0; hrow < 2; ++hrow) {
-      mx[hrow] = fmaxf(mx[hrow], __shfl_xor_sync(0xffffffffu, mx[hrow], 1));
-      mx[hrow] = fmaxf(mx[hrow], __shfl_xor_sync(0xffffffffu, mx[hrow], 2));
-      const float m_new = fmaxf(m[hrow], mx[hrow]);
-      alpha[hrow] = 1.f;
-      if (m_new > m[hrow] + kRescaleLog2Dec) {
-        alpha[hrow] = ex2(m[hrow] - m_new);
-        m[hrow] = m_new;
-      }
-    }
-    // P as the A operand of the k16 steps: pa[ks] covers keys 16 ks .. 16 ks + 15
-    uint32_t pa[kKT / 16][4];
-#pragma unroll
-    for (int hrow = 0; hrow < 2; ++hrow) l[hrow] *= alpha[hrow];
-#pragma unroll
-    for (int nt = 0; nt < NS; ++nt) {
-#pragma unroll
-      for (int hrow = 0; hrow < 2; ++hrow) {
-        const bool none = (m[hrow] == -INFINITY);
-        const float p0 = none ? 0.f : ex2(sc[nt][2 * hrow] - m[hrow]);
-        const float p1 = none ? 0.f : ex2(sc[nt][2 * hrow + 1] - m[hrow]);
-        l[hrow] += p0 + p1;
-        pa[nt >> 1][(nt & 1) * 2 + hrow] = MmaOp<T>::pack(p0, p1);
-      }
-    }
-    if (alpha[0] != 1.f || alpha[1] != 1.f) {
-#pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        o[j][0] *= alpha[0];
-        o[j][1] *= alpha[0];
-        o[j][2] *= alpha[1];
-        o[j][3] *= alpha[1];
-      }
-    }
-    // ---- O += P V: V tile rows = keys, ldmatrix.trans gives the k16 x n8 B fragments
-#pragma unroll
-    for (int ks = 0; ks < kKT / 16; ++ks) {
-      const int vrow = ks * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-#pragma unroll
-      for (int j2 = 0; j2 < NT / 2; ++j2) {
-        const int chunk = 2 * j2 + (lane >> 4);  // 16-byte chunk of dv (8 columns)
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(sw128(vst + (chunk >> 3) * kKT * 128, vrow, chunk & 7), b0, b1, b2, b3);
-        MmaOp<T>::run(o[2 * j2], pa[ks], b0, b1);
-        MmaOp<T>::run(o[2 * j2 + 1], pa[ks], b2, b3);
-      }
-    }
-    // ---- the slot is read: refill it with tile gt + ST (the async proxy's write must
-    // follow this warp's reads of the slot)
-    __syncwarp();
-    if (gt + ST < n_tiles) {
-      if (!p.paged && lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue(gt + ST);
-      issued = gt + ST + 1;
-    }
-    if (p.paged) cp_async_commit();
-
-    // ---- end of a key block: write its partial (or the output when it is the only one)
-    if ((gt + 1) % tpb == 0 || gt + 1 == n_tiles) flush(c);
-  }
-  if (ok) {
-    // key blocks of this run that hold no key of this tile's rows (past a sequence's
-    // length, outside a window) still get their (empty) partial, or the final output
-    for (int64_t c = c_begin + (n_tiles + tpb - 1) / tpb; c < c_end; ++c) flush(c);
-  }
-  // a wait that gave up leaves copies in flight: they land before the warp leaves
-  if (p.paged) {
-    cp_async_wait<0>();
-  } else if (lane == 0) {
-    for (int i = consumed; i < issued; ++i) mbar_wait(full(i % ST), (i / ST) & 1, kDrainLimitDec, nullptr);
-  }
-  __syncwarp();
-}
-
-template <typename T, int DMAX, int DV>
-cudaError_t launch_dec_t(const DecArgs& a, int64_t grid, cudaStream_t st) {
-  using Sh = DecShape<DMAX, DV>;
-  static std::atomic<unsigned long long> configured{0};
-  cudaError_t e = set_max_dynamic_smem_once(configured, (const void*)sdpa_decode_mma<T, DMAX, DV>, Sh::kSmem);
-  if (e != cudaSuccess) return e;
-  sdpa_decode_mma<T, DMAX, DV><<<(unsigned)grid, Sh::WPC * 32, Sh::kSmem, st>>>(a);
-  return cudaGetLastError();
-}
-
-// (d, dv) buckets with a kernel: the smallest bucket covering the head is used; the
-// TMA tiles zero-fill the columns between the head size and the bucket.
-constexpr int kDecBuckets[][2] = {{64, 64}, {128, 64}, {128, 128}, {192, 128}, {192, 192}, {256, 256}};
-
-int dec_bucket(int64_t d, int64_t dv) {
-  for (int i = 0; i < 6; ++i)
-    if (d <= kDecBuckets[i][0] && dv <= kDecBuckets[i][1]) return i;
-  return -1;
-}
-
-struct DecInfo {
-  int wpc, ctas_per_sm, smem, kt;
-};
-template <int DMAX, int DV>
-constexpr DecInfo dec_info_t() {
-  return {DecShape<DMAX, DV>::WPC, DecShape<DMAX, DV>::kCtasPerSm, DecShape<DMAX, DV>::kSmem, DecShape<DMAX, DV>::KT};
-}
-DecInfo dec_info(int64_t d, int64_t dv) {
-  switch (dec_bucket(d, dv)) {
-    case 0: return dec_info_t<64, 64>();
-    case 1: return dec_info_t<128, 64>();
-    case 2: return dec_info_t<128, 128>();
-    case 3: return dec_info_t<192, 128>();
-    case 4: return dec_info_t<192, 192>();
-    case 5: return dec_info_t<256, 256>();
-    default: return {0, 0, 0, 0};
-  }
-}
-
-template <typename T>
-cudaError_t launch_dec_bucket(const DecArgs& a, int64_t grid, cudaStream_t st) {
-  switch (dec_bucket(a.p.d, a.p.dv)) {
-    case 0: return launch_dec_t<T, 64, 64>(a, grid, st);
-    case 1: return launch_dec_t<T, 128, 64>(a, grid, st);
-    case 2: return launch_dec_t<T, 128, 128>(a, grid, st);
-    case 3: return launch_dec_t<T, 192, 128>(a, grid, st);
-    case 4: return launch_dec_t<T, 192, 192>(a, grid, st);
-    case 5: return launch_dec_t<T, 256, 256>(a, grid, st);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
-}  // namespace
+using namespace dec;
 
 bool decode_mma_supported(int dtype, int64_t d, int64_t dv) {
   return (dtype == 1 || dtype == 2) && d % 16 == 0 && dv % 16 == 0 && dec_bucket(d, dv) >= 0;
@@ -510,28 +44,19 @@ int64_t decode_mma_grid(int64_t warp_units, int64_t d, int64_t dv) {
 }
 
 cudaError_t launch_decode_mma(int dtype, const Params& p, cudaStream_t st) {
+  if (p.paged) return launch_decode_paged(dtype, p, st);
   DecArgs a;
   memset(&a, 0, sizeof(a));
   a.p = p;
-  const int64_t BH = p.B * p.Hkv;
   const int kt = dec_info(p.d, p.dv).kt;
   if (!kt) return cudaErrorInvalidValue;
-  if (!p.paged) {
-    // K and V as 4-D [B][Hkv][Lk][d] views with the caller's strides (a slice of a longer
-    // cache or a transposed [B, L, H, D] layout reads in place)
-    const int64_t kd[4] = {p.d, p.Lk, p.Hkv, p.B}, ks[3] = {p.k_sl, p.k_sh, p.k_sb};
-    const int64_t vd[4] = {p.dv, p.Lk, p.Hkv, p.B}, vs[3] = {p.v_sl, p.v_sh, p.v_sb};
-    if (!encode_tiled_16bit(&a.tmk, dtype, p.k, 4, kd, ks, kt) || !encode_tiled_16bit(&a.tmv, dtype, p.v, 4, vd, vs, kt))
-      return cudaErrorInvalidValue;
-  }
-  a.n_rc = (int)((p.G + kRowsDec - 1) / kRowsDec);
-  a.dpanels = (int)((p.d + 63) / 64);
-  a.dvpanels = (int)((p.dv + 63) / 64);
-  // every warp walks whole key blocks: a block size that is not a whole number of tiles,
-  // or a run count outside [1, blocks], is a planner error
-  if (p.spans < 1 || p.spans > p.nblk || p.keys_per_blk % kt != 0) return cudaErrorInvalidValue;
-  const int64_t grid = decode_mma_grid(BH * a.n_rc * p.spans, p.d, p.dv);
-  return dtype == 1 ? launch_dec_bucket<__half>(a, grid, st) : launch_dec_bucket<__nv_bfloat16>(a, grid, st);
+  // K and V as 4-D [B][Hkv][Lk][d] views with the caller's strides (a slice of a longer
+  // cache or a transposed [B, L, H, D] layout reads in place)
+  const int64_t kd[4] = {p.d, p.Lk, p.Hkv, p.B}, ks[3] = {p.k_sl, p.k_sh, p.k_sb};
+  const int64_t vd[4] = {p.dv, p.Lk, p.Hkv, p.B}, vs[3] = {p.v_sl, p.v_sh, p.v_sb};
+  if (!encode_tiled_16bit(&a.tmk, dtype, p.k, 4, kd, ks, kt) || !encode_tiled_16bit(&a.tmv, dtype, p.v, 4, vd, vs, kt))
+    return cudaErrorInvalidValue;
+  return launch_dec_kv<kKvTma>(dtype, a, st);
 }
 
 }  // namespace nvsdpa

@@ -62,5 +62,7 @@ int decode_mma_ctas_per_sm(int64_t d, int64_t dv);
 int decode_mma_warps_per_cta(int64_t d, int64_t dv);
 int64_t decode_mma_grid(int64_t warp_units, int64_t d, int64_t dv);
 cudaError_t launch_decode_mma(int dtype, const Params& p, cudaStream_t st);
+// decode_paged.cu
+cudaError_t launch_decode_paged(int dtype, const Params& p, cudaStream_t st);
 
 }  // namespace nvsdpa
