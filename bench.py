@@ -394,6 +394,18 @@ def feature_lines(torch, nv, dev, stream, pk, pc, px, dc, dx, mc, mx, args):
     out["additive_prefill"] = tc_line(mc.name.replace("bool", "additive"), prefill_flops(mc), ms,
                                       {"mask_bytes_per_call": am.numel() * 2})
     del mq, mk_, mv, am, mo
+    # decode with one sequence (the measured key split's case) and with 8 queries per sequence
+    for name, B1, Lq1 in (("decode_b1", 1, 1), ("decode_lq8", dc.B, 8)):
+        c1 = dc.with_(B=B1, Lq=Lq1)
+        x1 = W.make_inputs(c1)
+        q1, k1, v1, s1 = (up(x1[n], c1.dtype) for n in ("q", "k", "v", "sinks"))
+        o1 = torch.empty((c1.B, c1.Hq, c1.Lq, c1.dv), dtype=q1.dtype, device=dev)
+        ms = timed(lambda: nv.sdpa(q1, k1, v1, mask_kind="causal", scale=c1.scale_f32, sinks=s1, out=o1,
+                                   want_lse=False))
+        _, pl1 = nv.nv_sdpa_plan((c1.B, c1.Hq, c1.Hkv, c1.Lq, c1.Lk, c1.d, c1.dv), 1, 1, W.DTYPE_CODES[c1.dtype])
+        out[name] = hbm_line(f"decode_f16_b{c1.B}_h32x4_lq{c1.Lq}_lk32769_d128_sinks", kv_bytes(c1), ms,
+                             {"nblk": pl1["nblk"], "keys_per_blk": pl1["keys_per_blk"]})
+        del q1, k1, v1, o1
     # decode: a window of 4096 over the 32769 keys, and the keys in a paged cache
     dq, dk, dv_ = (up(dx[n], dc.dtype) for n in ("q", "k", "v"))
     dsk = up(dx["sinks"], dc.dtype)

@@ -11,10 +11,12 @@
 #include <mutex>
 #include <vector>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 
 #include "nv_sdpa.h"
 #include "common.cuh"
+#include "decode_blocks_table.h"
 #include "kernels.h"
 
 #define NV_SDPA_API extern "C" __attribute__((visibility("default")))
@@ -203,6 +205,17 @@ CallShape call_shape(const nv_sdpa_dims& x, const Resolved& r) {
   return c;
 }
 
+// NV_SDPA_DECODE_BLOCKS=n forces n key blocks on the tensor-core decode: a tuning and
+// measurement override (unset, 0 or not a number: the planner's own choice).  Read at
+// every plan, so a plan is pure only for a fixed environment.
+int64_t decode_blocks_override() {
+  const char* s = std::getenv("NV_SDPA_DECODE_BLOCKS");
+  if (!s || !*s) return 0;
+  char* end = nullptr;
+  const long long v = std::strtoll(s, &end, 10);
+  return (end && *end == 0 && v > 0) ? (int64_t)v : 0;
+}
+
 // The decode key split: blocks of keys_per_blk (a multiple of `quantum`) over `span`
 // keys, enough of them that one batch item alone keeps 2 x (SM count) warps streaming,
 // each at least 256 keys.  Depends on the head shape and the span alone, never on B.
@@ -214,6 +227,34 @@ void split_keys(int64_t span, int64_t units_per_item, int64_t quantum, int64_t* 
   const int64_t kpb = cdiv(cdiv(span, nblk), quantum) * quantum;
   *kpb_out = kpb;
   *nblk_out = std::max<int64_t>(1, cdiv(span, kpb));
+}
+
+// The tensor-core decode's key split from the measured table: the nearest entry (head
+// bucket first, then work units per batch item, then span, each by ratio) gives the keys
+// per block, and the span is cut into blocks of that many keys (at most the merge pass's
+// limit).
+void split_keys_measured(int64_t dmax, int64_t units_per_item, int64_t span, int64_t* nblk_out,
+                         int64_t* kpb_out) {
+  const DecodeBlocksEntry* best = &kDecodeBlocks[0];
+  double best_d = 1e300;
+  for (const DecodeBlocksEntry& t : kDecodeBlocks) {
+    const double dd = 4.0 * std::fabs(std::log2((double)t.dmax / (double)std::max<int64_t>(dmax, 1))) +
+                      2.0 * std::fabs(std::log2((double)t.units / (double)std::max<int64_t>(units_per_item, 1))) +
+                      std::fabs(std::log2((double)t.span / (double)std::max<int64_t>(span, 1)));
+    if (dd < best_d) {
+      best_d = dd;
+      best = &t;
+    }
+  }
+  int64_t kpb = best->keys_per_blk;
+  int64_t nblk = std::max<int64_t>(1, cdiv(span, kpb));
+  if (nblk > merge_max_blocks()) {
+    nblk = merge_max_blocks();
+    kpb = cdiv(cdiv(span, nblk), 64) * 64;
+    nblk = cdiv(span, kpb);
+  }
+  *nblk_out = nblk;
+  *kpb_out = kpb;
 }
 
 // The router.  Pure for a given device: depends on its arguments and the current
@@ -260,7 +301,8 @@ int make_plan(const CallShape& cs, int mask_kind, int has_sinks, int dtype, nv_s
   }
   if (pl->path == NV_SDPA_PATH_DECODE && decode_mma_supported(dtype, x.d, x.dv)) {
     // Tensor-core decode.  The keys of each KV head are cut into blocks that depend on
-    // the head shape and the span alone, never on B.  Every block's partial is computed
+    // the head shape and the span alone, never on B: their size comes from the table of
+    // rates measured on a GB300 (decode_blocks_table.h).  Every block's partial is computed
     // the same way whichever warp computes it, so a batch item gets the bits it would get
     // alone.  How many warps share a (b, KV head, 16-row tile)'s blocks (each walking a
     // contiguous run of them) is free, and is chosen so that all warps run as one wave:
@@ -269,7 +311,12 @@ int make_plan(const CallShape& cs, int mask_kind, int has_sinks, int dtype, nv_s
     pl->kernel = NV_SDPA_KERNEL_DECODE_MMA;
     pl->rows_per_cta = decode_mma_rows_per_warp();
     const int64_t rc = cdiv(G, pl->rows_per_cta);
-    split_keys(cs.span, x.Hkv * rc, 64, &pl->nblk, &pl->keys_per_blk);
+    split_keys_measured(std::max(x.d, x.dv), x.Hkv * rc, cs.span, &pl->nblk, &pl->keys_per_blk);
+    if (const int64_t forced = decode_blocks_override()) {
+      const int64_t nb = std::max<int64_t>(1, std::min(forced, std::min(cdiv(cs.span, 64), merge_max_blocks())));
+      pl->keys_per_blk = cdiv(cdiv(cs.span, nb), 64) * 64;
+      pl->nblk = cdiv(cs.span, pl->keys_per_blk);
+    }
     int64_t units, warp_units;
     if (!mul_ok(x.B * x.Hkv, rc, &units) || !mul_ok(units, decode_spans(x, pl->nblk), &warp_units))
       return NV_SDPA_ERR_UNSUPPORTED;

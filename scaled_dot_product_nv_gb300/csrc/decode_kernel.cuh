@@ -246,14 +246,9 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
       return true;
     }
   };
-  int issued = n_tiles < ST ? n_tiles : ST;
   if (KV != kKvPagedRows && lane == 0) {
     tma_prefetch_desc(&a.tmk);
     tma_prefetch_desc(&a.tmv);
-  }
-  for (int i = 0; i < ST; ++i) {
-    if (i < issued) issue(i);
-    if constexpr (KV == kKvPagedRows) cp_async_commit();  // one group per slot, empty ones included
   }
 
   // This lane's two query rows (gid and gid + 8 of the row tile): the keys [lo, hi) each
@@ -361,6 +356,14 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
     m[0] = m[1] = -INFINITY;
     l[0] = l[1] = 0.f;
   };
+
+  // the first ST tiles of the run (issued after the setup's global loads, so that the
+  // loop's first wait follows the copies closely)
+  int issued = n_tiles < ST ? n_tiles : ST;
+  for (int i = 0; i < ST; ++i) {
+    if (i < issued) issue(i);
+    if constexpr (KV == kKvPagedRows) cp_async_commit();  // one group per slot, empty ones included
+  }
 
   bool ok = true;
   for (int gt = 0; gt < n_tiles; ++gt) {

@@ -400,15 +400,16 @@ def test_paged_clamps_hostile_tables_and_lengths(dt, B, hq, hkv, lq, d, bs, max_
     compare(f"hostile {dt}", c, got, glse, want, wlse)
 
 
-def test_paged_single_pass_equals_contiguous_bits():
-    """Where both plans take one key block, paged attention gives the contiguous call's bits."""
+def test_paged_equals_contiguous_bits_on_the_same_split():
+    """Where both plans cut the keys into the same blocks, paged attention gives the
+    contiguous call's bits."""
     import torch
     nv = ensure_built()
     c = _case(2, 8, 2, 1, 200, 128, 128, "f16", "causal", True, 801, "u2")
     x, kc, vc, table, ln = _paged_inputs(c, [200, 200], 16, 801, extra_blocks=0)
     _, pp = nv.nv_sdpa_paged_plan((2, 8, 2, 1, 128, 128, kc.shape[0], 16, table.shape[1]), 1, 0, 0, 1, 1)
     _, pc = nv.nv_sdpa_plan((2, 8, 2, 1, 200, 128, 128), 1, 1, 1)
-    assert pp["nblk"] == pc["nblk"] == 1
+    assert (pp["nblk"], pp["keys_per_blk"]) == (pc["nblk"], pc["keys_per_blk"])
     got, glse = run_paged(c, x, kc, vc, table, ln)
     one, one_lse = run_ex(c, x)
     assert np.array_equal(got, one) and np.array_equal(glse, one_lse)

@@ -324,7 +324,7 @@ def _scale_cases():
                                          seed=64), "prefill_tc", False),
         ("decode_split", W.Case(2, 8, 2, 1, 3000, 128, 128, "f16", "causal", True, None, "u2", seed=65),
          "decode_mma", True),
-        ("decode_one_block", W.Case(1, 4, 4, 3, 200, 64, 64, "bf16", "none", False, None, "n0.5", seed=66),
+        ("decode_one_block", W.Case(1, 4, 4, 3, 60, 64, 64, "bf16", "none", False, None, "n0.5", seed=66),
          "decode_mma", False),
         ("decode_bool", W.Case(1, 8, 2, 5, 900, 128, 128, "bf16", "bool", True, None, "n0.5", seed=67),
          "decode_mma", True),
