@@ -324,6 +324,54 @@ def window_pairs(Lq, Lk, W):
     return float(np.maximum(hi - lo, 0).sum())
 
 
+def sweep_lines(torch, nv, dev, stream, pk):
+    """Throughput of every case of the 108-case bf16 head-shape sweep (parity cases; most
+    are small and latency-bound): per (d, dv), the min / median / max roofline fraction
+    over its prefill cases (TFLOP/s of the tensor peak) and its decode cases (GB/s of K+V
+    against the copy bandwidth), each call timed as CUDA-graph-free back-to-back calls."""
+    per = {}
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5000)
+    for c in W.sweep_bf16():
+        # the sweep's value recipe, U[0, 2), drawn on the device (timing only)
+        shapes = {"q": (c.B, c.Hq, c.Lq, c.d), "k": (c.B, c.Hkv, c.Lk, c.d), "v": (c.B, c.Hkv, c.Lk, c.dv)}
+        t = {n: (torch.rand(sh, generator=gen, device=dev) * 2).to(torch.bfloat16) for n, sh in shapes.items()}
+        o = torch.empty((c.B, c.Hq, c.Lq, c.dv), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((c.B, c.Hq, c.Lq), dtype=torch.float32, device=dev)
+        dims = (c.B, c.Hq, c.Hkv, c.Lq, c.Lk, c.d, c.dv)
+        mk = W.MASK_CODES[c.mask]
+
+        def call():
+            st = nv.nv_sdpa(t["q"].data_ptr(), t["k"].data_ptr(), t["v"].data_ptr(), dims, mk, 0, 0, c.scale_f32,
+                            o.data_ptr(), lse.data_ptr(), 2, stream.cuda_stream)
+            if st != 0:
+                raise nv.NvSdpaError(st)
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(20):
+            call()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / 20
+        if c.Lq == 1:
+            frac = kv_bytes(c) / (ms / 1e3) / 1e9 / pk["hbm_gbs"]
+            kind = "decode"
+        else:
+            frac = prefill_flops(c) / (ms / 1e3) / 1e12 / pk["bf16_tflops"]
+            kind = "prefill"
+        per.setdefault(f"{c.d}x{c.dv} {kind}", []).append((frac, ms, c.name))
+    out = {}
+    for key, v in sorted(per.items()):
+        fr = sorted(f for f, _, _ in v)
+        best = max(v)
+        out[key] = {"cases": len(v), "frac_min": round(fr[0], 4), "frac_median": round(fr[len(fr) // 2], 4),
+                    "frac_max": round(fr[-1], 4), "best_case": best[2], "best_ms": round(best[1], 5)}
+    return out
+
+
 def feature_lines(torch, nv, dev, stream, pk, pc, px, dc, dx, mc, mx, args):
     """Throughput of the options beyond nv_sdpa() on the workloads' shapes: causal sliding
     windows (prefill and decode), paged decode, an additive-mask prefill and a prefill with
@@ -576,6 +624,7 @@ def run_ours(args):
 
     # --------------------------------------------------------------- the options beyond nv_sdpa()
     features = feature_lines(torch, nv, dev, stream, pk, pc, px, dc, dx, mc, mx, args)
+    sweep = sweep_lines(torch, nv, dev, stream, pk)
 
     # --------------------------------------------------------------- end to end (host buffers)
     e2e_steps = min(args.steps, 10)
@@ -642,6 +691,7 @@ def run_ours(args):
         "decode": decode,
         "prefill_mask": prefill_mask,
         "features": features,
+        "sweep": sweep,
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "api": "nv_sdpa_host (pinned host buffers; copies, device alloc, sync inside)"},
@@ -709,27 +759,53 @@ def run_reference(args):
 
 def run_profile_case(args):
     """Launches one workload `args.steps` times with no timing or JSON: the program an
-    ncu capture runs (small enough to profile: the workloads' own sizes, < 1 GB)."""
+    ncu capture runs (small enough to profile: the workloads' own sizes, < 2 GB)."""
     import torch
     import scaled_dot_product_nv_gb300 as nv
-    case = {"prefill": W.prefill_bf16_gqa(), "decode": W.decode_f16_long_kv(),
-            "mask": W.prefill_f16_boolmask_sinks(), "tiny": W.tiny_f32_causal()}[args.profile_case]
-    x = W.make_inputs(case)
+    cases = {"prefill": W.prefill_bf16_gqa(), "decode": W.decode_f16_long_kv(),
+             "mask": W.prefill_f16_boolmask_sinks(), "tiny": W.tiny_f32_causal(),
+             # the 256-wide decode bucket (3 warps per CTA, 32-key tiles)
+             "decode256": W.Case(8, 16, 2, 1, 32769, 256, 256, "f16", "causal", True, None, "u2", seed=7,
+                                 name="decode_f16_b8_h16x2_lk32769_d256_sinks"),
+             # f32 decode on the FP32-FMA kernel, split over key blocks
+             "f32": W.Case(8, 32, 4, 1, 8193, 128, 128, "f32", "causal", True, None, "u2", seed=8,
+                           name="decode_f32_b8_h32x4_lk8193_d128_sinks"),
+             "paged": W.decode_f16_long_kv()}
+    case = cases[args.profile_case]
     dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(case.seed)
+    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[case.dtype]
 
-    def up(a, dt):
-        if a is None:
-            return None
-        if dt == "bf16":
-            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
-        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-    q, k, v, s = (up(x[n], case.dtype) for n in ("q", "k", "v", "sinks"))
-    m = up(x["mask"], "u8")
-    for _ in range(args.steps):
-        nv.sdpa(q, k, v, mask_kind=case.mask, scale=case.scale_f32, bool_mask=m, sinks=s)
+    def rnd(*shape):
+        return (torch.randn(shape, generator=gen, device=dev) * 0.5).to(tdt)
+    q = rnd(case.B, case.Hq, case.Lq, case.d)
+    k = rnd(case.B, case.Hkv, case.Lk, case.d)
+    v = rnd(case.B, case.Hkv, case.Lk, case.dv)
+    s = rnd(case.Hq) if case.sinks else None
+    m = None
+    if case.mask == "bool":
+        m = (torch.rand((case.Lq, case.Lk), generator=gen, device=dev) < 0.9).to(torch.uint8)
+    if args.profile_case == "paged":
+        bs = 16
+        per = -(-case.Lk // bs)
+
+        def pages(t):
+            pad = torch.zeros((case.B, case.Hkv, per * bs, t.shape[3]), dtype=t.dtype, device=dev)
+            pad[:, :, :case.Lk] = t
+            return pad.view(case.B, case.Hkv, per, bs, t.shape[3]).permute(0, 2, 1, 3, 4).reshape(
+                case.B * per, case.Hkv, bs, t.shape[3]).contiguous()
+        kc, vc = pages(k), pages(v)
+        table = torch.arange(case.B * per, device=dev, dtype=torch.int32).view(case.B, per)
+        lens = torch.full((case.B,), case.Lk, dtype=torch.int32, device=dev)
+        for _ in range(args.steps):
+            nv.sdpa_paged(q, kc, vc, table, lens, mask_kind="causal", scale=case.scale_f32, sinks=s)
+    else:
+        for _ in range(args.steps):
+            nv.sdpa(q, k, v, mask_kind=case.mask, scale=case.scale_f32, bool_mask=m, sinks=s)
     torch.cuda.synchronize()
     st, detail = nv.nv_sdpa_device_status(0)
-    print(f"profile case {case.name}: {args.steps} calls, device status {st}")
+    print(f"profile case {case.name} ({args.profile_case}): {args.steps} calls, device status {st}")
     return 0 if st == 0 else 1
 
 
@@ -741,7 +817,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["prefill", "decode", "mask", "tiny"],
+    ap.add_argument("--profile-case", choices=["prefill", "decode", "mask", "tiny", "decode256", "f32", "paged"],
                     help="only launch this workload --steps times (for ncu); prints no JSON")
     args = ap.parse_args()
     if args.profile_case:
