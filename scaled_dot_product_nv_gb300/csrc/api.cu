@@ -286,7 +286,8 @@ int make_plan(const CallShape& cs, int mask_kind, int has_sinks, int dtype, nv_s
   if (!fits32 && dtype != NV_SDPA_F32) return NV_SDPA_ERR_UNSUPPORTED;
   if (pl->path == NV_SDPA_PATH_PREFILL && prefill_tc_supported(dtype, x.d, x.dv)) {
     // tcgen05 kernel: one CTA per 128 or 256 rows of one KV head, all keys (no split)
-    const PrefillGeom geo = prefill_tc_geometry(x.B, x.Hkv, g, x.Lq, x.d, x.dv, cs.qo_packed);
+    const PrefillGeom geo =
+        prefill_tc_geometry(x.B, x.Hkv, g, x.Lq, x.d, x.dv, cs.qo_packed, mask_kind == NV_SDPA_MASK_ADD);
     pl->kernel = NV_SDPA_KERNEL_PREFILL_TC;
     pl->rows_per_cta = 128 * geo.nq;
     pl->keys_per_blk = x.Lk;

@@ -50,7 +50,7 @@ struct PrefillGeom {
   int64_t n_it, n_rt, grid;
 };
 PrefillGeom prefill_tc_geometry(int64_t B, int64_t Hkv, int64_t g, int64_t Lq, int64_t d, int64_t dv,
-                                bool qo_packed);
+                                bool qo_packed, bool additive);
 cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, cudaStream_t st);
 
 // decode_mma.cu

@@ -70,6 +70,7 @@ struct TcArgs {
                      // (strided layouts); otherwise 3-D [B*Hkv][G][D] maps of packed rows
   int n_it;          // head_local: 128-position blocks per head
   int tma_out;       // the output tile fits the Q tile's shared memory: store it by TMA
+  int64_t amask_total;  // elements of the additive mask (loads never pass its end)
 };
 
 // barrier slots
@@ -144,20 +145,69 @@ __device__ __forceinline__ uint32_t col_bound(int c0, int lo, int hi) {
 // window), a bit-packed boolean mask, or an additive mask.
 enum { kMmBounds = 0, kMmBits = 1, kMmAdd = 2 };
 
+// Words of additive-mask values a softmax step holds: BN / 2 pairs (one word unused
+// otherwise).
+template <int BN, int MM>
+__host__ __device__ constexpr int av_words() { return MM == kMmAdd ? BN / 2 : 1; }
+
+// One row's additive-mask values of a key tile, av[w] = the tile's columns 2w and 2w + 1,
+// from the mask tensor `base` (T elements, `total` of them) where the tile's column 0 is
+// element `off`.  The row may start anywhere: the loads are 16-byte chunks from the
+// 8-element boundary at or below `off`, shifted down by the difference, so that a warp's
+// load touches each of its 32 rows' lines once per 8 columns.  Columns past the row are
+// whatever follows it (the caller masks them); nothing past the tensor is read.
+template <typename T, int BN>
+__device__ __forceinline__ void load_additive(const T* base, int64_t off, int64_t total, bool row_ok,
+                                              uint32_t (&av)[BN / 2]) {
+  constexpr int kChunks = BN / 8 + 1;
+  uint32_t w[4 * kChunks];
+  const int64_t a0 = off & ~int64_t(7);
+  const int m = (int)(off - a0);
+#pragma unroll
+  for (int c = 0; c < kChunks; ++c) {
+    const int64_t e = a0 + 8 * c;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (row_ok) {
+      if (e + 8 <= total) {
+        v = __ldg(reinterpret_cast<const uint4*>(base + e));
+      } else {
+        // the tensor's last chunk: element by element, nothing past its end
+        uint16_t h[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          h[k] = (e + k < total) ? __ldg(reinterpret_cast<const unsigned short*>(base + e + k)) : (uint16_t)0;
+        v = make_uint4(h[0] | (uint32_t)h[1] << 16, h[2] | (uint32_t)h[3] << 16, h[4] | (uint32_t)h[5] << 16,
+                       h[6] | (uint32_t)h[7] << 16);
+      }
+    }
+    w[4 * c] = v.x;
+    w[4 * c + 1] = v.y;
+    w[4 * c + 2] = v.z;
+    w[4 * c + 3] = v.w;
+  }
+  const int ws = m >> 1;
+  const bool odd = (m & 1) != 0;
+#pragma unroll
+  for (int i = 0; i < BN / 2; ++i) {
+    const uint32_t lo = ws == 0 ? w[i] : (ws == 1 ? w[i + 1] : (ws == 2 ? w[i + 2] : w[i + 3]));
+    const uint32_t hi = ws == 0 ? w[i + 1] : (ws == 1 ? w[i + 2] : (ws == 2 ? w[i + 3] : w[i + 4]));
+    av[i] = odd ? __funnelshift_r(lo, hi, 16) : lo;
+  }
+}
+
 // One query row's softmax step on its t-th key tile, key tile kt of the sequence.  tS /
 // tO: TMEM addresses (lane base included) of this tile's S columns and of O; the row
 // sees keys [first_key, last_key]; mrow: its mask row (MM = kMmBits: bit-packed words,
-// kMmAdd: the additive row in T), unused otherwise.  PF: the tile's words were loaded
-// ahead by the caller into mw.  Returns false if a wait gave up.
+// kMmAdd: unused; the tile's additive values are in av), unused otherwise.  PF: the tile's
+// words were loaded ahead by the caller into mw.  Returns false if a wait gave up.
 template <typename T, int BN, int MM, bool PF>
 __device__ __forceinline__ bool softmax_tile(const TcArgs& a, int t, int kt, uint32_t tS, uint32_t tO,
                                              bool row_ok, int first_key, int last_key, const void* mrow_any,
-                                             const uint32_t (&mw)[BN / 32], float& m_run, float& l_run,
-                                             uint32_t pv_bar, bool wait_pv, uint64_t limit,
-                                             volatile int* abort) {
+                                             const uint32_t (&mw)[BN / 32], const uint32_t (&av)[av_words<BN, MM>()],
+                                             float& m_run, float& l_run, uint32_t pv_bar, bool wait_pv,
+                                             uint64_t limit, volatile int* abort) {
   const Params& p = a.p;
   const uint32_t* mrow = static_cast<const uint32_t*>(mrow_any);
-  const T* arow = static_cast<const T*>(mrow_any);
   uint32_t sr[BN];
   if constexpr (BN == 128) tmem_ld128_sync(tS, sr);
   else tmem_ld64_sync(tS, sr);
@@ -224,19 +274,11 @@ __device__ __forceinline__ bool softmax_tile(const TcArgs& a, int t, int kt, uin
         const int col = c * 32 + e;
         float x0, x1;
         f2_unpack(f2_mul(f2_pack(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])), c2), x0, x1);
-        if (MM == kMmAdd && (vb & (3u << e))) {
-          // the additive term, in log2 units (a pair of 16-bit values where aligned)
-          float a0, a1;
-          if ((p.Lk & 1) == 0) {
-            const uint32_t w = __ldg(reinterpret_cast<const unsigned int*>(arow + j0 + col));
-            a0 = to_f32<T>(*reinterpret_cast<const T*>(&w));
-            a1 = to_f32<T>(*(reinterpret_cast<const T*>(&w) + 1));
-          } else {
-            a0 = (vb & (1u << e)) ? to_f32<T>(arow[j0 + col]) : 0.f;
-            a1 = (vb & (2u << e)) ? to_f32<T>(arow[j0 + col + 1]) : 0.f;
-          }
-          x0 = fmaf(a0, kLog2e, x0);
-          x1 = fmaf(a1, kLog2e, x1);
+        if constexpr (MM == kMmAdd) {
+          // the additive term, in log2 units (masked columns are replaced below)
+          const uint32_t wv = av[col >> 1];
+          x0 = fmaf(to_f32<T>(*reinterpret_cast<const T*>(&wv)), kLog2e, x0);
+          x1 = fmaf(to_f32<T>(*(reinterpret_cast<const T*>(&wv) + 1)), kLog2e, x1);
         }
         x0 = (vb & (1u << e)) ? x0 : -INFINITY;
         x1 = (vb & (2u << e)) ? x1 : -INFINITY;
@@ -732,9 +774,10 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
         // S of this tile was issued after P_{t-1} V_{t-1} of the same Q tile, and a commit
         // tracks every earlier MMA of the issuing thread, so s_full already implies that O
         // holds P_{t-1} V_{t-1}
+        uint32_t no_add[av_words<BN, MM>()];  // (additive masks take the one-tile variant)
         ok = softmax_tile<T, BN, MM, false>(a, t, kt0 + t, tmem + lane_base + tS_col(q), tO, row_ok, first_key,
-                                            last_key, mrow_any, no_words, m_run, l_run, bar(kBarPvDone + q), false,
-                                            limit, abort);
+                                            last_key, mrow_any, no_words, no_add, m_run, l_run, bar(kBarPvDone + q),
+                                            false, limit, abort);
         if (!ok) {
           fail(p, abort, kStatTimeoutMma);
           break;
@@ -752,10 +795,26 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
           dst[c] = (MM == kMmBits && row_ok) ? __ldg(mrow + ((kt0 + t) * BN) / 32 + c) : 0u;
       };
       if (n_tiles > 0) load_mw(0, mw);
+      // this row's additive-mask values of a key tile (kMmAdd)
+      uint32_t av[av_words<BN, MM>()];
+      auto load_av = [&](int t, uint32_t (&dst)[av_words<BN, MM>()]) {
+        if constexpr (MM == kMmAdd) {
+          const int64_t off = (int64_t)((const T*)mrow_any - reinterpret_cast<const T*>(p.amask)) +
+                              (int64_t)(kt0 + t) * BN;
+          load_additive<T, BN>(reinterpret_cast<const T*>(p.amask), off, a.amask_total, row_ok, dst);
+        }
+      };
+      if (n_tiles > 0) load_av(0, av);
       for (int t = 0; t < n_tiles; ++t) {
         uint32_t mw_next[BN / 32];
         if (t + 1 < n_tiles) load_mw(t + 1, mw_next);
         const int slot = t & 1;
+        // the next tile's additive values, loaded a tile ahead so that their latency falls
+        // in this tile's work
+        uint32_t av_next[av_words<BN, MM>()];
+        if constexpr (MM == kMmAdd) {
+          if (t + 1 < n_tiles) load_av(t + 1, av_next);
+        }
         ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull + slot), (t >> 1) & 1, limit, abort));
         if (!ok) {
           fail(p, abort, kStatTimeoutMma);
@@ -764,8 +823,8 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
         tc_fence_after();
         // S_t was issued before P_{t-1} V_{t-1}: the softmax waits for that product
         ok = softmax_tile<T, BN, MM, true>(a, t, kt0 + t, tmem + lane_base + tS_col(slot), tO, row_ok, first_key,
-                                           last_key, mrow_any, mw, m_run, l_run, bar(kBarPvDone + q), true, limit,
-                                           abort);
+                                           last_key, mrow_any, mw, av, m_run, l_run, bar(kBarPvDone + q), true,
+                                           limit, abort);
         if (!ok) {
           fail(p, abort, kStatTimeoutMma);
           break;
@@ -774,6 +833,10 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
         mbar_arrive(bar(kBarPFull + slot));
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) mw[c] = mw_next[c];
+        if constexpr (MM == kMmAdd) {
+#pragma unroll
+          for (int c = 0; c < av_words<BN, MM>(); ++c) av[c] = av_next[c];
+        }
       }
     }
     // ---- epilogue
@@ -907,11 +970,13 @@ size_t prefill_tc_mask_words(int64_t Lk) {
 }
 
 PrefillGeom prefill_tc_geometry(int64_t B, int64_t Hkv, int64_t g, int64_t Lq, int64_t d, int64_t dv,
-                                bool qo_packed) {
+                                bool qo_packed, bool additive) {
   PrefillGeom r{};
-  r.bn = prefill_tc_bn(d, dv);
+  // (an additive mask takes 64-key tiles: two tiles' values live in registers)
+  r.bn = additive ? 64 : prefill_tc_bn(d, dv);
   const int64_t G = g * Lq;
-  r.nq = prefill_tc_q_tiles(d, dv, G);
+  // (an additive mask is read into registers per tile: the one-tile variant has room)
+  r.nq = additive ? 1 : prefill_tc_q_tiles(d, dv, G);
   // strided q / out: Q tiles of one query head each (pairs of heads need an even group)
   if (!qo_packed && g % 2 != 0) r.nq = 1;
   r.qo5 = qo_packed ? 0 : 1;
@@ -929,9 +994,10 @@ cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, c
   TcArgs a;
   memset(&a, 0, sizeof(a));
   a.p = p;
-  const PrefillGeom geo = prefill_tc_geometry(p.B, p.Hkv, p.g, p.Lq, p.d, p.dv, p.qo_packed != 0);
+  const PrefillGeom geo =
+      prefill_tc_geometry(p.B, p.Hkv, p.g, p.Lq, p.d, p.dv, p.qo_packed != 0, p.mask_kind == kMaskAdd);
   const int bn = geo.bn, nq = geo.nq;
-  if (!bn) return cudaErrorInvalidValue;
+  if (!bn || !prefill_tc_bn(p.d, p.dv)) return cudaErrorInvalidValue;
   const int64_t BH = p.B * p.Hkv;
   // K and V as 4-D [B][Hkv][Lk][d] views with the caller's strides
   const int64_t kd[4] = {p.d, p.Lk, p.Hkv, p.B}, ks[3] = {p.k_sl, p.k_sh, p.k_sb};
@@ -959,6 +1025,8 @@ cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, c
   a.n_pv = (int)((p.dv + 15) / 16 * 16);
   a.itile_order = (p.Lq % (kBM * nq) == 0) ? 1 : 0;
   a.head_local = geo.head_local;
+  if (p.mask_kind == kMaskAdd)
+    a.amask_total = (p.am_sb ? p.B * p.am_sb : (p.am_sh ? p.Hq * p.am_sh : p.Lq * p.Lk));
   if (p.mask_kind == kMaskBool) {
     a.mask_words = (int64_t)prefill_tc_mask_words(p.Lk);
     a.mask_bits = mask_bits;
