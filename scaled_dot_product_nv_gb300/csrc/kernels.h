@@ -40,13 +40,13 @@ cudaError_t launch_fill_no_keys(int dtype, const Params& p, cudaStream_t st);
 bool prefill_tc_supported(int dtype, int64_t d, int64_t dv);
 int prefill_tc_bn(int64_t d, int64_t dv);
 int prefill_tc_q_tiles(int64_t d, int64_t dv, int64_t G);
-size_t prefill_tc_smem_bytes(int64_t d, int64_t dv, int bn, int nq);
+size_t prefill_tc_smem_bytes(int64_t d, int64_t dv, int bn, int nq, int stg);
 int64_t prefill_tc_rows_per_cta(int64_t d, int64_t dv, int64_t G);
 size_t prefill_tc_mask_words(int64_t Lk);
-// How a tensor-core prefill call is tiled: key tile, Q tiles per CTA, packed rows or
-// head-local tiles (strided q / out go through 5-D maps), and the grid.
+// How a tensor-core prefill call is tiled: key tile, Q tiles per CTA, K / V ring depth,
+// packed rows or head-local tiles (strided q / out go through 5-D maps), and the grid.
 struct PrefillGeom {
-  int bn, nq, head_local, qo5;
+  int bn, nq, stg, head_local, qo5;
   int64_t n_it, n_rt, grid;
 };
 PrefillGeom prefill_tc_geometry(int64_t B, int64_t Hkv, int64_t g, int64_t Lq, int64_t d, int64_t dv,

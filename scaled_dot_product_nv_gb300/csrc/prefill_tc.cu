@@ -430,10 +430,11 @@ __device__ __forceinline__ void epilogue_row_smem(const Params& p, uint32_t tO, 
 template <int NQ>
 constexpr int tc_threads() { return (2 + 4 * NQ) * 32; }
 
-template <typename T, int BN, int NQ, int MM>
+template <typename T, int BN, int NQ, int MM, int STG>
 __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __grid_constant__ TcArgs a) {
   static_assert(NQ == 1 || NQ == 2, "one or two Q tiles per CTA");
   static_assert(NQ == 1 || BN == 128, "the two-tile variant uses 128-key tiles");
+  static_assert(STG >= 1 && STG <= kStages && (NQ == 1 || STG == 2), "ring depth");
   constexpr int kMaxKsteps = (NQ == 2) ? 8 : 16;  // d <= 128 for two tiles, <= 256 otherwise
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -445,8 +446,8 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
   const uint32_t v_bytes = a.dvpanels * BN * 128;
   const uint32_t sQ = smem_addr(base);
   const uint32_t sK = sQ + NQ * q_bytes;
-  const uint32_t sV = sK + kStages * k_bytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + NQ * q_bytes + kStages * (k_bytes + v_bytes));
+  const uint32_t sV = sK + STG * k_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + NQ * q_bytes + STG * (k_bytes + v_bytes));
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_holder + 1);
   auto bar = [&](int i) { return smem_addr(bars + i); };
@@ -510,7 +511,7 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
   // ---- set-up: barriers, TMEM
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQ), 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < STG; ++s) {
       mbar_init(bar(kBarKvFull + s), 1);
       mbar_init(bar(kBarKvEmpty + s), 1);
       mbar_init(bar(kBarVFull + s), 1);
@@ -563,8 +564,8 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
       // one ring slot: wait until its previous tile is released, then load tile t into it
       auto load = [&](int full, int empty, uint32_t ring, uint32_t bytes, const CUtensorMap* tm1, int panels1,
                       uint32_t ring2, const CUtensorMap* tm2, int panels2, int t) {
-        const int s = t % kStages;
-        if (!mbar_wait(bar(empty + s), ((t / kStages) & 1) ^ 1, limit, abort)) {
+        const int s = t % STG;
+        if (!mbar_wait(bar(empty + s), ((t / STG) & 1) ^ 1, limit, abort)) {
           fail(p, abort, kStatTimeoutSlotFree);
           return false;
         }
@@ -579,10 +580,10 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
       };
       int k_issued = 0, v_issued = 0;
       if constexpr (NQ == 2) {
-        // K and V of tile t together into stage t % kStages
+        // K and V of tile t together into stage t % STG
         for (int t = 0; t < n_max; ++t) {
-          const int s = t % kStages;
-          if (!mbar_wait(bar(kBarKvEmpty + s), ((t / kStages) & 1) ^ 1, limit, abort)) {
+          const int s = t % STG;
+          if (!mbar_wait(bar(kBarKvEmpty + s), ((t / STG) & 1) ^ 1, limit, abort)) {
             fail(p, abort, kStatTimeoutSlotFree);
             break;
           }
@@ -611,11 +612,11 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
       }
       // Every copy issued must land before the CTA may exit (a no-op when all were consumed).
       mbar_wait(bar(kBarQ), 0, kDrainLimit, nullptr);
-      for (int t = k_issued > kStages ? k_issued - kStages : 0; t < k_issued; ++t)
-        mbar_wait(bar(kBarKvFull + t % kStages), (t / kStages) & 1, kDrainLimit, nullptr);
+      for (int t = k_issued > STG ? k_issued - STG : 0; t < k_issued; ++t)
+        mbar_wait(bar(kBarKvFull + t % STG), (t / STG) & 1, kDrainLimit, nullptr);
       if constexpr (NQ == 1)
-        for (int t = v_issued > kStages ? v_issued - kStages : 0; t < v_issued; ++t)
-          mbar_wait(bar(kBarVFull + t % kStages), (t / kStages) & 1, kDrainLimit, nullptr);
+        for (int t = v_issued > STG ? v_issued - STG : 0; t < v_issued; ++t)
+          mbar_wait(bar(kBarVFull + t % STG), (t / STG) & 1, kDrainLimit, nullptr);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -634,7 +635,7 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
       auto issue_s = [&](int t, int q, int slot) {
         const uint32_t dst = tmem + tS_col(slot);
         const uint64_t ad = qd0 + (uint64_t)(q * (q_bytes >> 4));
-        const uint64_t bd = kd0 + (uint64_t)((t % kStages) * (k_bytes >> 4));
+        const uint64_t bd = kd0 + (uint64_t)((t % STG) * (k_bytes >> 4));
         if (a.ksteps_qk == kMaxKsteps) {
           // the head fills this variant: straight-line issue, no branch between MMAs (the
           // single issuing thread must keep pace with 64-cycle 128x128x16 MMAs)
@@ -652,7 +653,7 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
       // O_q += P (from S slot `slot`) V_t, then commit to pv_done[q]
       auto issue_pv = [&](int t, int q, int slot) {
         const uint32_t dst = tmem + tO_col(q), src = tmem + tS_col(slot);
-        const uint64_t bd = vd0 + (uint64_t)((t % kStages) * (v_bytes >> 4));
+        const uint64_t bd = vd0 + (uint64_t)((t % STG) * (v_bytes >> 4));
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           mma_ts(dst, src + kk * 8, bd + (uint64_t)(kk * 128), idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
@@ -660,7 +661,7 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
       };
       // (the issuer's waits never suspend: see mbar_wait)
       auto wait_kv = [&](int t) {
-        if (mbar_wait<false>(bar(kBarKvFull + t % kStages), (t / kStages) & 1, limit, abort)) {
+        if (mbar_wait<false>(bar(kBarKvFull + t % STG), (t / STG) & 1, limit, abort)) {
           tc_fence_after();
           return true;
         }
@@ -681,7 +682,7 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
       if constexpr (NQ == 1) {
         // K slots are released once their S is done, V slots once their P V is
         auto wait_v = [&](int t) {
-          if (mbar_wait<false>(bar(kBarVFull + t % kStages), (t / kStages) & 1, limit, abort)) {
+          if (mbar_wait<false>(bar(kBarVFull + t % STG), (t / STG) & 1, limit, abort)) {
             tc_fence_after();
             return true;
           }
@@ -696,12 +697,12 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
           if (t + 1 < n_max) {
             if (!(ok = wait_kv(t + 1))) break;
             issue_s(t + 1, 0, (t + 1) & 1);
-            mma_commit(bar(kBarKvEmpty + (t + 1) % kStages));
+            mma_commit(bar(kBarKvEmpty + (t + 1) % STG));
           }
           if (!(ok = wait_p(t & 1, (t >> 1) & 1))) break;
           if (!(ok = wait_v(t))) break;
           issue_pv(t, 0, t & 1);
-          mma_commit(bar(kBarVEmpty + t % kStages));
+          mma_commit(bar(kBarVEmpty + t % STG));
         }
       } else {
         if (ok) {
@@ -720,7 +721,7 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
             if (!(ok = wait_p(1, t & 1))) break;
             issue_pv(t, 1, 1);
           }
-          mma_commit(bar(kBarKvEmpty + t % kStages));
+          mma_commit(bar(kBarKvEmpty + t % STG));
           if (nxt && t + 1 < n_q[1]) issue_s(t + 1, 1, 1);
         }
       }
@@ -735,16 +736,18 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
     const int q4 = warp & 3;       // TMEM lane quarter this warp may access
     const int row = q4 * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-    const int qi = q == 0 ? 0 : NQ - 1;
+    // (selects, not an index: the arrays stay in registers)
+    const int i0_q = q == 0 ? i0[0] : i0[NQ - 1], row0_q = q == 0 ? row0[0] : row0[NQ - 1];
+    const int hhq_q = q == 0 ? hhq[0] : hhq[NQ - 1];
     bool row_ok;
     int i, hh;
     if (a.head_local) {
-      i = i0[qi] + row;
+      i = i0_q + row;
       row_ok = i < p.Lq;
-      hh = hhq[qi];
+      hh = hhq_q;
       if (!row_ok) i = 0;
     } else {
-      const int rho = row0[qi] + row;
+      const int rho = row0_q + row;
       row_ok = rho < p.G;
       i = row_ok ? rho % (int)p.Lq : 0;
       hh = row_ok ? rho / (int)p.Lq : 0;
@@ -758,7 +761,7 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
     const void* mrow_any = mrow;
     if constexpr (MM == kMmAdd)
       mrow_any = reinterpret_cast<const T*>(p.amask) + bb * p.am_sb + h * p.am_sh + (int64_t)i * p.Lk;
-    const int n_tiles = n_q[q];
+    const int n_tiles = q == 0 ? n_q[0] : n_q[NQ - 1];
     const uint32_t tO = tmem + lane_base + tO_col(q);
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
@@ -860,10 +863,9 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
       if (all_ok && warp == 2 + 4 * q && lane == 0) {
         for (int pn = 0; pn < a.dvpanels; ++pn) {
           if (a.qo5)
-            tma_store_5d(&a.tmo, smem_addr(stage + pn * (kBM * 128)), pn * 64, (int)i0[qi], hhq[qi], (int)hkv,
-                         (int)bb);
+            tma_store_5d(&a.tmo, smem_addr(stage + pn * (kBM * 128)), pn * 64, i0_q, hhq_q, (int)hkv, (int)bb);
           else
-            tma_store_3d(&a.tmo, smem_addr(stage + pn * (kBM * 128)), pn * 64, (int)row0[qi], (int)bh);
+            tma_store_3d(&a.tmo, smem_addr(stage + pn * (kBM * 128)), pn * 64, row0_q, (int)bh);
         }
         bulk_commit_group();
         bulk_wait_read_all();  // the stage must stay intact until the copy has read it
@@ -902,57 +904,71 @@ __global__ void sdpa_pack_mask_bits(const uint8_t* __restrict__ mask, int64_t Lq
 
 // ------------------------------------------------------------------------- host side
 
-template <typename T, int BN, int NQ, int MM>
+template <typename T, int BN, int NQ, int MM, int STG>
 cudaError_t launch_tc_t(const TcArgs& a, size_t smem, int64_t grid, cudaStream_t st) {
   static std::atomic<unsigned long long> configured{0};
   cudaError_t e =
-      set_max_dynamic_smem_once(configured, (const void*)sdpa_prefill_tc<T, BN, NQ, MM>, (int)kTcMaxSmem);
+      set_max_dynamic_smem_once(configured, (const void*)sdpa_prefill_tc<T, BN, NQ, MM, STG>, (int)kTcMaxSmem);
   if (e != cudaSuccess) return e;
-  sdpa_prefill_tc<T, BN, NQ, MM><<<(unsigned)grid, tc_threads<NQ>(), smem, st>>>(a);
+  sdpa_prefill_tc<T, BN, NQ, MM, STG><<<(unsigned)grid, tc_threads<NQ>(), smem, st>>>(a);
   return cudaGetLastError();
 }
 
 template <typename T, int MM>
-cudaError_t launch_tc_mm(int bn, int nq, const TcArgs& a, size_t smem, int64_t grid, cudaStream_t st) {
-  if (nq == 2) return launch_tc_t<T, 128, 2, MM>(a, smem, grid, st);
-  return bn == 128 ? launch_tc_t<T, 128, 1, MM>(a, smem, grid, st) : launch_tc_t<T, 64, 1, MM>(a, smem, grid, st);
+cudaError_t launch_tc_mm(int bn, int nq, int stg, const TcArgs& a, size_t smem, int64_t grid, cudaStream_t st) {
+  if (nq == 2) return stg == 2 ? launch_tc_t<T, 128, 2, MM, 2>(a, smem, grid, st) : cudaErrorInvalidValue;
+  if constexpr (MM == kMmAdd) {
+    // (additive masks always take 64-key tiles and two stages)
+    if (bn != 64 || stg != 2) return cudaErrorInvalidValue;
+    return launch_tc_t<T, 64, 1, MM, 2>(a, smem, grid, st);
+  } else {
+    if (bn == 64) return stg == 2 ? launch_tc_t<T, 64, 1, MM, 2>(a, smem, grid, st) : cudaErrorInvalidValue;
+    return stg == 2 ? launch_tc_t<T, 128, 1, MM, 2>(a, smem, grid, st) : launch_tc_t<T, 128, 1, MM, 1>(a, smem, grid, st);
+  }
 }
 
 template <typename T>
-cudaError_t launch_tc_cfg(int bn, int nq, const TcArgs& a, size_t smem, int64_t grid, cudaStream_t st) {
-  if (a.p.mask_kind == kMaskBool) return launch_tc_mm<T, kMmBits>(bn, nq, a, smem, grid, st);
-  if (a.p.mask_kind == kMaskAdd) return launch_tc_mm<T, kMmAdd>(bn, nq, a, smem, grid, st);
-  return launch_tc_mm<T, kMmBounds>(bn, nq, a, smem, grid, st);
+cudaError_t launch_tc_cfg(int bn, int nq, int stg, const TcArgs& a, size_t smem, int64_t grid, cudaStream_t st) {
+  if (a.p.mask_kind == kMaskBool) return launch_tc_mm<T, kMmBits>(bn, nq, stg, a, smem, grid, st);
+  if (a.p.mask_kind == kMaskAdd) return launch_tc_mm<T, kMmAdd>(bn, nq, stg, a, smem, grid, st);
+  return launch_tc_mm<T, kMmBounds>(bn, nq, stg, a, smem, grid, st);
 }
 
-size_t smem_need(int64_t d, int64_t dv, int bn, int nq) {
+size_t smem_need(int64_t d, int64_t dv, int bn, int nq, int stg) {
   const int64_t dp = (d + 63) / 64, dvp = (dv + 63) / 64;
-  return (size_t)(nq * dp * kBM * 128 + kStages * (dp + dvp) * bn * 128) + 1024 /*align*/ + 256 /*bars*/;
+  return (size_t)(nq * dp * kBM * 128 + stg * (dp + dvp) * bn * 128) + 1024 /*align*/ + 256 /*bars*/;
+}
+
+// The key tile and the depth of the K / V rings of the one-tile variant: the largest
+// tile whose two S buffers and O fit the 512 TMEM columns, with two stages if they fit in
+// shared memory, else one (each ring then refills while the other operand's product runs;
+// 128-key tiles keep the S products at the full MMA rate, where 64-key ones run at 2/3).
+struct TileChoice {
+  int bn, stg;
+};
+TileChoice tile_choice(int64_t d, int64_t dv) {
+  const int64_t npv = (dv + 15) / 16 * 16;
+  for (int bn : {128, 64})
+    for (int stg : {2, 1})
+      if ((int64_t)smem_need(d, dv, bn, 1, stg) <= kTcMaxSmem && 2 * bn + npv <= kTmemCols) return {bn, stg};
+  return {0, 0};
 }
 
 }  // namespace
 
-int prefill_tc_bn(int64_t d, int64_t dv) {
-  // largest key tile whose 2-stage K/V ring plus one Q tile fit in shared memory and
-  // whose two S buffers plus O fit in the 512 TMEM columns
-  const int64_t npv = (dv + 15) / 16 * 16;
-  for (int bn : {128, 64}) {
-    if ((int64_t)smem_need(d, dv, bn, 1) <= kTcMaxSmem && 2 * bn + npv <= kTmemCols) return bn;
-  }
-  return 0;
-}
+int prefill_tc_bn(int64_t d, int64_t dv) { return tile_choice(d, dv).bn; }
 
 int prefill_tc_q_tiles(int64_t d, int64_t dv, int64_t G) {
   // two Q tiles share each K/V tile when both O accumulators fit next to the two S
   // tiles (dv <= 128), both Q tiles and the ring fit in shared memory, and there are
   // more than 128 rows to fill them
-  if (dv <= 128 && prefill_tc_bn(d, dv) == 128 && (int64_t)smem_need(d, dv, 128, 2) <= kTcMaxSmem && G > kBM)
+  if (dv <= 128 && prefill_tc_bn(d, dv) == 128 && (int64_t)smem_need(d, dv, 128, 2, 2) <= kTcMaxSmem && G > kBM)
     return 2;
   return 1;
 }
 
-size_t prefill_tc_smem_bytes(int64_t d, int64_t dv, int bn, int nq) {
-  const size_t s = smem_need(d, dv, bn, nq);
+size_t prefill_tc_smem_bytes(int64_t d, int64_t dv, int bn, int nq, int stg) {
+  const size_t s = smem_need(d, dv, bn, nq, stg);
   // at least 120 KB so that one CTA (with its 512 TMEM columns) owns the SM
   return s < 120 * 1024 ? 120 * 1024 : s;
 }
@@ -973,10 +989,12 @@ PrefillGeom prefill_tc_geometry(int64_t B, int64_t Hkv, int64_t g, int64_t Lq, i
                                 bool qo_packed, bool additive) {
   PrefillGeom r{};
   // (an additive mask takes 64-key tiles: two tiles' values live in registers)
-  r.bn = additive ? 64 : prefill_tc_bn(d, dv);
+  const TileChoice tc = tile_choice(d, dv);
+  r.bn = additive ? 64 : tc.bn;
   const int64_t G = g * Lq;
   // (an additive mask is read into registers per tile: the one-tile variant has room)
   r.nq = additive ? 1 : prefill_tc_q_tiles(d, dv, G);
+  r.stg = (r.nq == 2 || r.bn == 64) ? 2 : tc.stg;
   // strided q / out: Q tiles of one query head each (pairs of heads need an even group)
   if (!qo_packed && g % 2 != 0) r.nq = 1;
   r.qo5 = qo_packed ? 0 : 1;
@@ -996,8 +1014,9 @@ cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, c
   a.p = p;
   const PrefillGeom geo =
       prefill_tc_geometry(p.B, p.Hkv, p.g, p.Lq, p.d, p.dv, p.qo_packed != 0, p.mask_kind == kMaskAdd);
-  const int bn = geo.bn, nq = geo.nq;
-  if (!bn || !prefill_tc_bn(p.d, p.dv)) return cudaErrorInvalidValue;
+  const int bn = geo.bn, nq = geo.nq, stg = geo.stg;
+  if (!bn || !prefill_tc_bn(p.d, p.dv) || (int64_t)smem_need(p.d, p.dv, bn, nq, stg) > kTcMaxSmem)
+    return cudaErrorInvalidValue;
   const int64_t BH = p.B * p.Hkv;
   // K and V as 4-D [B][Hkv][Lk][d] views with the caller's strides
   const int64_t kd[4] = {p.d, p.Lk, p.Hkv, p.B}, ks[3] = {p.k_sl, p.k_sh, p.k_sb};
@@ -1039,9 +1058,9 @@ cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, c
     if (e != cudaSuccess) return e;
   }
   const int64_t grid = geo.grid;
-  const size_t smem = prefill_tc_smem_bytes(p.d, p.dv, bn, nq);
-  if (dtype == 1) return launch_tc_cfg<__half>(bn, nq, a, smem, grid, st);
-  return launch_tc_cfg<__nv_bfloat16>(bn, nq, a, smem, grid, st);
+  const size_t smem = prefill_tc_smem_bytes(p.d, p.dv, bn, nq, stg);
+  if (dtype == 1) return launch_tc_cfg<__half>(bn, nq, stg, a, smem, grid, st);
+  return launch_tc_cfg<__nv_bfloat16>(bn, nq, stg, a, smem, grid, st);
 }
 
 }  // namespace nvsdpa
