@@ -452,7 +452,7 @@ def feature_lines(torch, nv, dev, stream, pk, pc, px, dc, dx, mc, mx, args):
                                    want_lse=False))
         _, pl1 = nv.nv_sdpa_plan((c1.B, c1.Hq, c1.Hkv, c1.Lq, c1.Lk, c1.d, c1.dv), 1, 1, W.DTYPE_CODES[c1.dtype])
         out[name] = hbm_line(f"decode_f16_b{c1.B}_h32x4_lq{c1.Lq}_lk32769_d128_sinks", kv_bytes(c1), ms,
-                             {"nblk": pl1["nblk"], "keys_per_blk": pl1["keys_per_blk"]})
+                             {"nblk": pl1["nblk"], "keys_per_blk": pl1["keys_per_blk"], "kernel": pl1["kernel"]})
         del q1, k1, v1, o1
     # decode: a window of 4096 over the 32769 keys, and the keys in a paged cache
     dq, dk, dv_ = (up(dx[n], dc.dtype) for n in ("q", "k", "v"))
@@ -770,7 +770,9 @@ def run_profile_case(args):
              # f32 decode on the FP32-FMA kernel, split over key blocks
              "f32": W.Case(8, 32, 4, 1, 8193, 128, 128, "f32", "causal", True, None, "u2", seed=8,
                            name="decode_f32_b8_h32x4_lk8193_d128_sinks"),
-             "paged": W.decode_f16_long_kv()}
+             "paged": W.decode_f16_long_kv(),
+             # eight queries per sequence: 64 rows per KV head, the split tcgen05 kernel
+             "decode_lq8": W.decode_f16_long_kv().with_(Lq=8, name="decode_f16_b8_h32x4_lq8_lk32769_d128_sinks")}
     case = cases[args.profile_case]
     dev = torch.device("cuda", 0)
     gen = torch.Generator(device=dev)
@@ -817,7 +819,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["prefill", "decode", "mask", "tiny", "decode256", "f32", "paged"],
+    ap.add_argument("--profile-case", choices=["prefill", "decode", "mask", "tiny", "decode256", "f32", "paged",
+                                               "decode_lq8"],
                     help="only launch this workload --steps times (for ncu); prints no JSON")
     args = ap.parse_args()
     if args.profile_case:

@@ -88,7 +88,9 @@ typedef enum {
   NV_SDPA_KERNEL_FILL = 1,          /* Lk == 0 rows                                     */
   NV_SDPA_KERNEL_PREFILL_TC = 2,    /* tcgen05 + TMEM + TMA prefill, f16/bf16           */
   NV_SDPA_KERNEL_TILED_SIMT = 3,    /* FP32-FMA tiled online softmax (f32; any path)    */
-  NV_SDPA_KERNEL_DECODE_MMA = 4     /* TMA-staged tensor-core decode pass 1, f16/bf16   */
+  NV_SDPA_KERNEL_DECODE_MMA = 4,    /* TMA-staged tensor-core decode pass 1, f16/bf16   */
+  NV_SDPA_KERNEL_DECODE_TC = 5      /* decode with g*Lq > 16 rows per KV head: the      */
+                                    /* tcgen05 prefill kernel split over key blocks     */
 } nv_sdpa_kernel;
 
 /* What nv_sdpa() will launch for a problem.  Pure for a given device: a function of its

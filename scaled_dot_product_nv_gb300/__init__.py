@@ -27,7 +27,7 @@ OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_TIMEOUT = 0, 1, 2, 3, 4
 DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
 MASKS = {"none": 0, "causal": 1, "bool": 2, "add": 3}
 PATHS = {0: "noop", 1: "no_keys", 2: "prefill", 3: "decode"}
-KERNELS = {0: "none", 1: "fill", 2: "prefill_tc", 3: "tiled_simt", 4: "decode_mma"}
+KERNELS = {0: "none", 1: "fill", 2: "prefill_tc", 3: "tiled_simt", 4: "decode_mma", 5: "decode_tc"}
 
 
 class Dims(ctypes.Structure):

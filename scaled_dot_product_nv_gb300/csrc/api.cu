@@ -162,7 +162,9 @@ int resolve_options(const nv_sdpa_dims& x, int mask_kind, int dtype, const nv_sd
     // "nuvec-core 0.5.0 tests/fast.rs", window_errors_empty_inputs_and_full_windows: a window
     // of 0, or a window without the causal mask, is an error
     if (o.window < 1 || mask_kind != NV_SDPA_MASK_CAUSAL) return NV_SDPA_ERR_INVALID;
-    r->window = o.window;
+    // a window of at least Lk keys hides no key from any row (the last row's position is
+    // Lk - 1): it is the causal call, and runs as one, bit for bit
+    r->window = o.window >= x.Lk ? 0 : o.window;
   } else if (o.window != 0) {
     return NV_SDPA_ERR_INVALID;
   }
@@ -195,10 +197,11 @@ struct CallShape {
   int64_t span;     // keys one row tile's blocks cover: Lk, or the window's reach
   bool qo_packed;   // q and out contiguous
   bool paged;
+  bool window;      // a causal sliding window is set
 };
 
 CallShape call_shape(const nv_sdpa_dims& x, const Resolved& r) {
-  CallShape c{x, x.Lk, r.qo_packed, false};
+  CallShape c{x, x.Lk, r.qo_packed, false, r.window > 0};
   // rows of one tile are at most Lq positions apart: their bands together cover at most
   // window + Lq - 1 keys
   if (r.window > 0 && r.window < x.Lk) c.span = std::min<int64_t>(x.Lk, r.window + std::max<int64_t>(x.Lq, 1) - 1);
@@ -287,7 +290,7 @@ int make_plan(const CallShape& cs, int mask_kind, int has_sinks, int dtype, nv_s
   if (pl->path == NV_SDPA_PATH_PREFILL && prefill_tc_supported(dtype, x.d, x.dv)) {
     // tcgen05 kernel: one CTA per 128 or 256 rows of one KV head, all keys (no split)
     const PrefillGeom geo =
-        prefill_tc_geometry(x.B, x.Hkv, g, x.Lq, x.d, x.dv, cs.qo_packed, mask_kind == NV_SDPA_MASK_ADD);
+        prefill_tc_geometry(x.B, x.Hkv, g, x.Lq, x.d, x.dv, cs.qo_packed, mask_kind == NV_SDPA_MASK_ADD, 0);
     pl->kernel = NV_SDPA_KERNEL_PREFILL_TC;
     pl->rows_per_cta = 128 * geo.nq;
     pl->keys_per_blk = x.Lk;
@@ -297,6 +300,40 @@ int make_plan(const CallShape& cs, int mask_kind, int has_sinks, int dtype, nv_s
     if (mask_kind == NV_SDPA_MASK_BOOL) {  // bit-packed copy of the mask
       pl->launches = 2;
       pl->scratch_bytes = x.Lq * (int64_t)prefill_tc_mask_words(x.Lk) * 4;
+    }
+    return NV_SDPA_OK;
+  }
+  if (pl->path == NV_SDPA_PATH_DECODE && G > decode_mma_rows_per_warp() && cs.qo_packed && !cs.paged &&
+      !cs.window && (mask_kind == NV_SDPA_MASK_NONE || mask_kind == NV_SDPA_MASK_CAUSAL) &&
+      prefill_tc_supported(dtype, x.d, x.dv)) {
+    // More query rows per KV head than one mma.sync row tile (g x Lq > 16): the tcgen05
+    // prefill kernel, split over key blocks, reads each KV head's keys once for up to 128
+    // rows (the mma.sync decode kernel would stream them once per 16 rows, and its
+    // products, not HBM, would bound it).  Blocks of whole 128-key tiles, cut from key 0,
+    // sized from the keys and the head count alone (never B): as many as fill the CTA
+    // slots (two per SM for heads up to 128) once for an 8-sequence batch, at least 8
+    // tiles each.  (Measured, 8 x 32/4 heads x 8 queries x 32769 keys, f16: 9 blocks
+    // 4846 GB/s, 19 blocks 4435, 33 blocks 3890.)
+    pl->kernel = NV_SDPA_KERNEL_DECODE_TC;
+    pl->rows_per_cta = 128;
+    const int64_t n_rt = cdiv(G, 128), tiles = cdiv(x.Lk, 128);
+    const int64_t slots = (x.d <= 128 && x.dv <= 128 ? 2 : 1) * (int64_t)device_sm_count();
+    const int64_t target = std::max<int64_t>(1, slots / (8 * x.Hkv * n_rt));
+    int64_t blk_tiles = std::max<int64_t>(8, cdiv(tiles, target));
+    if (const int64_t forced = decode_blocks_override())
+      blk_tiles = cdiv(tiles, std::max<int64_t>(1, std::min(forced, tiles)));
+    blk_tiles = std::max<int64_t>(blk_tiles, cdiv(tiles, merge_max_blocks()));
+    pl->keys_per_blk = blk_tiles * 128;
+    pl->nblk = cdiv(tiles, blk_tiles);
+    int64_t grid;
+    if (!mul_ok(x.B * x.Hkv, n_rt, &grid) || !mul_ok(grid, pl->nblk, &grid) || grid > 0x7fffffff)
+      return NV_SDPA_ERR_UNSUPPORTED;
+    pl->grid = grid;
+    pl->launches = pl->nblk > 1 ? 2 : 1;
+    if (pl->nblk > 1) {
+      const int64_t rows = x.B * x.Hq * x.Lq;
+      if (rows > 0x7fffffff) return NV_SDPA_ERR_UNSUPPORTED;  // the merge grid: one CTA per row
+      pl->scratch_bytes = cdiv(rows * pl->nblk * x.dv * 4, 256) * 256 + rows * pl->nblk * 2 * 4;
     }
     return NV_SDPA_OK;
   }
@@ -500,8 +537,11 @@ cudaError_t launch_plan(int dtype, const nv_sdpa_plan_t& pl, Params& p, void* sc
     p.part_o = static_cast<float*>(scratch);
     p.part_ml = reinterpret_cast<float*>(static_cast<char*>(scratch) + o_bytes);
   }
-  if (pl.kernel == NV_SDPA_KERNEL_PREFILL_TC) return launch_prefill_tc(dtype, p, static_cast<uint32_t*>(scratch), cs);
-  if (pl.kernel == NV_SDPA_KERNEL_DECODE_MMA) {
+  if (pl.kernel == NV_SDPA_KERNEL_PREFILL_TC)
+    return launch_prefill_tc(dtype, p, static_cast<uint32_t*>(scratch), false, cs);
+  if (pl.kernel == NV_SDPA_KERNEL_DECODE_TC) {
+    ce = launch_prefill_tc(dtype, p, nullptr, true, cs);
+  } else if (pl.kernel == NV_SDPA_KERNEL_DECODE_MMA) {
     ce = launch_decode_mma(dtype, p, cs);
   } else {
     ce = launch_tiled_simt(dtype, p, cs);

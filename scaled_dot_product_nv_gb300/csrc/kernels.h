@@ -45,13 +45,17 @@ int64_t prefill_tc_rows_per_cta(int64_t d, int64_t dv, int64_t G);
 size_t prefill_tc_mask_words(int64_t Lk);
 // How a tensor-core prefill call is tiled: key tile, Q tiles per CTA, K / V ring depth,
 // packed rows or head-local tiles (strided q / out go through 5-D maps), and the grid.
+// With nblk > 0, the split-KV form (decode-sized row groups): one Q tile of packed rows
+// per CTA and key block.
 struct PrefillGeom {
-  int bn, nq, stg, head_local, qo5;
+  int bn, nq, stg, head_local, qo5, split, tmem_cols;
   int64_t n_it, n_rt, grid;
 };
 PrefillGeom prefill_tc_geometry(int64_t B, int64_t Hkv, int64_t g, int64_t Lq, int64_t d, int64_t dv,
-                                bool qo_packed, bool additive);
-cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, cudaStream_t st);
+                                bool qo_packed, bool additive, int64_t nblk);
+// split: the split-KV form over p.nblk blocks of p.keys_per_blk keys (partials to
+// p.part_o / p.part_ml when nblk > 1; the merge pass is the caller's)
+cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, bool split, cudaStream_t st);
 
 // decode_mma.cu
 bool decode_mma_supported(int dtype, int64_t d, int64_t dv);

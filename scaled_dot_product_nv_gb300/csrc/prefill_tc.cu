@@ -30,11 +30,14 @@
 //     tensor pipe works for the other (ping-pong), with two warps per scheduler.
 // * Causal: key tiles wholly above the (bottom-right aligned) diagonal are never loaded,
 //   and a warp takes the unmasked fast path on every tile it sees completely.  Boolean
-//   masks arrive as a bit-packed copy made by sdpa_pack_mask_bits.
+//   masks arrive as a bit-packed copy made by sdpa_pack_mask_bits, which this kernel
+//   overlaps as its programmatic dependent.
 // * Every mbarrier wait is bounded; a wait that runs out records a status bit, raises
 //   a shared abort flag that the other roles also watch, and the CTA drains its
 //   in-flight copies and MMAs before freeing TMEM and exiting.
 #include <cuda.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -46,7 +49,7 @@ namespace {
 using namespace sm100;
 
 constexpr int kBM = 128;
-constexpr int kStages = 2;
+constexpr int kStages = 2;  // the deepest K / V ring (barrier slots)
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr uint64_t kDrainLimit = 1ull << 18;  // polls of <= ~10 us each
@@ -71,6 +74,10 @@ struct TcArgs {
   int n_it;          // head_local: 128-position blocks per head
   int tma_out;       // the output tile fits the Q tile's shared memory: store it by TMA
   int64_t amask_total;  // elements of the additive mask (loads never pass its end)
+  int split;         // NQ = 1, packed rows: CTA x is key block x % nblk of its row block, and
+                     // (nblk > 1) its rows' partials go to part_o / part_ml for the merge
+  int blk_tiles;     // split: key tiles per block (keys_per_blk / BN)
+  int tmem_cols;     // TMEM columns allocated: 512, or 256 where two CTAs share the SM
 };
 
 // barrier slots
@@ -200,7 +207,7 @@ __device__ __forceinline__ void load_additive(const T* base, int64_t off, int64_
 // sees keys [first_key, last_key]; mrow: its mask row (MM = kMmBits: bit-packed words,
 // kMmAdd: unused; the tile's additive values are in av), unused otherwise.  PF: the tile's
 // words were loaded ahead by the caller into mw.  Returns false if a wait gave up.
-template <typename T, int BN, int MM, bool PF>
+template <typename T, int BN, int NQ, int MM, bool PF>
 __device__ __forceinline__ bool softmax_tile(const TcArgs& a, int t, int kt, uint32_t tS, uint32_t tO,
                                              bool row_ok, int first_key, int last_key, const void* mrow_any,
                                              const uint32_t (&mw)[BN / 32], const uint32_t (&av)[av_words<BN, MM>()],
@@ -260,65 +267,78 @@ __device__ __forceinline__ bool softmax_tile(const TcArgs& a, int t, int kt, uin
     f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
     l_run = l_run * alpha + ((a0 + a1) + (b0 + b1));
   } else {
-    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-    const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
+    // RAW (scale > 0, no additive term): the maximum is taken over the raw visible scores
+    // and scaled once, and P = 2^(s*c - m) is one FFMA as on the fast path (a hidden score
+    // is -inf, and -inf * c stays -inf); otherwise the scores are scaled (and the additive
+    // term added) first.
+    auto masked_tile = [&](auto raw_tag) {
+      constexpr bool RAW = decltype(raw_tag)::value;
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
 #pragma unroll
-    for (int c = 0; c < BN / 32; ++c) {
-      uint32_t bits = 0xffffffffu;
-      if constexpr (MM == kMmBits) bits = PF ? mw[c] : (row_ok ? __ldg(mrow + j0 / 32 + c) : 0u);
-      // the visible columns of this word: mask bits, causal / key-count bound, window
-      // band, the row
-      const uint32_t vb = row_ok ? (bits & col_bound(c * 32, vis_lo, vis_hi)) : 0u;
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t bits = 0xffffffffu;
+        if constexpr (MM == kMmBits) bits = PF ? mw[c] : (row_ok ? __ldg(mrow + j0 / 32 + c) : 0u);
+        // the visible columns of this word: mask bits, causal / key-count bound, window
+        // band, the row
+        const uint32_t vb = row_ok ? (bits & col_bound(c * 32, vis_lo, vis_hi)) : 0u;
 #pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const int col = c * 32 + e;
-        float x0, x1;
-        f2_unpack(f2_mul(f2_pack(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])), c2), x0, x1);
-        if constexpr (MM == kMmAdd) {
-          // the additive term, in log2 units (masked columns are replaced below)
-          const uint32_t wv = av[col >> 1];
-          x0 = fmaf(to_f32<T>(*reinterpret_cast<const T*>(&wv)), kLog2e, x0);
-          x1 = fmaf(to_f32<T>(*(reinterpret_cast<const T*>(&wv) + 1)), kLog2e, x1);
+        for (int e = 0; e < 32; e += 2) {
+          const int col = c * 32 + e;
+          float x0 = __uint_as_float(sr[col]), x1 = __uint_as_float(sr[col + 1]);
+          if constexpr (!RAW) {
+            f2_unpack(f2_mul(f2_pack(x0, x1), c2), x0, x1);
+            if constexpr (MM == kMmAdd) {
+              // the additive term, in log2 units (masked columns are replaced below)
+              const uint32_t wv = av[col >> 1];
+              x0 = fmaf(to_f32<T>(*reinterpret_cast<const T*>(&wv)), kLog2e, x0);
+              x1 = fmaf(to_f32<T>(*(reinterpret_cast<const T*>(&wv) + 1)), kLog2e, x1);
+            }
+          }
+          x0 = (vb & (1u << e)) ? x0 : -INFINITY;
+          x1 = (vb & (2u << e)) ? x1 : -INFINITY;
+          sr[col] = __float_as_uint(x0);
+          sr[col + 1] = __float_as_uint(x1);
+          m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], x0, x1);
         }
-        x0 = (vb & (1u << e)) ? x0 : -INFINITY;
-        x1 = (vb & (2u << e)) ? x1 : -INFINITY;
-        sr[col] = __float_as_uint(x0);
-        sr[col + 1] = __float_as_uint(x1);
-        m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], x0, x1);
       }
-    }
-    const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-    const float m_new = fmaxf(m_run, mt);
-    need = m_new > m_run + kRescaleLog2;
-    if (need) {
-      alpha = ex2(m_run - m_new);
-      m_run = m_new;
-    }
-    // P = 2^(s - m); while no key of the row has been visible every s is -inf and
-    // 2^(s + 0) = 0
-    const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-    const uint64_t nm2 = f2_pack(neg_m, neg_m);
-    uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-    for (int c2i = 0; c2i < BN / 64; ++c2i) {
-      uint32_t pk[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int idx = c2i * 64 + 2 * e;
-        float y0, y1;
-        f2_unpack(f2_add(f2_pack(__uint_as_float(sr[idx]), __uint_as_float(sr[idx + 1])), nm2), y0, y1);
-        const float p0 = ex2(y0), p1 = ex2(y1);
-        acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
-        pk[e] = pack2<T>(p0, p1);
+      float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      if constexpr (RAW) mt *= p.scale_log2;
+      const float m_new = fmaxf(m_run, mt);
+      need = m_new > m_run + kRescaleLog2;
+      if (need) {
+        alpha = ex2(m_run - m_new);
+        m_run = m_new;
       }
-      tmem_st32(tS + c2i * 32, pk);
-    }
-    {
+      // P = 2^(s - m); while no key of the row has been visible every s is -inf and
+      // 2^(s + 0) = 0
+      const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+      const uint64_t nm2 = f2_pack(neg_m, neg_m);
+      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+      for (int c2i = 0; c2i < BN / 64; ++c2i) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int idx = c2i * 64 + 2 * e;
+          float y0, y1;
+          const uint64_t sv = f2_pack(__uint_as_float(sr[idx]), __uint_as_float(sr[idx + 1]));
+          if constexpr (RAW) f2_unpack(f2_fma(sv, c2, nm2), y0, y1);
+          else f2_unpack(f2_add(sv, nm2), y0, y1);
+          const float p0 = ex2(y0), p1 = ex2(y1);
+          acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
+          pk[e] = pack2<T>(p0, p1);
+        }
+        tmem_st32(tS + c2i * 32, pk);
+      }
       float a0, a1, b0, b1;
       f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
       f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
       l_run = l_run * alpha + ((a0 + a1) + (b0 + b1));
-    }
+    };
+    // (the two-tile variant, at its register limit, keeps the one general form)
+    if (NQ == 1 && MM != kMmAdd && p.scale_log2 > 0.f) masked_tile(std::true_type{});
+    else masked_tile(std::false_type{});
   }
   tmem_st_wait();
   if (t > 0 && wait_pv) {
@@ -427,11 +447,49 @@ __device__ __forceinline__ void epilogue_row_smem(const Params& p, uint32_t tO, 
   if (row_ok && p.lse) p.lse[(b * p.Hq + h) * p.Lq + i] = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
 }
 
+// Split-KV: the partial of key block c for one query row -- its running maximum m (log2
+// units), the sum l of 2^(s - m) and the unnormalised O, all relative to the same m
+// (zeros and m = -inf when the block holds no key the row sees) -- for the merge pass.
+__device__ __forceinline__ void partial_row(const Params& p, uint32_t tO, bool have_o, bool row_ok, int64_t b,
+                                            int64_t h, int64_t i, int64_t c, float m_run, float l_run) {
+  const int64_t row_global = (b * p.Hq + h) * p.Lq + i;
+  const int64_t slot = row_global * p.nblk + c;
+  float* po = p.part_o + slot * p.dv;
+  const int dv = (int)p.dv;
+  for (int c0 = 0; c0 < dv; c0 += 32) {
+    uint32_t o[32];
+    if (have_o) {
+      tmem_ld32_sync(tO + c0, o);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) o[e] = 0u;
+    }
+    if (row_ok) {
+#pragma unroll
+      for (int e4 = 0; e4 < 8; ++e4) {
+        const int col = c0 + e4 * 4;
+        if (col < dv)
+          *reinterpret_cast<uint4*>(po + col) = make_uint4(o[e4 * 4], o[e4 * 4 + 1], o[e4 * 4 + 2], o[e4 * 4 + 3]);
+      }
+    }
+  }
+  if (row_ok) {
+    p.part_ml[slot * 2 + 0] = have_o ? m_run : -INFINITY;
+    p.part_ml[slot * 2 + 1] = have_o ? l_run : 0.f;
+  }
+}
+
 template <int NQ>
 constexpr int tc_threads() { return (2 + 4 * NQ) * 32; }
 
+// CTAs per SM a variant is compiled for: the 64-key one-tile variant with the key bounds
+// alone serves the split-KV decode of heads up to 128, two CTAs per SM (each with 256
+// TMEM columns and under half the shared memory); every other variant owns its SM.
+template <int BN, int NQ, int MM>
+constexpr int tc_ctas_per_sm() { return (BN == 64 && NQ == 1 && MM == kMmBounds) ? 2 : 1; }
+
 template <typename T, int BN, int NQ, int MM, int STG>
-__global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __grid_constant__ TcArgs a) {
+__global__ void __launch_bounds__(tc_threads<NQ>(), (tc_ctas_per_sm<BN, NQ, MM>())) sdpa_prefill_tc(const __grid_constant__ TcArgs a) {
   static_assert(NQ == 1 || NQ == 2, "one or two Q tiles per CTA");
   static_assert(NQ == 1 || BN == 128, "the two-tile variant uses 128-key tiles");
   static_assert(STG >= 1 && STG <= kStages && (NQ == 1 || STG == 2), "ring depth");
@@ -458,7 +516,16 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
   // (32-bit: the planner sends no call whose rows, keys or CTAs do not fit)
   const int BH = (int)(p.B * p.Hkv);
   int bh, row0[NQ], i0[NQ], hhq[NQ];
-  if (a.head_local) {
+  int blk = 0;  // split: this CTA's key block
+  if (NQ == 1 && a.split) {
+    // split-KV (decode-sized row groups): key block, then row block, then (b, kv head)
+    int x = (int)blockIdx.x;
+    blk = x % (int)p.nblk; x /= (int)p.nblk;
+    row0[0] = (x % a.n_rt) * kBM;
+    bh = x / a.n_rt;
+    hhq[0] = 0;
+    i0[0] = 0;
+  } else if (a.head_local) {
     const int per = (int)(p.g / NQ);  // Q-tile groups (heads or head pairs) per KV head
     int x = (int)blockIdx.x;
     const int pr = x % per; x /= per;
@@ -496,6 +563,12 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
   int first_q[NQ], end_q[NQ];
 #pragma unroll
   for (int q = 0; q < NQ; ++q) tile_key_range<BN>(a, row0[q], i0[q], first_q[q], end_q[q]);
+  if (NQ == 1 && a.split) {
+    // the key tiles of block blk, cut from key 0 (whatever the rows' bounds)
+    const int b0 = blk * a.blk_tiles, b1 = b0 + a.blk_tiles;
+    first_q[0] = first_q[0] > b0 ? first_q[0] : b0;
+    end_q[0] = end_q[0] < b1 ? end_q[0] : b1;
+  }
   int kt0 = 0x7fffffff;
 #pragma unroll
   for (int q = 0; q < NQ; ++q)
@@ -527,7 +600,7 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_addr(tmem_holder), kTmemCols);
+    tmem_alloc(smem_addr(tmem_holder), (uint32_t)a.tmem_cols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -732,6 +805,8 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
     __syncwarp();
   } else {
     // ================================================================ softmax / epilogue
+    // (a bit-packed mask is written by the packing grid this kernel may overlap)
+    if constexpr (MM == kMmBits) asm volatile("griddepcontrol.wait;" ::: "memory");
     const int q = (warp - 2) / 4;  // which Q tile this warpgroup serves
     const int q4 = warp & 3;       // TMEM lane quarter this warp may access
     const int row = q4 * 32 + lane;
@@ -778,7 +853,7 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
         // tracks every earlier MMA of the issuing thread, so s_full already implies that O
         // holds P_{t-1} V_{t-1}
         uint32_t no_add[av_words<BN, MM>()];  // (additive masks take the one-tile variant)
-        ok = softmax_tile<T, BN, MM, false>(a, t, kt0 + t, tmem + lane_base + tS_col(q), tO, row_ok, first_key,
+        ok = softmax_tile<T, BN, NQ, MM, false>(a, t, kt0 + t, tmem + lane_base + tS_col(q), tO, row_ok, first_key,
                                             last_key, mrow_any, no_words, no_add, m_run, l_run, bar(kBarPvDone + q),
                                             false, limit, abort);
         if (!ok) {
@@ -825,7 +900,7 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
         }
         tc_fence_after();
         // S_t was issued before P_{t-1} V_{t-1}: the softmax waits for that product
-        ok = softmax_tile<T, BN, MM, true>(a, t, kt0 + t, tmem + lane_base + tS_col(slot), tO, row_ok, first_key,
+        ok = softmax_tile<T, BN, NQ, MM, true>(a, t, kt0 + t, tmem + lane_base + tS_col(slot), tO, row_ok, first_key,
                                            last_key, mrow_any, mw, av, m_run, l_run, bar(kBarPvDone + q), true,
                                            limit, abort);
         if (!ok) {
@@ -849,7 +924,10 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
       tc_fence_after();
     }
     ok = __all_sync(0xffffffffu, ok && !*abort);
-    if (a.tma_out) {
+    if (NQ == 1 && a.split && p.nblk > 1) {
+      // this key block's partial of the row: (m, l) and the unnormalised O
+      if (ok) partial_row(p, tO, n_tiles > 0, row_ok, bb, h, i, blk, m_run, l_run);
+    } else if (a.tma_out) {
       // The tile goes out through shared memory and one TMA store per panel: the row
       // stores of a warp would touch 32 rows each, and a CTA could not retire before
       // they drained.  The stage is this Q tile's buffer, unread since its last S
@@ -880,25 +958,34 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), 1) sdpa_prefill_tc(const __g
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, (uint32_t)a.tmem_cols);
   }
 }
 
 // Bool mask [Lq, Lk] bytes -> bits [Lq, words]: bit e of word w = mask[i, 32 w + e] != 0,
-// zero past Lk (the key tiles' padding).
-__global__ void sdpa_pack_mask_bits(const uint8_t* __restrict__ mask, int64_t Lq, int64_t Lk,
-                                    int64_t words, uint32_t* __restrict__ bits) {
-  const int64_t n = Lq * words;
-  for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < n;
-       w += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t i = w / words, j0 = (w % words) * 32;
-    uint32_t v = 0;
+// zero past Lk (the key tiles' padding).  A warp packs four words of a row per step: its
+// lanes read 32 consecutive bytes per word (any alignment) and one ballot gives the word.
+// The attention kernel is launched as a programmatic dependent: it may start once every
+// CTA here has begun, and its softmax warps wait for this grid before reading a bit.
+constexpr int kPackWarps = 8;
+__global__ void __launch_bounds__(kPackWarps * 32)
+sdpa_pack_mask_bits(const uint8_t* __restrict__ mask, int64_t Lq, int64_t Lk, int64_t words,
+                    uint32_t* __restrict__ bits) {
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int lane = threadIdx.x & 31;
+  const int64_t quads = words / 4;  // words per row is a multiple of 4
+  const int64_t n = Lq * quads;
+  const int64_t nwarps = (int64_t)gridDim.x * kPackWarps;
+  for (int64_t x = (int64_t)blockIdx.x * kPackWarps + (threadIdx.x >> 5); x < n; x += nwarps) {
+    const int64_t i = x / quads, w0 = (x % quads) * 4;
     const uint8_t* row = mask + i * Lk;
-    for (int e = 0; e < 32; ++e) {
-      const int64_t j = j0 + e;
-      if (j < Lk && row[j]) v |= 1u << e;
+    uint32_t v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t j = (w0 + k) * 32 + lane;
+      v[k] = __ballot_sync(0xffffffffu, j < Lk && row[j] != 0);
     }
-    bits[w] = v;
+    if (lane < 4) bits[i * words + w0 + lane] = lane == 0 ? v[0] : (lane == 1 ? v[1] : (lane == 2 ? v[2] : v[3]));
   }
 }
 
@@ -910,8 +997,26 @@ cudaError_t launch_tc_t(const TcArgs& a, size_t smem, int64_t grid, cudaStream_t
   cudaError_t e =
       set_max_dynamic_smem_once(configured, (const void*)sdpa_prefill_tc<T, BN, NQ, MM, STG>, (int)kTcMaxSmem);
   if (e != cudaSuccess) return e;
-  sdpa_prefill_tc<T, BN, NQ, MM, STG><<<(unsigned)grid, tc_threads<NQ>(), smem, st>>>(a);
-  return cudaGetLastError();
+  if constexpr (MM == kMmBits) {
+    // behind the mask packing, as its programmatic dependent: the prologue, the Q loads and
+    // the first products overlap the packing, and the softmax warps wait for its bits.
+    // (The packing itself was launched in stream order, so every earlier write of the
+    // stream -- q, k, v included -- is complete before this kernel can start.)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(tc_threads<NQ>());
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, sdpa_prefill_tc<T, BN, NQ, MM, STG>, a);
+  } else {
+    sdpa_prefill_tc<T, BN, NQ, MM, STG><<<(unsigned)grid, tc_threads<NQ>(), smem, st>>>(a);
+    return cudaGetLastError();
+  }
 }
 
 template <typename T, int MM>
@@ -946,10 +1051,10 @@ size_t smem_need(int64_t d, int64_t dv, int bn, int nq, int stg) {
 struct TileChoice {
   int bn, stg;
 };
-TileChoice tile_choice(int64_t d, int64_t dv) {
+TileChoice tile_choice(int64_t d, int64_t dv, int max_stages = 2) {
   const int64_t npv = (dv + 15) / 16 * 16;
   for (int bn : {128, 64})
-    for (int stg : {2, 1})
+    for (int stg = max_stages; stg >= 1; --stg)
       if ((int64_t)smem_need(d, dv, bn, 1, stg) <= kTcMaxSmem && 2 * bn + npv <= kTmemCols) return {bn, stg};
   return {0, 0};
 }
@@ -986,8 +1091,26 @@ size_t prefill_tc_mask_words(int64_t Lk) {
 }
 
 PrefillGeom prefill_tc_geometry(int64_t B, int64_t Hkv, int64_t g, int64_t Lq, int64_t d, int64_t dv,
-                                bool qo_packed, bool additive) {
+                                bool qo_packed, bool additive, int64_t nblk) {
   PrefillGeom r{};
+  if (nblk > 0) {
+    // split-KV over nblk key blocks: one Q tile of packed rows per CTA and key block.
+    // Heads up to 128: 64-key tiles in two-stage rings and 256 TMEM columns, so that two
+    // CTAs -- two independent streams of keys -- share each SM; wider heads: the
+    // one-tile variant's own tiles, one CTA per SM.
+    const TileChoice tc = (d <= 128 && dv <= 128) ? TileChoice{64, 2} : tile_choice(d, dv);
+    r.bn = tc.bn;
+    r.stg = tc.stg;
+    r.tmem_cols = (d <= 128 && dv <= 128) ? 256 : 512;
+    r.nq = 1;
+    r.head_local = 0;
+    r.qo5 = 0;
+    r.n_it = (Lq + kBM - 1) / kBM;
+    r.n_rt = (g * Lq + kBM - 1) / kBM;
+    r.grid = B * Hkv * r.n_rt * nblk;
+    r.split = 1;
+    return r;
+  }
   // (an additive mask takes 64-key tiles: two tiles' values live in registers)
   const TileChoice tc = tile_choice(d, dv);
   r.bn = additive ? 64 : tc.bn;
@@ -1005,15 +1128,23 @@ PrefillGeom prefill_tc_geometry(int64_t B, int64_t Hkv, int64_t g, int64_t Lq, i
   r.n_it = (Lq + kBM - 1) / kBM;
   r.n_rt = (G + kBM * r.nq - 1) / (kBM * r.nq);
   r.grid = r.head_local ? B * Hkv * (g / r.nq) * r.n_it : B * Hkv * r.n_rt;
+  r.tmem_cols = kTmemCols;
   return r;
 }
 
-cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, cudaStream_t st) {
+cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, bool split, cudaStream_t st) {
   TcArgs a;
   memset(&a, 0, sizeof(a));
   a.p = p;
-  const PrefillGeom geo =
-      prefill_tc_geometry(p.B, p.Hkv, p.g, p.Lq, p.d, p.dv, p.qo_packed != 0, p.mask_kind == kMaskAdd);
+  const PrefillGeom geo = prefill_tc_geometry(p.B, p.Hkv, p.g, p.Lq, p.d, p.dv, p.qo_packed != 0,
+                                              p.mask_kind == kMaskAdd, split ? p.nblk : 0);
+  // the split form reads packed q / out rows, with the key bounds (no mask tensor, window)
+  if (split && (!p.qo_packed || p.mask_kind == kMaskBool || p.mask_kind == kMaskAdd || p.window > 0 || p.nblk < 1 ||
+                p.keys_per_blk % geo.bn != 0 || (p.nblk > 1 && (!p.part_o || !p.part_ml))))
+    return cudaErrorInvalidValue;
+  a.split = geo.split;
+  a.blk_tiles = split ? (int)(p.keys_per_blk / geo.bn) : 0;
+  a.tmem_cols = geo.tmem_cols;
   const int bn = geo.bn, nq = geo.nq, stg = geo.stg;
   if (!bn || !prefill_tc_bn(p.d, p.dv) || (int64_t)smem_need(p.d, p.dv, bn, nq, stg) > kTcMaxSmem)
     return cudaErrorInvalidValue;
@@ -1049,16 +1180,18 @@ cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, c
   if (p.mask_kind == kMaskBool) {
     a.mask_words = (int64_t)prefill_tc_mask_words(p.Lk);
     a.mask_bits = mask_bits;
-    const int64_t n = p.Lq * a.mask_words;
-    int64_t g = (n + 255) / 256;
+    const int64_t n = p.Lq * (a.mask_words / 4);  // one warp step per four words
+    int64_t g = (n + kPackWarps - 1) / kPackWarps;
     const int64_t cap = (int64_t)device_sm_count() * 8;
     if (g > cap) g = cap;
-    sdpa_pack_mask_bits<<<(unsigned)(g > 0 ? g : 1), 256, 0, st>>>(p.mask, p.Lq, p.Lk, a.mask_words, mask_bits);
+    sdpa_pack_mask_bits<<<(unsigned)(g > 0 ? g : 1), kPackWarps * 32, 0, st>>>(p.mask, p.Lq, p.Lk, a.mask_words,
+                                                                               mask_bits);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   const int64_t grid = geo.grid;
-  const size_t smem = prefill_tc_smem_bytes(p.d, p.dv, bn, nq, stg);
+  // (two CTAs per SM: the ring and Q alone; otherwise at least 120 KB, one CTA per SM)
+  const size_t smem = geo.tmem_cols == 256 ? smem_need(p.d, p.dv, bn, nq, stg) : prefill_tc_smem_bytes(p.d, p.dv, bn, nq, stg);
   if (dtype == 1) return launch_tc_cfg<__half>(bn, nq, stg, a, smem, grid, st);
   return launch_tc_cfg<__nv_bfloat16>(bn, nq, stg, a, smem, grid, st);
 }

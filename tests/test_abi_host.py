@@ -139,6 +139,27 @@ def test_decode_grid_is_one_wave_and_splits_only_by_shape(nv):
         assert pl["grid"] <= max(152, -(-units // wpc))
 
 
+def test_decode_with_many_rows_per_kv_head_takes_the_split_tcgen05_kernel(nv):
+    """g x Lq > 16 query rows per KV head: the tcgen05 prefill kernel split over blocks of
+    whole 128-key tiles (at least 8), the same blocks for every batch size; a window, a
+    boolean mask or 16 rows or fewer keep the mma.sync decode kernel."""
+    dims = (8, 32, 4, 8, 32769, 128, 128)
+    ref = None
+    for B in (1, 2, 8, 64):
+        st, pl = plan(nv, (B,) + dims[1:], "causal", 1, "f16")
+        assert st == 0 and pl["path"] == "decode" and pl["kernel"] == "decode_tc", pl
+        assert pl["keys_per_blk"] % 128 == 0 and pl["keys_per_blk"] >= 8 * 128
+        assert pl["nblk"] * pl["keys_per_blk"] >= 32769 > (pl["nblk"] - 1) * pl["keys_per_blk"]
+        assert pl["grid"] == B * 4 * pl["nblk"] and pl["launches"] == 2
+        ref = ref or (pl["nblk"], pl["keys_per_blk"])
+        assert (pl["nblk"], pl["keys_per_blk"]) == ref
+    assert plan(nv, dims, "bool", 0, "bf16")[1]["kernel"] == "decode_mma"
+    assert plan(nv, (8, 8, 4, 8, 32769, 128, 128), "causal", 0, "bf16")[1]["kernel"] == "decode_mma"  # 16 rows
+    st, pl = nv.nv_sdpa_plan_ex(dims, nv.MASKS["causal"], 0, nv.DTYPES["bf16"], nv.make_options(window=512))
+    assert st == 0 and pl["kernel"] == "decode_mma"
+    assert plan(nv, dims, "causal", 0, "f32")[1]["kernel"] == "tiled_simt"
+
+
 # ----------------------------------------------------------------------------- entry points
 
 def test_nv_sdpa_rejects_before_touching_a_device(nv):
