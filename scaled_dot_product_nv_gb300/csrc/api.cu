@@ -303,13 +303,15 @@ int make_plan(const CallShape& cs, int mask_kind, int has_sinks, int dtype, nv_s
     }
     return NV_SDPA_OK;
   }
-  if (pl->path == NV_SDPA_PATH_DECODE && G > decode_mma_rows_per_warp() && cs.qo_packed && !cs.paged &&
+  if (pl->path == NV_SDPA_PATH_DECODE && (G > decode_mma_rows_per_warp() || x.d > 128 || x.dv > 128) &&
+      cs.qo_packed && !cs.paged &&
       !cs.window && (mask_kind == NV_SDPA_MASK_NONE || mask_kind == NV_SDPA_MASK_CAUSAL) &&
       prefill_tc_supported(dtype, x.d, x.dv)) {
-    // More query rows per KV head than one mma.sync row tile (g x Lq > 16): the tcgen05
-    // prefill kernel, split over key blocks, reads each KV head's keys once for up to 128
-    // rows (the mma.sync decode kernel would stream them once per 16 rows, and its
-    // products, not HBM, would bound it).  Blocks of whole 128-key tiles, cut from key 0,
+    // More query rows per KV head than one mma.sync row tile (g x Lq > 16), or heads
+    // wider than 128: the tcgen05 prefill kernel, split over key blocks, reads each KV
+    // head's keys once for up to 128 rows (the mma.sync decode kernel would stream them
+    // once per 16 rows, and its products, not HBM, would bound it; for wide heads its
+    // accumulators overflow the registers).  Blocks of whole 128-key tiles, cut from key 0,
     // sized from the keys and the head count alone (never B): as many as fill the CTA
     // slots (two per SM for heads up to 128) once for an 8-sequence batch, at least 8
     // tiles each.  (Measured, 8 x 32/4 heads x 8 queries x 32769 keys, f16: 9 blocks

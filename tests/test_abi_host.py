@@ -140,9 +140,10 @@ def test_decode_grid_is_one_wave_and_splits_only_by_shape(nv):
 
 
 def test_decode_with_many_rows_per_kv_head_takes_the_split_tcgen05_kernel(nv):
-    """g x Lq > 16 query rows per KV head: the tcgen05 prefill kernel split over blocks of
-    whole 128-key tiles (at least 8), the same blocks for every batch size; a window, a
-    boolean mask or 16 rows or fewer keep the mma.sync decode kernel."""
+    """g x Lq > 16 query rows per KV head, or a head wider than 128: the tcgen05 prefill
+    kernel split over blocks of whole 128-key tiles (at least 8), the same blocks for
+    every batch size; a window, a boolean mask or 16 rows or fewer of a head up to 128
+    keep the mma.sync decode kernel."""
     dims = (8, 32, 4, 8, 32769, 128, 128)
     ref = None
     for B in (1, 2, 8, 64):
@@ -158,6 +159,11 @@ def test_decode_with_many_rows_per_kv_head_takes_the_split_tcgen05_kernel(nv):
     st, pl = nv.nv_sdpa_plan_ex(dims, nv.MASKS["causal"], 0, nv.DTYPES["bf16"], nv.make_options(window=512))
     assert st == 0 and pl["kernel"] == "decode_mma"
     assert plan(nv, dims, "causal", 0, "f32")[1]["kernel"] == "tiled_simt"
+    # heads wider than 128 take it at any row count (the mma.sync kernel's accumulators
+    # would not fit its registers)
+    for d, dv in [(256, 256), (192, 192), (192, 128), (64, 256)]:
+        st, pl = plan(nv, (8, 16, 2, 1, 32769, d, dv), "causal", 1, "f16")
+        assert st == 0 and pl["kernel"] == "decode_tc", (d, dv, pl)
 
 
 # ----------------------------------------------------------------------------- entry points

@@ -33,6 +33,8 @@ CASES = [
      True),
     # fewer keys than queries under the causal mask: the first rows see no key
     (W.Case(1, 16, 2, 8, 5, 64, 64, "bf16", "causal", True, None, "n0.5", seed=85, name="keys_lt_queries"), False),
+    # one query per sequence on 256-wide heads (4 rows per KV head)
+    (W.Case(2, 8, 2, 1, 5000, 256, 256, "bf16", "causal", True, None, "n0.5", seed=89, name="lq1_d256"), True),
     # 192-wide heads, a tail block of a few keys
     (W.Case(3, 12, 3, 6, 2177, 192, 192, "bf16", "causal", False, None, "n0.5", seed=86, name="d192_tail"), True),
 ]
