@@ -36,6 +36,7 @@ struct DecArgs {
   int n_rc;       // row tiles of 16 rows per KV head
   int dpanels, dvpanels;
   int sub_rows;   // kKvPagedTma: rows of one TMA box, gcd(page, key tile)
+  int wpc;        // warps per CTA of this launch (at most the bucket's WPC)
 };
 
 template <typename T> struct MmaOp;
@@ -109,19 +110,19 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
   const uint32_t k_bytes = a.dpanels * kKT * 128, v_bytes = a.dvpanels * kKT * 128;
   const uint32_t stage_bytes = k_bytes + v_bytes;
   const uint32_t ring = smem_addr(base) + warp * ST * stage_bytes;  // this warp's stages
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + Sh::WPC * ST * stage_bytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + a.wpc * ST * stage_bytes);
   auto full = [&](int s) { return smem_addr(bars + warp * ST + s); };
 
   // the merge pass may be scheduled once every CTA of this grid is running
   asm volatile("griddepcontrol.launch_dependents;");
   if (threadIdx.x == 0) {
-    for (int i = 0; i < Sh::WPC * ST; ++i) mbar_init(smem_addr(bars + i), 1);
+    for (int i = 0; i < a.wpc * ST; ++i) mbar_init(smem_addr(bars + i), 1);
     fence_mbar_init();
   }
   __syncthreads();
 
   // ---- this warp's work: (b, KV head, row tile) and a contiguous run of its key blocks
-  const int64_t gw = (int64_t)blockIdx.x * Sh::WPC + warp;
+  const int64_t gw = (int64_t)blockIdx.x * a.wpc + warp;
   if (gw >= p.B * p.Hkv * a.n_rc * p.spans) return;
   const int64_t span = gw % p.spans;
   const int64_t unit = gw / p.spans;
@@ -498,7 +499,10 @@ cudaError_t launch_dec_t(const DecArgs& a, int64_t grid, cudaStream_t st) {
   static std::atomic<unsigned long long> configured{0};
   cudaError_t e = set_max_dynamic_smem_once(configured, (const void*)sdpa_decode_mma<T, DMAX, DV, KV>, Sh::kSmem);
   if (e != cudaSuccess) return e;
-  sdpa_decode_mma<T, DMAX, DV, KV><<<(unsigned)grid, Sh::WPC * 32, Sh::kSmem, st>>>(a);
+  if (a.wpc < 1 || a.wpc > Sh::WPC) return cudaErrorInvalidValue;
+  constexpr int ST = Sh::ST;
+  const int smem = a.wpc * ST * Sh::kStageBytes + 1024 + a.wpc * ST * 8 + 64;  // (Sh::kSmem at WPC warps)
+  sdpa_decode_mma<T, DMAX, DV, KV><<<(unsigned)grid, a.wpc * 32, smem, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -555,8 +559,9 @@ cudaError_t launch_dec_kv(int dtype, DecArgs& a, cudaStream_t st) {
   // every warp walks whole key blocks: a block size that is not a whole number of tiles,
   // or a run count outside [1, blocks], is a planner error
   if (!kt || p.spans < 1 || p.spans > p.nblk || p.keys_per_blk % kt != 0) return cudaErrorInvalidValue;
-  const int wpc = dec_info(p.d, p.dv).wpc;
-  const int64_t grid = (p.B * p.Hkv * a.n_rc * p.spans + wpc - 1) / wpc;
+  const int64_t warp_units = p.B * p.Hkv * a.n_rc * p.spans;
+  a.wpc = decode_mma_cta_warps(warp_units, p.d, p.dv);
+  const int64_t grid = (warp_units + a.wpc - 1) / a.wpc;
   return dtype == 1 ? launch_dec_bucket<__half, KV>(a, grid, st) : launch_dec_bucket<__nv_bfloat16, KV>(a, grid, st);
 }
 

@@ -22,6 +22,8 @@
 //   on the accumulator fragments (row max over a lane quad), P re-packed in registers as
 //   the A operand of O += P V with V read by ldmatrix.trans.  Tensor-core math keeps the
 //   SMs far from the ALU limit that FP32 dot products would hit at 8 query rows per key.
+#include <algorithm>
+
 #include "decode_kernel.cuh"
 
 namespace nvsdpa {
@@ -38,8 +40,19 @@ int decode_mma_warps_per_cta(int64_t d, int64_t dv) { return dec_info(d, dv).wpc
 int decode_mma_ctas_per_sm(int64_t d, int64_t dv) { return dec_info(d, dv).ctas_per_sm; }
 size_t decode_mma_smem_bytes(int64_t d, int64_t dv) { return (size_t)dec_info(d, dv).smem; }
 
+// Warps per CTA: the bucket's full CTA when the warps fill every SM, else fewer, so that
+// a small grid spreads over the SMs instead of piling onto a few (each warp streams its
+// own keys; an SM's share of the HBM stream grows with the warps it holds only up to the
+// bucket's size).
+int decode_mma_cta_warps(int64_t warp_units, int64_t d, int64_t dv) {
+  const DecInfo di = dec_info(d, dv);
+  if (!di.wpc) return 0;
+  const int64_t per_sm = (warp_units + (int64_t)device_sm_count() - 1) / (int64_t)device_sm_count();
+  return (int)std::max<int64_t>(1, std::min<int64_t>(di.wpc, per_sm));
+}
+
 int64_t decode_mma_grid(int64_t warp_units, int64_t d, int64_t dv) {
-  const int wpc = dec_info(d, dv).wpc;
+  const int wpc = decode_mma_cta_warps(warp_units, d, dv);
   return wpc ? (warp_units + wpc - 1) / wpc : 0;
 }
 

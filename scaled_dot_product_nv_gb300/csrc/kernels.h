@@ -64,6 +64,7 @@ int64_t decode_mma_key_tile();
 size_t decode_mma_smem_bytes(int64_t d, int64_t dv);
 int decode_mma_ctas_per_sm(int64_t d, int64_t dv);
 int decode_mma_warps_per_cta(int64_t d, int64_t dv);
+int decode_mma_cta_warps(int64_t warp_units, int64_t d, int64_t dv);
 int64_t decode_mma_grid(int64_t warp_units, int64_t d, int64_t dv);
 cudaError_t launch_decode_mma(int dtype, const Params& p, cudaStream_t st);
 // decode_paged.cu

@@ -157,19 +157,23 @@ enum { kMmBounds = 0, kMmBits = 1, kMmAdd = 2 };
 template <int BN, int MM>
 __host__ __device__ constexpr int av_words() { return MM == kMmAdd ? BN / 2 : 1; }
 
-// One row's additive-mask values of a key tile, av[w] = the tile's columns 2w and 2w + 1,
-// from the mask tensor `base` (T elements, `total` of them) where the tile's column 0 is
-// element `off`.  The row may start anywhere: the loads are 16-byte chunks from the
-// 8-element boundary at or below `off`, shifted down by the difference, so that a warp's
-// load touches each of its 32 rows' lines once per 8 columns.  Columns past the row are
-// whatever follows it (the caller masks them); nothing past the tensor is read.
+// Words of raw 16-byte chunks a row's additive values of one key tile span (any
+// alignment: one chunk more than the tile's columns fill).
+template <int BN, int MM>
+__host__ __device__ constexpr int ar_words() { return MM == kMmAdd ? 4 * (BN / 8 + 1) : 1; }
+
+// One row's additive-mask values of a key tile, in two steps so that the loads of the
+// next tile are in flight while this one is computed: load_additive issues the loads of
+// the 16-byte chunks from the 8-element boundary at or below `off` (the tile's column 0
+// in the mask tensor `base`, T elements, `total` of them) into w, and shift_additive
+// later gives av[i] = the tile's columns 2i and 2i + 1, shifted down by off mod 8.  A
+// warp's load touches each of its 32 rows' lines once per 8 columns.  Columns past the
+// row are whatever follows it (the caller masks them); nothing past the tensor is read.
 template <typename T, int BN>
 __device__ __forceinline__ void load_additive(const T* base, int64_t off, int64_t total, bool row_ok,
-                                              uint32_t (&av)[BN / 2]) {
+                                              uint32_t (&w)[4 * (BN / 8 + 1)]) {
   constexpr int kChunks = BN / 8 + 1;
-  uint32_t w[4 * kChunks];
   const int64_t a0 = off & ~int64_t(7);
-  const int m = (int)(off - a0);
 #pragma unroll
   for (int c = 0; c < kChunks; ++c) {
     const int64_t e = a0 + 8 * c;
@@ -192,6 +196,10 @@ __device__ __forceinline__ void load_additive(const T* base, int64_t off, int64_
     w[4 * c + 2] = v.z;
     w[4 * c + 3] = v.w;
   }
+}
+
+template <int BN>
+__device__ __forceinline__ void shift_additive(const uint32_t (&w)[4 * (BN / 8 + 1)], int m, uint32_t (&av)[BN / 2]) {
   const int ws = m >> 1;
   const bool odd = (m & 1) != 0;
 #pragma unroll
@@ -873,25 +881,25 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), (tc_ctas_per_sm<BN, NQ, MM>(
           dst[c] = (MM == kMmBits && row_ok) ? __ldg(mrow + ((kt0 + t) * BN) / 32 + c) : 0u;
       };
       if (n_tiles > 0) load_mw(0, mw);
-      // this row's additive-mask values of a key tile (kMmAdd)
-      uint32_t av[av_words<BN, MM>()];
-      auto load_av = [&](int t, uint32_t (&dst)[av_words<BN, MM>()]) {
-        if constexpr (MM == kMmAdd) {
-          const int64_t off = (int64_t)((const T*)mrow_any - reinterpret_cast<const T*>(p.amask)) +
-                              (int64_t)(kt0 + t) * BN;
-          load_additive<T, BN>(reinterpret_cast<const T*>(p.amask), off, a.amask_total, row_ok, dst);
-        }
+      // this row's additive-mask values (kMmAdd): the raw chunks of the next key tile are
+      // loaded while this one is computed (the row's offset mod 8 is the same for every
+      // tile: 8 divides BN)
+      uint32_t ar[ar_words<BN, MM>()];
+      const int64_t am_row = MM == kMmAdd ? (int64_t)((const T*)mrow_any - reinterpret_cast<const T*>(p.amask)) : 0;
+      auto load_raw = [&](int t) {
+        if constexpr (MM == kMmAdd)
+          load_additive<T, BN>(reinterpret_cast<const T*>(p.amask), am_row + (int64_t)(kt0 + t) * BN,
+                               a.amask_total, row_ok, ar);
       };
-      if (n_tiles > 0) load_av(0, av);
+      if (n_tiles > 0) load_raw(0);
       for (int t = 0; t < n_tiles; ++t) {
         uint32_t mw_next[BN / 32];
         if (t + 1 < n_tiles) load_mw(t + 1, mw_next);
         const int slot = t & 1;
-        // the next tile's additive values, loaded a tile ahead so that their latency falls
-        // in this tile's work
-        uint32_t av_next[av_words<BN, MM>()];
+        uint32_t av[av_words<BN, MM>()];
         if constexpr (MM == kMmAdd) {
-          if (t + 1 < n_tiles) load_av(t + 1, av_next);
+          shift_additive<BN>(ar, (int)((am_row + (int64_t)kt0 * BN) & 7), av);
+          if (t + 1 < n_tiles) load_raw(t + 1);
         }
         ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull + slot), (t >> 1) & 1, limit, abort));
         if (!ok) {
@@ -911,10 +919,6 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), (tc_ctas_per_sm<BN, NQ, MM>(
         mbar_arrive(bar(kBarPFull + slot));
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) mw[c] = mw_next[c];
-        if constexpr (MM == kMmAdd) {
-#pragma unroll
-          for (int c = 0; c < av_words<BN, MM>(); ++c) av[c] = av_next[c];
-        }
       }
     }
     // ---- epilogue

@@ -125,18 +125,22 @@ def test_decode_scratch_is_small_next_to_the_keys(nv):
 
 
 def test_decode_grid_is_one_wave_and_splits_only_by_shape(nv):
-    """The decode kernel's warps (8 per CTA, one CTA per SM of 152 for d = dv = 128) run as
-    one wave for any batch size, each walking a run of key blocks; the blocks themselves
+    """The decode kernel's warps (up to 8 per CTA, one CTA per SM of 152 for d = dv = 128)
+    run as one wave for any batch size, each walking a run of key blocks; a grid of fewer
+    warps than 8 per SM takes smaller CTAs, spread over the SMs.  The blocks themselves
     depend on the head shape and Lk only."""
-    wpc, warp_slots = 8, 8 * 152
+    warp_slots = 8 * 152
     for B in (1, 2, 8, 64):
         st, pl = plan(nv, (B, 32, 4, 1, 32769, 128, 128), "causal", 1, "f16")
         assert st == 0 and pl["path"] == "decode" and pl["kernel"] == "decode_mma"
         assert (pl["nblk"], pl["keys_per_blk"]) == (74, 448)
         units = B * 4
         spans = min(pl["nblk"], max(1, warp_slots // units))
+        wpc = max(1, min(8, -(-units * spans // 152)))
         assert pl["grid"] == -(-units * spans // wpc)
-        assert pl["grid"] <= max(152, -(-units // wpc))
+        assert pl["grid"] <= max(152, -(-units // 8))
+    # one sequence: 4 x 74 warps in CTAs of 2, over 148 SMs
+    assert plan(nv, (1, 32, 4, 1, 32769, 128, 128), "causal", 1, "f16")[1]["grid"] == 148
 
 
 def test_decode_with_many_rows_per_kv_head_takes_the_split_tcgen05_kernel(nv):
