@@ -443,15 +443,19 @@ def feature_lines(torch, nv, dev, stream, pk, pc, px, dc, dx, mc, mx, args):
                                       {"mask_bytes_per_call": am.numel() * 2})
     del mq, mk_, mv, am, mo
     # decode with one sequence (the measured key split's case) and with 8 queries per sequence
-    for name, B1, Lq1 in (("decode_b1", 1, 1), ("decode_lq8", dc.B, 8)):
+    # and the pages' 256-wide decode shape (16/2 heads, one query over the same keys)
+    for name, B1, Lq1, hd in (("decode_b1", 1, 1, None), ("decode_lq8", dc.B, 8, None),
+                              ("decode_d256", dc.B, 1, (16, 2, 256))):
         c1 = dc.with_(B=B1, Lq=Lq1)
+        if hd:
+            c1 = c1.with_(Hq=hd[0], Hkv=hd[1], d=hd[2], dv=hd[2])
         x1 = W.make_inputs(c1)
         q1, k1, v1, s1 = (up(x1[n], c1.dtype) for n in ("q", "k", "v", "sinks"))
         o1 = torch.empty((c1.B, c1.Hq, c1.Lq, c1.dv), dtype=q1.dtype, device=dev)
         ms = timed(lambda: nv.sdpa(q1, k1, v1, mask_kind="causal", scale=c1.scale_f32, sinks=s1, out=o1,
                                    want_lse=False))
         _, pl1 = nv.nv_sdpa_plan((c1.B, c1.Hq, c1.Hkv, c1.Lq, c1.Lk, c1.d, c1.dv), 1, 1, W.DTYPE_CODES[c1.dtype])
-        out[name] = hbm_line(f"decode_f16_b{c1.B}_h32x4_lq{c1.Lq}_lk32769_d128_sinks", kv_bytes(c1), ms,
+        out[name] = hbm_line(f"decode_f16_b{c1.B}_h{c1.Hq}x{c1.Hkv}_lq{c1.Lq}_lk32769_d{c1.d}_sinks", kv_bytes(c1), ms,
                              {"nblk": pl1["nblk"], "keys_per_blk": pl1["keys_per_blk"], "kernel": pl1["kernel"]})
         del q1, k1, v1, o1
     # decode: a window of 4096 over the 32769 keys, and the keys in a paged cache
@@ -772,7 +776,10 @@ def run_profile_case(args):
                            name="decode_f32_b8_h32x4_lk8193_d128_sinks"),
              "paged": W.decode_f16_long_kv(),
              # eight queries per sequence: 64 rows per KV head, the split tcgen05 kernel
-             "decode_lq8": W.decode_f16_long_kv().with_(Lq=8, name="decode_f16_b8_h32x4_lq8_lk32769_d128_sinks")}
+             "decode_lq8": W.decode_f16_long_kv().with_(Lq=8, name="decode_f16_b8_h32x4_lq8_lk32769_d128_sinks"),
+             # the 256-wide prefill with an additive mask [1, 16, 1024, 1801] instead of the boolean one
+             "additive": W.prefill_f16_boolmask_sinks().with_(mask="add",
+                                                              name="prefill_f16_b1_h16x2_lq1024_lk1801_d256_additive_sinks")}
     case = cases[args.profile_case]
     dev = torch.device("cuda", 0)
     gen = torch.Generator(device=dev)
@@ -785,9 +792,11 @@ def run_profile_case(args):
     k = rnd(case.B, case.Hkv, case.Lk, case.d)
     v = rnd(case.B, case.Hkv, case.Lk, case.dv)
     s = rnd(case.Hq) if case.sinks else None
-    m = None
+    m = am = None
     if case.mask == "bool":
         m = (torch.rand((case.Lq, case.Lk), generator=gen, device=dev) < 0.9).to(torch.uint8)
+    if case.mask == "add":
+        am = rnd(1, case.Hq, case.Lq, case.Lk)
     if args.profile_case == "paged":
         bs = 16
         per = -(-case.Lk // bs)
@@ -804,7 +813,7 @@ def run_profile_case(args):
             nv.sdpa_paged(q, kc, vc, table, lens, mask_kind="causal", scale=case.scale_f32, sinks=s)
     else:
         for _ in range(args.steps):
-            nv.sdpa(q, k, v, mask_kind=case.mask, scale=case.scale_f32, bool_mask=m, sinks=s)
+            nv.sdpa(q, k, v, mask_kind=case.mask, scale=case.scale_f32, bool_mask=m, sinks=s, add_mask=am)
     torch.cuda.synchronize()
     st, detail = nv.nv_sdpa_device_status(0)
     print(f"profile case {case.name} ({args.profile_case}): {args.steps} calls, device status {st}")
@@ -820,7 +829,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-case", choices=["prefill", "decode", "mask", "tiny", "decode256", "f32", "paged",
-                                               "decode_lq8"],
+                                               "decode_lq8", "additive"],
                     help="only launch this workload --steps times (for ncu); prints no JSON")
     args = ap.parse_args()
     if args.profile_case:
