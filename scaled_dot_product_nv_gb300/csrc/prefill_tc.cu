@@ -413,7 +413,7 @@ __device__ __forceinline__ void epilogue_row(const Params& p, uint32_t tO, bool 
   if (row_ok && p.lse) p.lse[lse_row] = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
 }
 
-// The same, for a TMA store of the whole tile: the row is written (scaled and rounded)
+// The same, for one TMA store of the whole tile (the two-tile variant): the row is written (scaled and rounded)
 // into `stage`, the tile's shared-memory image in the 128-byte-swizzled layout of the
 // loads (64-column panels of 128 rows x 128 B, 16-byte chunk c of row r at
 // (c ^ (r mod 8)) * 16); the log-sum-exp is written directly.
@@ -453,6 +453,50 @@ __device__ __forceinline__ void epilogue_row_smem(const Params& p, uint32_t tO, 
     }
   }
   if (row_ok && p.lse) p.lse[(b * p.Hq + h) * p.Lq + i] = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
+}
+
+// The same, for a TMA store of the tile panel by panel: epilogue_factor gives the row's
+// output factor (sink folded in, one division) and writes its log-sum-exp;
+// epilogue_panel_smem writes the row's 64 columns of panel pn (scaled, rounded once) into
+// `stage`, the tile's shared-memory image in the 128-byte-swizzled layout of the loads
+// (64-column panels of 128 rows x 128 B, 16-byte chunk c of row r at (c ^ (r mod 8)) * 16).
+template <typename T>
+__device__ __forceinline__ float epilogue_factor(const Params& p, bool row_ok, int64_t b, int64_t h, int64_t i,
+                                                 float m_run, float l_run) {
+  const float sk = sink_log2<T>(p, h);
+  const float M = fmaxf(m_run, sk);
+  float f = 0.f, L = 0.f;
+  if (M != -INFINITY) {
+    const float am = ex2(m_run - M);
+    L = l_run * am + ex2(sk - M);
+    f = am / L;
+  }
+  if (row_ok && p.lse) p.lse[(b * p.Hq + h) * p.Lq + i] = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
+  return f;
+}
+
+template <typename T>
+__device__ __forceinline__ void epilogue_panel_smem(const Params& p, uint32_t tO, bool have_o, float f, uint8_t* stage,
+                                                    int r, int pn) {
+  const int dv = (int)p.dv, c0 = pn * 64;
+  uint32_t o[64];
+  if (have_o) {
+    tmem_ld64_sync(tO + c0, o);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 64; ++e) o[e] = 0u;
+  }
+#pragma unroll
+  for (int e8 = 0; e8 < 8; ++e8) {
+    if (c0 + e8 * 8 < dv) {
+      uint4 v;
+      v.x = pack2<T>(__uint_as_float(o[e8 * 8 + 0]) * f, __uint_as_float(o[e8 * 8 + 1]) * f);
+      v.y = pack2<T>(__uint_as_float(o[e8 * 8 + 2]) * f, __uint_as_float(o[e8 * 8 + 3]) * f);
+      v.z = pack2<T>(__uint_as_float(o[e8 * 8 + 4]) * f, __uint_as_float(o[e8 * 8 + 5]) * f);
+      v.w = pack2<T>(__uint_as_float(o[e8 * 8 + 6]) * f, __uint_as_float(o[e8 * 8 + 7]) * f);
+      *reinterpret_cast<uint4*>(stage + pn * (kBM * 128) + r * 128 + ((e8 ^ (r & 7)) << 4)) = v;
+    }
+  }
 }
 
 // Split-KV: the partial of key block c for one query row -- its running maximum m (log2
@@ -939,18 +983,38 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), (tc_ctas_per_sm<BN, NQ, MM>(
       // loaded at all when the tile sees no key.  Every thread of the warpgroup reaches
       // the barrier, whatever happened before it.
       uint8_t* stage = base + q * q_bytes;
-      if (ok) epilogue_row_smem<T>(p, tO, n_tiles > 0, row_ok, bb, h, i, m_run, l_run, stage, row);
-      fence_proxy_async_smem();
-      const bool all_ok = bar_and(1 + q, 128, ok);
-      if (all_ok && warp == 2 + 4 * q && lane == 0) {
-        for (int pn = 0; pn < a.dvpanels; ++pn) {
+      const bool leader = warp == 2 + 4 * q && lane == 0;
+      if constexpr (NQ == 2) {
+        // (the two-tile variant, at its register limit, stages the whole tile first)
+        if (ok) epilogue_row_smem<T>(p, tO, n_tiles > 0, row_ok, bb, h, i, m_run, l_run, stage, row);
+        fence_proxy_async_smem();
+        const bool all_ok = bar_and(1 + q, 128, ok);
+        if (all_ok && leader) {
+          for (int pn = 0; pn < a.dvpanels; ++pn) {
+            if (a.qo5)
+              tma_store_5d(&a.tmo, smem_addr(stage + pn * (kBM * 128)), pn * 64, i0_q, hhq_q, (int)hkv, (int)bb);
+            else
+              tma_store_3d(&a.tmo, smem_addr(stage + pn * (kBM * 128)), pn * 64, row0_q, (int)bh);
+          }
+          bulk_commit_group();
+          bulk_wait_read_all();  // the stage must stay intact until the copy has read it
+        }
+      } else {
+      // Panel by panel: each panel's TMA store runs while the next one is staged.
+      const float f = ok ? epilogue_factor<T>(p, row_ok, bb, h, i, m_run, l_run) : 0.f;
+      for (int pn = 0; pn < a.dvpanels; ++pn) {
+        if (ok) epilogue_panel_smem<T>(p, tO, n_tiles > 0, f, stage, row, pn);
+        fence_proxy_async_smem();
+        const bool all_ok = bar_and(1 + q, 128, ok);
+        if (all_ok && leader) {
           if (a.qo5)
             tma_store_5d(&a.tmo, smem_addr(stage + pn * (kBM * 128)), pn * 64, i0_q, hhq_q, (int)hkv, (int)bb);
           else
             tma_store_3d(&a.tmo, smem_addr(stage + pn * (kBM * 128)), pn * 64, row0_q, (int)bh);
+          bulk_commit_group();
         }
-        bulk_commit_group();
-        bulk_wait_read_all();  // the stage must stay intact until the copy has read it
+      }
+      if (leader) bulk_wait_read_all();  // the stage must stay intact until the copies have read it
       }
     } else if (ok) {
       epilogue_row<T>(p, tO, n_tiles > 0, row_ok, bb, h, i, m_run, l_run);
