@@ -86,7 +86,18 @@ struct TcArgs {
 // is done)
 enum { kBarQ = 0, kBarKvFull = 1, kBarKvEmpty = 1 + kStages, kBarSFull = 1 + 2 * kStages,
        kBarPFull = 3 + 2 * kStages, kBarPvDone = 5 + 2 * kStages, kBarDrain = 7 + 2 * kStages,
-       kBarVFull = 8 + 2 * kStages, kBarVEmpty = 8 + 3 * kStages, kNumBars = 8 + 4 * kStages };
+       kBarVFull = 8 + 2 * kStages, kBarVEmpty = 8 + 3 * kStages, kBarMFull = 8 + 4 * kStages,
+       kNumBars = 10 + 4 * kStages };
+
+// Additive masks: each row's values of kAmTiles key tiles at a time are staged in shared
+// memory by one bulk copy per row, issued by the row's own softmax thread two chunks ahead
+// (16-byte aligned: from the 8-element boundary at or below the first column, 8 elements
+// more than the tiles span), in two buffers.
+constexpr int kAmTiles = 2;
+template <int BN>
+__host__ __device__ constexpr int am_row_bytes() { return (kAmTiles * BN + 8) * 2; }
+template <int BN>
+__host__ __device__ constexpr int am_bytes() { return 2 * 128 * am_row_bytes<BN>(); }
 
 __device__ __forceinline__ void fail(const Params& p, volatile int* abort, uint32_t bit) {
   *abort = 1;
@@ -156,59 +167,6 @@ enum { kMmBounds = 0, kMmBits = 1, kMmAdd = 2 };
 // otherwise).
 template <int BN, int MM>
 __host__ __device__ constexpr int av_words() { return MM == kMmAdd ? BN / 2 : 1; }
-
-// Words of raw 16-byte chunks a row's additive values of one key tile span (any
-// alignment: one chunk more than the tile's columns fill).
-template <int BN, int MM>
-__host__ __device__ constexpr int ar_words() { return MM == kMmAdd ? 4 * (BN / 8 + 1) : 1; }
-
-// One row's additive-mask values of a key tile, in two steps so that the loads of the
-// next tile are in flight while this one is computed: load_additive issues the loads of
-// the 16-byte chunks from the 8-element boundary at or below `off` (the tile's column 0
-// in the mask tensor `base`, T elements, `total` of them) into w, and shift_additive
-// later gives av[i] = the tile's columns 2i and 2i + 1, shifted down by off mod 8.  A
-// warp's load touches each of its 32 rows' lines once per 8 columns.  Columns past the
-// row are whatever follows it (the caller masks them); nothing past the tensor is read.
-template <typename T, int BN>
-__device__ __forceinline__ void load_additive(const T* base, int64_t off, int64_t total, bool row_ok,
-                                              uint32_t (&w)[4 * (BN / 8 + 1)]) {
-  constexpr int kChunks = BN / 8 + 1;
-  const int64_t a0 = off & ~int64_t(7);
-#pragma unroll
-  for (int c = 0; c < kChunks; ++c) {
-    const int64_t e = a0 + 8 * c;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (row_ok) {
-      if (e + 8 <= total) {
-        v = __ldg(reinterpret_cast<const uint4*>(base + e));
-      } else {
-        // the tensor's last chunk: element by element, nothing past its end
-        uint16_t h[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          h[k] = (e + k < total) ? __ldg(reinterpret_cast<const unsigned short*>(base + e + k)) : (uint16_t)0;
-        v = make_uint4(h[0] | (uint32_t)h[1] << 16, h[2] | (uint32_t)h[3] << 16, h[4] | (uint32_t)h[5] << 16,
-                       h[6] | (uint32_t)h[7] << 16);
-      }
-    }
-    w[4 * c] = v.x;
-    w[4 * c + 1] = v.y;
-    w[4 * c + 2] = v.z;
-    w[4 * c + 3] = v.w;
-  }
-}
-
-template <int BN>
-__device__ __forceinline__ void shift_additive(const uint32_t (&w)[4 * (BN / 8 + 1)], int m, uint32_t (&av)[BN / 2]) {
-  const int ws = m >> 1;
-  const bool odd = (m & 1) != 0;
-#pragma unroll
-  for (int i = 0; i < BN / 2; ++i) {
-    const uint32_t lo = ws == 0 ? w[i] : (ws == 1 ? w[i + 1] : (ws == 2 ? w[i + 2] : w[i + 3]));
-    const uint32_t hi = ws == 0 ? w[i + 1] : (ws == 1 ? w[i + 2] : (ws == 2 ? w[i + 3] : w[i + 4]));
-    av[i] = odd ? __funnelshift_r(lo, hi, 16) : lo;
-  }
-}
 
 // One query row's softmax step on its t-th key tile, key tile kt of the sequence.  tS /
 // tO: TMEM addresses (lane base included) of this tile's S columns and of O; the row
@@ -557,7 +515,10 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), (tc_ctas_per_sm<BN, NQ, MM>(
   const uint32_t sQ = smem_addr(base);
   const uint32_t sK = sQ + NQ * q_bytes;
   const uint32_t sV = sK + STG * k_bytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + NQ * q_bytes + STG * (k_bytes + v_bytes));
+  // (additive masks: the two staging buffers of the rows' mask values follow the rings)
+  const uint32_t sM = sV + STG * v_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + NQ * q_bytes + STG * (k_bytes + v_bytes) +
+                                               (MM == kMmAdd ? am_bytes<BN>() : 0));
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_holder + 1);
   auto bar = [&](int i) { return smem_addr(bars + i); };
@@ -648,6 +609,7 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), (tc_ctas_per_sm<BN, NQ, MM>(
       mbar_init(bar(kBarPvDone + b), 1);
     }
     mbar_init(bar(kBarDrain), 1);
+    for (int b = 0; b < 2; ++b) mbar_init(bar(kBarMFull + b), 128);  // (one arrival per softmax thread)
     *abort = 0;
     fence_mbar_init();
   }
@@ -925,25 +887,79 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), (tc_ctas_per_sm<BN, NQ, MM>(
           dst[c] = (MM == kMmBits && row_ok) ? __ldg(mrow + ((kt0 + t) * BN) / 32 + c) : 0u;
       };
       if (n_tiles > 0) load_mw(0, mw);
-      // this row's additive-mask values (kMmAdd): the raw chunks of the next key tile are
-      // loaded while this one is computed (the row's offset mod 8 is the same for every
-      // tile: 8 divides BN)
-      uint32_t ar[ar_words<BN, MM>()];
-      const int64_t am_row = MM == kMmAdd ? (int64_t)((const T*)mrow_any - reinterpret_cast<const T*>(p.amask)) : 0;
-      auto load_raw = [&](int t) {
-        if constexpr (MM == kMmAdd)
-          load_additive<T, BN>(reinterpret_cast<const T*>(p.amask), am_row + (int64_t)(kt0 + t) * BN,
-                               a.amask_total, row_ok, ar);
+      // this row's additive-mask values (kMmAdd) of tile t, from the staged chunk: its
+      // copy starts at the 8-element boundary below the chunk's first column, so the tile's
+      // columns start m + (t mod kAmTiles) * BN elements in (m = the row's offset mod 8,
+      // the same for every chunk: 8 divides BN)
+      const int64_t am_row_off =
+          MM == kMmAdd ? (int64_t)(reinterpret_cast<const T*>(mrow_any) - reinterpret_cast<const T*>(p.amask)) : 0;
+      const int am_m = (int)(am_row_off & 7);  // (the tensor starts on a 16-byte boundary)
+      // this row's copy of chunk c (key tiles [kAmTiles c, kAmTiles c + kAmTiles) of the walk)
+      // into buffer c & 1: [a0, a0 + row bytes) from the 8-element boundary at or below its
+      // first column, clipped to the tensor's last 16-byte boundary; every softmax thread
+      // arrives on the buffer's barrier with its bytes, a row past the tile's end with none
+      const int n_chunks = MM == kMmAdd ? (n_tiles + kAmTiles - 1) / kAmTiles : 0;
+      auto issue_chunk = [&](int c) {
+        if constexpr (MM == kMmAdd) {
+          const int b = c & 1;
+          const int64_t a0 = (am_row_off + (int64_t)(kt0 + kAmTiles * c) * BN) & ~int64_t(7);
+          uint32_t n = 0;
+          if (row_ok && a0 < a.amask_total) {
+            const int64_t avail = (a.amask_total - a0) * 2;
+            n = (uint32_t)(avail >= am_row_bytes<BN>() ? am_row_bytes<BN>() : (avail & ~int64_t(15)));
+          }
+          const uint32_t fb = bar(kBarMFull + b);
+          // (the buffer's previous contents were read by this thread alone, by generic loads)
+          fence_proxy_async_smem();
+          mbar_arrive_expect_tx(fb, n);
+          if (n) bulk_load(sM + b * (kBM * am_row_bytes<BN>()) + row * am_row_bytes<BN>(),
+                           reinterpret_cast<const T*>(p.amask) + a0, n, fb);
+        }
       };
-      if (n_tiles > 0) load_raw(0);
+      int chunks_issued = 0, chunks_seen = 0;
+      for (; chunks_issued < 2 && chunks_issued < n_chunks; ++chunks_issued) issue_chunk(chunks_issued);
       for (int t = 0; t < n_tiles; ++t) {
         uint32_t mw_next[BN / 32];
         if (t + 1 < n_tiles) load_mw(t + 1, mw_next);
         const int slot = t & 1;
         uint32_t av[av_words<BN, MM>()];
         if constexpr (MM == kMmAdd) {
-          shift_additive<BN>(ar, (int)((am_row + (int64_t)kt0 * BN) & 7), av);
-          if (t + 1 < n_tiles) load_raw(t + 1);
+          const int c = t / kAmTiles, b = c & 1;
+          if (t % kAmTiles == 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarMFull + b), (c >> 1) & 1, limit, abort));
+            if (!ok) {
+              fail(p, abort, kStatTimeoutTmaFull);
+              break;
+            }
+            chunks_seen = c + 1;
+          }
+          const int e0 = am_m + (t % kAmTiles) * BN;
+          const uint32_t rs = sM + b * (kBM * am_row_bytes<BN>()) + row * am_row_bytes<BN>() + (e0 >> 1) * 4;
+          uint32_t w[BN / 2 + 1];
+#pragma unroll
+          for (int k = 0; k < BN / 2 + 1; ++k)
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[k]) : "r"(rs + 4 * k) : "memory");
+#pragma unroll
+          for (int k = 0; k < BN / 2; ++k) av[k] = (e0 & 1) ? __funnelshift_r(w[k], w[k + 1], 16) : w[k];
+          // the tensor's last elements past its last 16-byte boundary are not staged (a bulk
+          // copy moves whole 16-byte units): the row that ends there reads them directly
+          const int64_t g0 = am_row_off + (int64_t)(kt0 + t) * BN, staged_end = a.amask_total & ~int64_t(7);
+          if (row_ok && g0 + BN > staged_end) {
+            const unsigned short* mb = reinterpret_cast<const unsigned short*>(p.amask);
+            for (int k = 0; k < BN / 2; ++k) {
+              const int64_t e = g0 + 2 * k;
+              uint32_t lo = av[k] & 0xffffu, hi = av[k] >> 16;
+              if (e >= staged_end && e < a.amask_total) lo = __ldg(mb + e);
+              if (e + 1 >= staged_end && e + 1 < a.amask_total) hi = __ldg(mb + e + 1);
+              av[k] = lo | (hi << 16);
+            }
+          }
+          // the chunk's buffer row is this thread's again once its last tile is read: chunk
+          // c + 2 goes into it
+          if ((t % kAmTiles == kAmTiles - 1 || t + 1 == n_tiles) && c + 2 < n_chunks) {
+            issue_chunk(c + 2);
+            chunks_issued = c + 3;
+          }
         }
         ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull + slot), (t >> 1) & 1, limit, abort));
         if (!ok) {
@@ -963,6 +979,12 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), (tc_ctas_per_sm<BN, NQ, MM>(
         mbar_arrive(bar(kBarPFull + slot));
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) mw[c] = mw_next[c];
+      }
+      if constexpr (MM == kMmAdd) {
+        // a loop that stopped early leaves chunk copies in flight: they land before the
+        // CTA may leave (bounded: a barrier some thread never arrived on gives up)
+        for (int c = chunks_seen; c < chunks_issued; ++c)
+          mbar_wait(bar(kBarMFull + (c & 1)), (c >> 1) & 1, kDrainLimit, nullptr);
       }
     }
     // ---- epilogue
@@ -1089,12 +1111,12 @@ cudaError_t launch_tc_t(const TcArgs& a, size_t smem, int64_t grid, cudaStream_t
 
 template <typename T, int MM>
 cudaError_t launch_tc_mm(int bn, int nq, int stg, const TcArgs& a, size_t smem, int64_t grid, cudaStream_t st) {
-  if (nq == 2) return stg == 2 ? launch_tc_t<T, 128, 2, MM, 2>(a, smem, grid, st) : cudaErrorInvalidValue;
   if constexpr (MM == kMmAdd) {
-    // (additive masks always take 64-key tiles and two stages)
-    if (bn != 64 || stg != 2) return cudaErrorInvalidValue;
-    return launch_tc_t<T, 64, 1, MM, 2>(a, smem, grid, st);
+    // (additive masks always take the one-tile variant with 64-key tiles and one stage)
+    if (nq != 1 || bn != 64 || stg != 1) return cudaErrorInvalidValue;
+    return launch_tc_t<T, 64, 1, MM, 1>(a, smem, grid, st);
   } else {
+    if (nq == 2) return stg == 2 ? launch_tc_t<T, 128, 2, MM, 2>(a, smem, grid, st) : cudaErrorInvalidValue;
     if (bn == 64) return stg == 2 ? launch_tc_t<T, 64, 1, MM, 2>(a, smem, grid, st) : cudaErrorInvalidValue;
     return stg == 2 ? launch_tc_t<T, 128, 1, MM, 2>(a, smem, grid, st) : launch_tc_t<T, 128, 1, MM, 1>(a, smem, grid, st);
   }
@@ -1179,13 +1201,14 @@ PrefillGeom prefill_tc_geometry(int64_t B, int64_t Hkv, int64_t g, int64_t Lq, i
     r.split = 1;
     return r;
   }
-  // (an additive mask takes 64-key tiles: two tiles' values live in registers)
+  // (an additive mask takes 64-key tiles: a tile's values live in registers)
   const TileChoice tc = tile_choice(d, dv);
   r.bn = additive ? 64 : tc.bn;
   const int64_t G = g * Lq;
-  // (an additive mask is read into registers per tile: the one-tile variant has room)
+  // (an additive mask is staged in shared memory: the one-tile variant has room)
   r.nq = additive ? 1 : prefill_tc_q_tiles(d, dv, G);
-  r.stg = (r.nq == 2 || r.bn == 64) ? 2 : tc.stg;
+  // (an additive mask stages its values next to one-stage K and V rings)
+  r.stg = additive ? 1 : ((r.nq == 2 || r.bn == 64) ? 2 : tc.stg);
   // strided q / out: Q tiles of one query head each (pairs of heads need an even group)
   if (!qo_packed && g % 2 != 0) r.nq = 1;
   r.qo5 = qo_packed ? 0 : 1;
@@ -1214,7 +1237,8 @@ cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, b
   a.blk_tiles = split ? (int)(p.keys_per_blk / geo.bn) : 0;
   a.tmem_cols = geo.tmem_cols;
   const int bn = geo.bn, nq = geo.nq, stg = geo.stg;
-  if (!bn || !prefill_tc_bn(p.d, p.dv) || (int64_t)smem_need(p.d, p.dv, bn, nq, stg) > kTcMaxSmem)
+  const size_t am_extra = p.mask_kind == kMaskAdd ? (size_t)am_bytes<64>() : 0;
+  if (!bn || !prefill_tc_bn(p.d, p.dv) || (int64_t)(smem_need(p.d, p.dv, bn, nq, stg) + am_extra) > kTcMaxSmem)
     return cudaErrorInvalidValue;
   const int64_t BH = p.B * p.Hkv;
   // K and V as 4-D [B][Hkv][Lk][d] views with the caller's strides
@@ -1259,7 +1283,8 @@ cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, b
   }
   const int64_t grid = geo.grid;
   // (two CTAs per SM: the ring and Q alone; otherwise at least 120 KB, one CTA per SM)
-  const size_t smem = geo.tmem_cols == 256 ? smem_need(p.d, p.dv, bn, nq, stg) : prefill_tc_smem_bytes(p.d, p.dv, bn, nq, stg);
+  const size_t smem = (geo.tmem_cols == 256 ? smem_need(p.d, p.dv, bn, nq, stg)
+                                            : prefill_tc_smem_bytes(p.d, p.dv, bn, nq, stg)) + am_extra;
   if (dtype == 1) return launch_tc_cfg<__half>(bn, nq, stg, a, smem, grid, st);
   return launch_tc_cfg<__nv_bfloat16>(bn, nq, stg, a, smem, grid, st);
 }

@@ -244,6 +244,24 @@ def test_additive_mask_matches_the_oracle(case, mshape):
     assert np.all(got[:, :, case.Lq // 2] == 0.0)
 
 
+@pytest.mark.parametrize("layouts", [("bhld_T", "contig", "contig", "bhld_T"), ("contig",) * 4],
+                         ids=["head_local_tiles", "packed_rows"])
+def test_additive_mask_staging_over_many_tiles(layouts):
+    """The staged additive values over many key tiles (chunks of two 64-key tiles, odd
+    counts, a row length that is no multiple of 8 elements, the tensor's last row ending
+    mid-chunk), with the rows taken from packed tiles and from head-local tiles (strided q
+    and out)."""
+    case = _case(2, 8, 2, 260, 1123, 128, 128, "bf16", "add", True, 409, name="add_staging_" + layouts[0])
+    x = W.make_inputs(case)
+    s = W.Stream(case.seed + 7)
+    am = s.normal(case.B * case.Hq * case.Lq * case.Lk).reshape(case.B, case.Hq, case.Lq, case.Lk)
+    am[..., ::11] = -np.inf
+    got, glse = run_ex(case, x, add_mask=am, layouts=layouts)
+    rows = _rows(case, n=60, seed=3)
+    want, wlse = want_ex(case, x, rows=rows, add_mask=am)
+    compare(case.name, case, got, glse, want, wlse, rows)
+
+
 # ----------------------------------------------------------------------------- strided views
 
 STRIDE_CASES = [
