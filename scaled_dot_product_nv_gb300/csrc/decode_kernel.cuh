@@ -72,6 +72,14 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "r"(addr));
 }
 
+// The transpose of an 8 x 8 matrix of 16-bit values held as an m8n8 fragment (thread t
+// holds row t / 4, columns 2 (t % 4) and 2 (t % 4) + 1): the same fragment of the transpose.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 // Byte address of (row, 16-byte chunk) in a [rows][128 B] panel written by TMA with the
 // 128-byte swizzle (chunk index XOR row mod 8).
 __device__ __forceinline__ uint32_t sw128(uint32_t panel, int row, int chunk) {
@@ -95,9 +103,14 @@ template <int DMAX, int DV> struct DecShape {
   static constexpr int kCtasPerSm = (kSmem <= 113 * 1024) ? 2 : 1;
 };
 
-template <typename T, int DMAX, int DV, int KV>
+// SW (up to 8 query rows per KV head, heads up to 128): the products are taken transposed,
+// S^T = K Q^T and O^T = V^T P^T, so that the 16 rows of each m16n8k16 are keys and value
+// columns, and the 8 query rows are its N side -- no padding rows, half the products of
+// the row-major form.  P^T reaches the B operand of O^T by an in-register 8 x 8 transpose.
+template <typename T, int DMAX, int DV, int KV, bool SW>
 __global__ void __launch_bounds__(DecShape<DMAX, DV>::WPC * 32, DecShape<DMAX, DV>::kCtasPerSm)
 sdpa_decode_mma(const __grid_constant__ DecArgs a) {
+  static_assert(!SW || (DMAX <= 128 && DV <= 128 && DecShape<DMAX, DV>::KT == 16), "the transposed form");
   using Sh = DecShape<DMAX, DV>;
   constexpr int ST = Sh::ST;
   constexpr int kKT = Sh::KT;
@@ -252,16 +265,16 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
     tma_prefetch_desc(&a.tmv);
   }
 
-  // This lane's two query rows (gid and gid + 8 of the row tile): the keys [lo, hi) each
-  // may see (32-bit: the planner sends no longer sequence here) and its mask row (boolean
-  // bytes or additive values, by mask kind).
+  // This lane's two query rows (gid and gid + 8 of the row tile; SW: 2 tig and 2 tig + 1):
+  // the keys [lo, hi) each may see (32-bit: the planner sends no longer sequence here) and
+  // its mask row (boolean bytes or additive values, by mask kind).
   int lo[2], hi[2];
   bool rok[2];
   const void* mk[2];
   const bool bool_mask = p.mask_kind == kMaskBool, add_mask = p.mask_kind == kMaskAdd;
 #pragma unroll
   for (int hrow = 0; hrow < 2; ++hrow) {
-    const int r = gid + 8 * hrow;
+    const int r = SW ? 2 * tig + hrow : gid + 8 * hrow;
     rok[hrow] = r < rows_here;
     const int64_t rho = rc * kRowsDec + (rok[hrow] ? r : 0);
     const int64_t i = rho % p.Lq, h = hkv * p.g + rho / p.Lq;
@@ -274,11 +287,26 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
                                      : nullptr);
   }
 
-  // Q fragments (A operand, row-major m16 x k16 per k-block), straight from global memory.
+  // Q fragments (A operand, row-major m16 x k16 per k-block; SW: B operand, Q^T k16 x n8,
+  // query row gid), straight from global memory.
   constexpr int kKB = DMAX / 16;  // k-blocks of the d bucket
   const int nkb = (int)((p.d + 15) / 16);
-  uint32_t qa[kKB][4];
-  {
+  uint32_t qa[kKB][SW ? 2 : 4];
+  if constexpr (SW) {
+    const bool gok = gid < rows_here;
+    const int64_t rho = rc * kRowsDec + (gok ? gid : 0);
+    const T* qrow = reinterpret_cast<const T*>(p.q) + q_offset(p, b, hkv * p.g + rho / p.Lq, rho % p.Lq);
+#pragma unroll
+    for (int kb = 0; kb < kKB; ++kb) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int c = kb * 16 + 2 * tig + 8 * e;
+        uint32_t v = 0;
+        if (kb < nkb && gok && c < p.d) v = *reinterpret_cast<const uint32_t*>(qrow + c);
+        qa[kb][e] = v;
+      }
+    }
+  } else {
     const T* qrow[2];
 #pragma unroll
     for (int hrow = 0; hrow < 2; ++hrow) {
@@ -298,7 +326,7 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
     }
   }
 
-  constexpr int NT = DV / 8;  // n-tiles of the output
+  constexpr int NT = SW ? DV / 16 : DV / 8;  // n-tiles of the output (SW: m-tiles of O^T)
   const int dv = (int)p.dv;
   float o[NT][4];
 #pragma unroll
@@ -312,13 +340,20 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
     float L[2];
 #pragma unroll
     for (int hrow = 0; hrow < 2; ++hrow) {
-      L[hrow] = l[hrow] + __shfl_xor_sync(0xffffffffu, l[hrow], 1);
-      L[hrow] += __shfl_xor_sync(0xffffffffu, L[hrow], 2);
+      if constexpr (SW) {
+        // (a row's keys are spread over the 8 lanes of one tig)
+        L[hrow] = l[hrow] + __shfl_xor_sync(0xffffffffu, l[hrow], 4);
+        L[hrow] += __shfl_xor_sync(0xffffffffu, L[hrow], 8);
+        L[hrow] += __shfl_xor_sync(0xffffffffu, L[hrow], 16);
+      } else {
+        L[hrow] = l[hrow] + __shfl_xor_sync(0xffffffffu, l[hrow], 1);
+        L[hrow] += __shfl_xor_sync(0xffffffffu, L[hrow], 2);
+      }
     }
 #pragma unroll
     for (int hrow = 0; hrow < 2; ++hrow) {
       if (!rok[hrow]) continue;
-      const int64_t rho = rc * kRowsDec + gid + 8 * hrow;
+      const int64_t rho = rc * kRowsDec + (SW ? 2 * tig + hrow : gid + 8 * hrow);
       const int64_t ri = rho % p.Lq, hr = hkv * p.g + rho / p.Lq;
       const int64_t row_global = (b * p.Hq + hr) * p.Lq + ri;
       const float M = m[hrow];
@@ -332,21 +367,45 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
           f = am / Lf;
         }
         T* orow = reinterpret_cast<T*>(p.out) + o_offset(p, b, hr, ri);
+        if constexpr (SW) {
+          // O^T fragment: value columns 16 j + gid and 16 j + gid + 8 of rows 2 tig, 2 tig + 1
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          const int cc = j * 8 + 2 * tig;
-          if (cc < dv)
-            *reinterpret_cast<uint32_t*>(orow + cc) = MmaOp<T>::pack(o[j][2 * hrow] * f, o[j][2 * hrow + 1] * f);
+          for (int j = 0; j < NT; ++j) {
+#pragma unroll
+            for (int hv = 0; hv < 2; ++hv) {
+              const int cc = j * 16 + gid + 8 * hv;
+              if (cc < dv) orow[cc] = from_f32<T>(o[j][2 * hv + hrow] * f);
+            }
+          }
+          if (gid == 0 && p.lse) p.lse[row_global] = (Mf == -INFINITY) ? -INFINITY : (Mf + log2f(Lf)) * kLn2;
+        } else {
+#pragma unroll
+          for (int j = 0; j < NT; ++j) {
+            const int cc = j * 8 + 2 * tig;
+            if (cc < dv)
+              *reinterpret_cast<uint32_t*>(orow + cc) = MmaOp<T>::pack(o[j][2 * hrow] * f, o[j][2 * hrow + 1] * f);
+          }
+          if (tig == 0 && p.lse) p.lse[row_global] = (Mf == -INFINITY) ? -INFINITY : (Mf + log2f(Lf)) * kLn2;
         }
-        if (tig == 0 && p.lse) p.lse[row_global] = (Mf == -INFINITY) ? -INFINITY : (Mf + log2f(Lf)) * kLn2;
       } else {
         float* po = p.part_o + (row_global * p.nblk + c) * p.dv;
+        if constexpr (SW) {
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          const int cc = j * 8 + 2 * tig;
-          if (cc < dv) *reinterpret_cast<float2*>(po + cc) = make_float2(o[j][2 * hrow], o[j][2 * hrow + 1]);
+          for (int j = 0; j < NT; ++j) {
+#pragma unroll
+            for (int hv = 0; hv < 2; ++hv) {
+              const int cc = j * 16 + gid + 8 * hv;
+              if (cc < dv) po[cc] = o[j][2 * hv + hrow];
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < NT; ++j) {
+            const int cc = j * 8 + 2 * tig;
+            if (cc < dv) *reinterpret_cast<float2*>(po + cc) = make_float2(o[j][2 * hrow], o[j][2 * hrow + 1]);
+          }
         }
-        if (tig == 0) {
+        if (SW ? gid == 0 : tig == 0) {
           p.part_ml[(row_global * p.nblk + c) * 2 + 0] = M;
           p.part_ml[(row_global * p.nblk + c) * 2 + 1] = L[hrow];
         }
@@ -380,90 +439,163 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
     const int64_t jb_end = u_lo + (c + 1) * p.keys_per_blk;
     const int j_end = (int)(jb_end < key_end ? jb_end : key_end);
     const uint32_t kst = ring + s * stage_bytes, vst = kst + k_bytes;
-    // ---- S = Q K^T over the tile's keys (n-tiles of 8 keys)
-    constexpr int NS = kKT / 8;  // n-tiles of S
-    float sc[NS][4];
+    if constexpr (SW) {
+      // ---- S^T = K Q^T: per 16 keys one m16 (keys) x n8 (query rows) tile; sc[e] holds
+      // key gid + 8 (e >> 1), row 2 tig + (e & 1)
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
-    for (int nt = 0; nt < NS; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-#pragma unroll
-    for (int kb = 0; kb < kKB; ++kb) {
-      if (kb < nkb) {
-        const int chunk = (kb & 3) * 2 + ((lane >> 3) & 1);
-#pragma unroll
-        for (int h16 = 0; h16 < kKT / 16; ++h16) {
-          uint32_t b0, b1, b2, b3;
-          const int krow = h16 * 16 + (lane >> 4) * 8 + (lane & 7);
-          ldsm_x4(sw128(kst + (kb >> 2) * kKT * 128, krow, chunk), b0, b1, b2, b3);
-          MmaOp<T>::run(sc[2 * h16], qa[kb], b0, b1);
-          MmaOp<T>::run(sc[2 * h16 + 1], qa[kb], b2, b3);
+      for (int kb = 0; kb < kKB; ++kb) {
+        if (kb < nkb) {
+          uint32_t af[4];
+          ldsm_x4(sw128(kst + (kb >> 2) * kKT * 128, krow, (kb & 3) * 2 + (lane >> 4)), af[0], af[1], af[2], af[3]);
+          MmaOp<T>::run(sc, af, qa[kb][0], qa[kb][1]);
         }
       }
-    }
-    // ---- mask, online softmax (rows gid / gid + 8; keys spread over the lane quad)
-    const int jt = (int)(key_begin + (int64_t)gt * kKT);
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int nt = 0; nt < NS; ++nt) {
+      // ---- mask, online softmax (a row's 16 keys over the 8 lanes of its tig)
+      const int jt = (int)(key_begin + (int64_t)gt * kKT);
+      float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int hrow = e >> 1;
-        const int j = jt + nt * 8 + 2 * tig + (e & 1);
+        const int hrow = e & 1;
+        const int j = jt + gid + 8 * (e >> 1);
         bool vis = rok[hrow] && j < j_end && j >= lo[hrow] && j < hi[hrow];
         if (bool_mask && vis) vis = static_cast<const uint8_t*>(mk[hrow])[j] != 0;
         float v = -INFINITY;
-        if (vis) v = add_mask ? fmaf(sc[nt][e], p.scale_log2, to_f32<T>(static_cast<const T*>(mk[hrow])[j]) * kLog2e)
-                              : sc[nt][e] * p.scale_log2;
-        sc[nt][e] = v;
+        if (vis) v = add_mask ? fmaf(sc[e], p.scale_log2, to_f32<T>(static_cast<const T*>(mk[hrow])[j]) * kLog2e)
+                              : sc[e] * p.scale_log2;
+        sc[e] = v;
         mx[hrow] = fmaxf(mx[hrow], v);
       }
-    }
-    float alpha[2];
-#pragma unroll
-    for (int hrow = 0; hrow < 2; ++hrow) {
-      mx[hrow] = fmaxf(mx[hrow], __shfl_xor_sync(0xffffffffu, mx[hrow], 1));
-      mx[hrow] = fmaxf(mx[hrow], __shfl_xor_sync(0xffffffffu, mx[hrow], 2));
-      const float m_new = fmaxf(m[hrow], mx[hrow]);
-      alpha[hrow] = 1.f;
-      if (m_new > m[hrow] + kRescaleLog2Dec) {
-        alpha[hrow] = ex2(m[hrow] - m_new);
-        m[hrow] = m_new;
-      }
-    }
-    // P as the A operand of the k16 steps: pa[ks] covers keys 16 ks .. 16 ks + 15
-    uint32_t pa[kKT / 16][4];
-#pragma unroll
-    for (int hrow = 0; hrow < 2; ++hrow) l[hrow] *= alpha[hrow];
-#pragma unroll
-    for (int nt = 0; nt < NS; ++nt) {
+      float alpha[2];
 #pragma unroll
       for (int hrow = 0; hrow < 2; ++hrow) {
-        const bool none = (m[hrow] == -INFINITY);
-        const float p0 = none ? 0.f : ex2(sc[nt][2 * hrow] - m[hrow]);
-        const float p1 = none ? 0.f : ex2(sc[nt][2 * hrow + 1] - m[hrow]);
-        l[hrow] += p0 + p1;
-        pa[nt >> 1][(nt & 1) * 2 + hrow] = MmaOp<T>::pack(p0, p1);
+        mx[hrow] = fmaxf(mx[hrow], __shfl_xor_sync(0xffffffffu, mx[hrow], 4));
+        mx[hrow] = fmaxf(mx[hrow], __shfl_xor_sync(0xffffffffu, mx[hrow], 8));
+        mx[hrow] = fmaxf(mx[hrow], __shfl_xor_sync(0xffffffffu, mx[hrow], 16));
+        const float m_new = fmaxf(m[hrow], mx[hrow]);
+        alpha[hrow] = 1.f;
+        if (m_new > m[hrow] + kRescaleLog2Dec) {
+          alpha[hrow] = ex2(m[hrow] - m_new);
+          m[hrow] = m_new;
+        }
+        l[hrow] *= alpha[hrow];
       }
-    }
-    if (alpha[0] != 1.f || alpha[1] != 1.f) {
+      float pv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int hrow = e & 1;
+        pv[e] = (m[hrow] == -INFINITY) ? 0.f : ex2(sc[e] - m[hrow]);
+        l[hrow] += pv[e];
+      }
+      // P^T as the B operand of O^T += V^T P^T: the 8 x 8 blocks (keys 0-7, keys 8-15) x
+      // rows, transposed in registers
+      const uint32_t pb0 = movmatrix_t(MmaOp<T>::pack(pv[0], pv[1]));
+      const uint32_t pb1 = movmatrix_t(MmaOp<T>::pack(pv[2], pv[3]));
+      if (alpha[0] != 1.f || alpha[1] != 1.f) {
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          o[j][0] *= alpha[0];
+          o[j][1] *= alpha[1];
+          o[j][2] *= alpha[0];
+          o[j][3] *= alpha[1];
+        }
+      }
+      // ---- O^T += V^T P^T: per 16 value columns, A = V^T from the V tile by ldmatrix.trans
+      const int vrow = (lane & 7) + (lane >> 4) * 8;
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
-        o[j][0] *= alpha[0];
-        o[j][1] *= alpha[0];
-        o[j][2] *= alpha[1];
-        o[j][3] *= alpha[1];
+        const int chunk = 2 * j + ((lane >> 3) & 1);  // 16-byte chunk of dv (8 columns)
+        uint32_t af[4];
+        ldsm_x4_t(sw128(vst + (chunk >> 3) * kKT * 128, vrow, chunk & 7), af[0], af[1], af[2], af[3]);
+        MmaOp<T>::run(o[j], af, pb0, pb1);
       }
-    }
-    // ---- O += P V: V tile rows = keys, ldmatrix.trans gives the k16 x n8 B fragments
-#pragma unroll
-    for (int ks = 0; ks < kKT / 16; ++ks) {
-      const int vrow = ks * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-#pragma unroll
-      for (int j2 = 0; j2 < NT / 2; ++j2) {
-        const int chunk = 2 * j2 + (lane >> 4);  // 16-byte chunk of dv (8 columns)
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(sw128(vst + (chunk >> 3) * kKT * 128, vrow, chunk & 7), b0, b1, b2, b3);
-        MmaOp<T>::run(o[2 * j2], pa[ks], b0, b1);
-        MmaOp<T>::run(o[2 * j2 + 1], pa[ks], b2, b3);
+    } else {
+      // ---- S = Q K^T over the tile's keys (n-tiles of 8 keys)
+      constexpr int NS = kKT / 8;  // n-tiles of S
+      float sc[NS][4];
+  #pragma unroll
+      for (int nt = 0; nt < NS; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+  #pragma unroll
+      for (int kb = 0; kb < kKB; ++kb) {
+        if (kb < nkb) {
+          const int chunk = (kb & 3) * 2 + ((lane >> 3) & 1);
+  #pragma unroll
+          for (int h16 = 0; h16 < kKT / 16; ++h16) {
+            uint32_t b0, b1, b2, b3;
+            const int krow = h16 * 16 + (lane >> 4) * 8 + (lane & 7);
+            ldsm_x4(sw128(kst + (kb >> 2) * kKT * 128, krow, chunk), b0, b1, b2, b3);
+            MmaOp<T>::run(sc[2 * h16], qa[kb], b0, b1);
+            MmaOp<T>::run(sc[2 * h16 + 1], qa[kb], b2, b3);
+          }
+        }
+      }
+      // ---- mask, online softmax (rows gid / gid + 8; keys spread over the lane quad)
+      const int jt = (int)(key_begin + (int64_t)gt * kKT);
+      float mx[2] = {-INFINITY, -INFINITY};
+  #pragma unroll
+      for (int nt = 0; nt < NS; ++nt) {
+  #pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int hrow = e >> 1;
+          const int j = jt + nt * 8 + 2 * tig + (e & 1);
+          bool vis = rok[hrow] && j < j_end && j >= lo[hrow] && j < hi[hrow];
+          if (bool_mask && vis) vis = static_cast<const uint8_t*>(mk[hrow])[j] != 0;
+          float v = -INFINITY;
+          if (vis) v = add_mask ? fmaf(sc[nt][e], p.scale_log2, to_f32<T>(static_cast<const T*>(mk[hrow])[j]) * kLog2e)
+                                : sc[nt][e] * p.scale_log2;
+          sc[nt][e] = v;
+          mx[hrow] = fmaxf(mx[hrow], v);
+        }
+      }
+      float alpha[2];
+  #pragma unroll
+      for (int hrow = 0; hrow < 2; ++hrow) {
+        mx[hrow] = fmaxf(mx[hrow], __shfl_xor_sync(0xffffffffu, mx[hrow], 1));
+        mx[hrow] = fmaxf(mx[hrow], __shfl_xor_sync(0xffffffffu, mx[hrow], 2));
+        const float m_new = fmaxf(m[hrow], mx[hrow]);
+        alpha[hrow] = 1.f;
+        if (m_new > m[hrow] + kRescaleLog2Dec) {
+          alpha[hrow] = ex2(m[hrow] - m_new);
+          m[hrow] = m_new;
+        }
+      }
+      // P as the A operand of the k16 steps: pa[ks] covers keys 16 ks .. 16 ks + 15
+      uint32_t pa[kKT / 16][4];
+  #pragma unroll
+      for (int hrow = 0; hrow < 2; ++hrow) l[hrow] *= alpha[hrow];
+  #pragma unroll
+      for (int nt = 0; nt < NS; ++nt) {
+  #pragma unroll
+        for (int hrow = 0; hrow < 2; ++hrow) {
+          const bool none = (m[hrow] == -INFINITY);
+          const float p0 = none ? 0.f : ex2(sc[nt][2 * hrow] - m[hrow]);
+          const float p1 = none ? 0.f : ex2(sc[nt][2 * hrow + 1] - m[hrow]);
+          l[hrow] += p0 + p1;
+          pa[nt >> 1][(nt & 1) * 2 + hrow] = MmaOp<T>::pack(p0, p1);
+        }
+      }
+      if (alpha[0] != 1.f || alpha[1] != 1.f) {
+  #pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          o[j][0] *= alpha[0];
+          o[j][1] *= alpha[0];
+          o[j][2] *= alpha[1];
+          o[j][3] *= alpha[1];
+        }
+      }
+      // ---- O += P V: V tile rows = keys, ldmatrix.trans gives the k16 x n8 B fragments
+  #pragma unroll
+      for (int ks = 0; ks < kKT / 16; ++ks) {
+        const int vrow = ks * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+  #pragma unroll
+        for (int j2 = 0; j2 < NT / 2; ++j2) {
+          const int chunk = 2 * j2 + (lane >> 4);  // 16-byte chunk of dv (8 columns)
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(sw128(vst + (chunk >> 3) * kKT * 128, vrow, chunk & 7), b0, b1, b2, b3);
+          MmaOp<T>::run(o[2 * j2], pa[ks], b0, b1);
+          MmaOp<T>::run(o[2 * j2 + 1], pa[ks], b2, b3);
+        }
       }
     }
     // ---- the slot is read: refill it with tile gt + ST (the async proxy's write must
@@ -493,16 +625,16 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
   __syncwarp();
 }
 
-template <typename T, int DMAX, int DV, int KV>
+template <typename T, int DMAX, int DV, int KV, bool SW>
 cudaError_t launch_dec_t(const DecArgs& a, int64_t grid, cudaStream_t st) {
   using Sh = DecShape<DMAX, DV>;
   static std::atomic<unsigned long long> configured{0};
-  cudaError_t e = set_max_dynamic_smem_once(configured, (const void*)sdpa_decode_mma<T, DMAX, DV, KV>, Sh::kSmem);
+  cudaError_t e = set_max_dynamic_smem_once(configured, (const void*)sdpa_decode_mma<T, DMAX, DV, KV, SW>, Sh::kSmem);
   if (e != cudaSuccess) return e;
   if (a.wpc < 1 || a.wpc > Sh::WPC) return cudaErrorInvalidValue;
   constexpr int ST = Sh::ST;
   const int smem = a.wpc * ST * Sh::kStageBytes + 1024 + a.wpc * ST * 8 + 64;  // (Sh::kSmem at WPC warps)
-  sdpa_decode_mma<T, DMAX, DV, KV><<<(unsigned)grid, a.wpc * 32, smem, st>>>(a);
+  sdpa_decode_mma<T, DMAX, DV, KV, SW><<<(unsigned)grid, a.wpc * 32, smem, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -537,13 +669,16 @@ inline DecInfo dec_info(int64_t d, int64_t dv) {
 
 template <typename T, int KV>
 cudaError_t launch_dec_bucket(const DecArgs& a, int64_t grid, cudaStream_t st) {
+  const bool sw = a.p.G <= 8;
   switch (dec_bucket(a.p.d, a.p.dv)) {
-    case 0: return launch_dec_t<T, 64, 64, KV>(a, grid, st);
-    case 1: return launch_dec_t<T, 128, 64, KV>(a, grid, st);
-    case 2: return launch_dec_t<T, 128, 128, KV>(a, grid, st);
-    case 3: return launch_dec_t<T, 192, 128, KV>(a, grid, st);
-    case 4: return launch_dec_t<T, 192, 192, KV>(a, grid, st);
-    case 5: return launch_dec_t<T, 256, 256, KV>(a, grid, st);
+    // (up to 8 query rows per KV head: the transposed products)
+    case 0: return sw ? launch_dec_t<T, 64, 64, KV, true>(a, grid, st) : launch_dec_t<T, 64, 64, KV, false>(a, grid, st);
+    case 1: return sw ? launch_dec_t<T, 128, 64, KV, true>(a, grid, st) : launch_dec_t<T, 128, 64, KV, false>(a, grid, st);
+    case 2:
+      return sw ? launch_dec_t<T, 128, 128, KV, true>(a, grid, st) : launch_dec_t<T, 128, 128, KV, false>(a, grid, st);
+    case 3: return launch_dec_t<T, 192, 128, KV, false>(a, grid, st);
+    case 4: return launch_dec_t<T, 192, 192, KV, false>(a, grid, st);
+    case 5: return launch_dec_t<T, 256, 256, KV, false>(a, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }
