@@ -48,7 +48,7 @@ size_t prefill_tc_mask_words(int64_t Lk);
 // With nblk > 0, the split-KV form (decode-sized row groups): one Q tile of packed rows
 // per CTA and key block.
 struct PrefillGeom {
-  int bn, nq, stg, head_local, qo5, split, tmem_cols;
+  int bn, nq, stg, head_local, qo5, split, tmem_cols, q_rows, unpadded;
   int64_t n_it, n_rt, grid;
 };
 PrefillGeom prefill_tc_geometry(int64_t B, int64_t Hkv, int64_t g, int64_t Lq, int64_t d, int64_t dv,

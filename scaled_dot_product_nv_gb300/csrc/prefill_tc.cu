@@ -49,7 +49,7 @@ namespace {
 using namespace sm100;
 
 constexpr int kBM = 128;
-constexpr int kStages = 2;  // the deepest K / V ring (barrier slots)
+constexpr int kStages = 3;  // the deepest K / V ring (barrier slots)
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr uint64_t kDrainLimit = 1ull << 18;  // polls of <= ~10 us each
@@ -78,6 +78,10 @@ struct TcArgs {
                      // (nblk > 1) its rows' partials go to part_o / part_ml for the merge
   int blk_tiles;     // split: key tiles per block (keys_per_blk / BN)
   int tmem_cols;     // TMEM columns allocated: 512, or 256 where two CTAs share the SM
+  int q_rows;        // rows of a Q tile's buffer: 128, or 64 (split-KV, at most 64 rows; the
+                     // MMA's rows past 64 read the next panel's, whose scores are masked)
+  int unpadded;      // the dynamic shared memory was requested without alignment slack:
+                     // its start must already be 1024-byte aligned (checked)
 };
 
 // barrier slots
@@ -503,13 +507,19 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), (tc_ctas_per_sm<BN, NQ, MM>(
   static_assert(NQ == 1 || NQ == 2, "one or two Q tiles per CTA");
   static_assert(NQ == 1 || BN == 128, "the two-tile variant uses 128-key tiles");
   static_assert(STG >= 1 && STG <= kStages && (NQ == 1 || STG == 2), "ring depth");
+  static_assert(STG <= 2 || (NQ == 1 && BN == 64 && MM == kMmBounds), "three stages: the two-CTA split-KV form");
   constexpr int kMaxKsteps = (NQ == 2) ? 8 : 16;  // d <= 128 for two tiles, <= 256 otherwise
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  if (a.unpadded && base != smem_raw) {
+    // (the request had no room to align: the CTA does nothing and the call reports it)
+    if (threadIdx.x == 0) record_status(a.p, kStatBadConfig);
+    return;
+  }
   const Params& p = a.p;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const uint32_t q_bytes = a.dpanels * kBM * 128;  // one Q tile
+  const uint32_t q_bytes = a.dpanels * a.q_rows * 128;  // one Q tile's buffer
   const uint32_t k_bytes = a.dpanels * BN * 128;
   const uint32_t v_bytes = a.dvpanels * BN * 128;
   const uint32_t sQ = smem_addr(base);
@@ -643,10 +653,10 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), (tc_ctas_per_sm<BN, NQ, MM>(
         if (n_q[q] > 0)
           for (int pn = 0; pn < a.dpanels; ++pn) {
             if (a.qo5)
-              tma_load_5d(sQ + q * q_bytes + pn * kBM * 128, &a.tmq, bar(kBarQ), pn * 64, (int)i0[q], hhq[q],
+              tma_load_5d(sQ + q * q_bytes + pn * a.q_rows * 128, &a.tmq, bar(kBarQ), pn * 64, (int)i0[q], hhq[q],
                           (int)hkv, (int)bb);
             else
-              tma_load_3d(sQ + q * q_bytes + pn * kBM * 128, &a.tmq, bar(kBarQ), pn * 64, (int)row0[q], (int)bh);
+              tma_load_3d(sQ + q * q_bytes + pn * a.q_rows * 128, &a.tmq, bar(kBarQ), pn * 64, (int)row0[q], (int)bh);
           }
       // one ring slot: wait until its previous tile is released, then load tile t into it
       auto load = [&](int full, int empty, uint32_t ring, uint32_t bytes, const CUtensorMap* tm1, int panels1,
@@ -722,17 +732,18 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), (tc_ctas_per_sm<BN, NQ, MM>(
       auto issue_s = [&](int t, int q, int slot) {
         const uint32_t dst = tmem + tS_col(slot);
         const uint64_t ad = qd0 + (uint64_t)(q * (q_bytes >> 4));
+        const uint32_t q_pan = (uint32_t)a.q_rows * 8;  // a Q panel in 16-byte units
         const uint64_t bd = kd0 + (uint64_t)((t % STG) * (k_bytes >> 4));
         if (a.ksteps_qk == kMaxKsteps) {
           // the head fills this variant: straight-line issue, no branch between MMAs (the
           // single issuing thread must keep pace with 64-cycle 128x128x16 MMAs)
 #pragma unroll
           for (int k = 0; k < kMaxKsteps; ++k)
-            mma_ss(dst, ad + (uint64_t)((k >> 2) * (kBM * 8) + (k & 3) * 2),
+            mma_ss(dst, ad + (uint64_t)((k >> 2) * q_pan + (k & 3) * 2),
                    bd + (uint64_t)((k >> 2) * (BN * 8) + (k & 3) * 2), idesc_s, k > 0);
         } else {
           for (int k = 0; k < a.ksteps_qk; ++k)
-            mma_ss(dst, ad + (uint64_t)((k >> 2) * (kBM * 8) + (k & 3) * 2),
+            mma_ss(dst, ad + (uint64_t)((k >> 2) * q_pan + (k & 3) * 2),
                    bd + (uint64_t)((k >> 2) * (BN * 8) + (k & 3) * 2), idesc_s, k > 0);
         }
         mma_commit(bar(kBarSFull + slot));
@@ -1117,7 +1128,13 @@ cudaError_t launch_tc_mm(int bn, int nq, int stg, const TcArgs& a, size_t smem, 
     return launch_tc_t<T, 64, 1, MM, 1>(a, smem, grid, st);
   } else {
     if (nq == 2) return stg == 2 ? launch_tc_t<T, 128, 2, MM, 2>(a, smem, grid, st) : cudaErrorInvalidValue;
-    if (bn == 64) return stg == 2 ? launch_tc_t<T, 64, 1, MM, 2>(a, smem, grid, st) : cudaErrorInvalidValue;
+    if (stg == 3 && bn != 64) return cudaErrorInvalidValue;
+    if (bn == 64) {
+      if constexpr (MM == kMmBounds) {
+        if (stg == 3) return launch_tc_t<T, 64, 1, MM, 3>(a, smem, grid, st);
+      }
+      return stg == 2 ? launch_tc_t<T, 64, 1, MM, 2>(a, smem, grid, st) : cudaErrorInvalidValue;
+    }
     return stg == 2 ? launch_tc_t<T, 128, 1, MM, 2>(a, smem, grid, st) : launch_tc_t<T, 128, 1, MM, 1>(a, smem, grid, st);
   }
 }
@@ -1129,9 +1146,10 @@ cudaError_t launch_tc_cfg(int bn, int nq, int stg, const TcArgs& a, size_t smem,
   return launch_tc_mm<T, kMmBounds>(bn, nq, stg, a, smem, grid, st);
 }
 
-size_t smem_need(int64_t d, int64_t dv, int bn, int nq, int stg) {
+size_t smem_need(int64_t d, int64_t dv, int bn, int nq, int stg, int q_rows = kBM, bool pad = true) {
   const int64_t dp = (d + 63) / 64, dvp = (dv + 63) / 64;
-  return (size_t)(nq * dp * kBM * 128 + stg * (dp + dvp) * bn * 128) + 1024 /*align*/ + 256 /*bars*/;
+  return (size_t)(nq * dp * q_rows * 128 + stg * (dp + dvp) * bn * 128) + (pad ? 1024 : 0) /*align*/ +
+         256 /*bars*/;
 }
 
 // The key tile and the depth of the K / V rings of the one-tile variant: the largest
@@ -1185,13 +1203,18 @@ PrefillGeom prefill_tc_geometry(int64_t B, int64_t Hkv, int64_t g, int64_t Lq, i
   PrefillGeom r{};
   if (nblk > 0) {
     // split-KV over nblk key blocks: one Q tile of packed rows per CTA and key block.
-    // Heads up to 128: 64-key tiles in two-stage rings and 256 TMEM columns, so that two
-    // CTAs -- two independent streams of keys -- share each SM; wider heads: the
-    // one-tile variant's own tiles, one CTA per SM.
-    const TileChoice tc = (d <= 128 && dv <= 128) ? TileChoice{64, 2} : tile_choice(d, dv);
+    // Heads up to 128: 64-key tiles and 256 TMEM columns, so that two CTAs -- two
+    // independent streams of keys -- share each SM, with three-stage rings where the rows
+    // fit a 64-row Q buffer (the two CTAs' shared memory then fits only unpadded), else
+    // two; wider heads: the one-tile variant's own tiles, one CTA per SM.
+    const bool small = d <= 128 && dv <= 128;
+    const bool q64 = small && g * Lq <= 64;
+    const TileChoice tc = small ? TileChoice{64, q64 ? 3 : 2} : tile_choice(d, dv);
     r.bn = tc.bn;
     r.stg = tc.stg;
-    r.tmem_cols = (d <= 128 && dv <= 128) ? 256 : 512;
+    r.tmem_cols = small ? 256 : 512;
+    r.q_rows = q64 ? 64 : kBM;
+    r.unpadded = q64 ? 1 : 0;
     r.nq = 1;
     r.head_local = 0;
     r.qo5 = 0;
@@ -1220,6 +1243,8 @@ PrefillGeom prefill_tc_geometry(int64_t B, int64_t Hkv, int64_t g, int64_t Lq, i
   r.n_rt = (G + kBM * r.nq - 1) / (kBM * r.nq);
   r.grid = r.head_local ? B * Hkv * (g / r.nq) * r.n_it : B * Hkv * r.n_rt;
   r.tmem_cols = kTmemCols;
+  r.q_rows = kBM;
+  r.unpadded = 0;
   return r;
 }
 
@@ -1238,8 +1263,10 @@ cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, b
   a.tmem_cols = geo.tmem_cols;
   const int bn = geo.bn, nq = geo.nq, stg = geo.stg;
   const size_t am_extra = p.mask_kind == kMaskAdd ? (size_t)am_bytes<64>() : 0;
-  if (!bn || !prefill_tc_bn(p.d, p.dv) || (int64_t)(smem_need(p.d, p.dv, bn, nq, stg) + am_extra) > kTcMaxSmem)
-    return cudaErrorInvalidValue;
+  const size_t need = smem_need(p.d, p.dv, bn, nq, stg, geo.q_rows, !geo.unpadded);
+  if (!bn || !prefill_tc_bn(p.d, p.dv) || (int64_t)(need + am_extra) > kTcMaxSmem) return cudaErrorInvalidValue;
+  a.q_rows = geo.q_rows;
+  a.unpadded = geo.unpadded;
   const int64_t BH = p.B * p.Hkv;
   // K and V as 4-D [B][Hkv][Lk][d] views with the caller's strides
   const int64_t kd[4] = {p.d, p.Lk, p.Hkv, p.B}, ks[3] = {p.k_sl, p.k_sh, p.k_sb};
@@ -1255,8 +1282,9 @@ cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, b
     a.tma_out = (out_fits && encode_tiled_16bit(&a.tmo, dtype, p.out, 5, od, os, kBM)) ? 1 : 0;
   } else {
     // the packed layout: [B*Hkv][G][D], the rows of one KV head contiguous
-    if (!encode_3d(&a.tmq, dtype, p.q, p.d, p.G, BH, kBM)) return cudaErrorInvalidValue;
-    a.tma_out = (out_fits && encode_3d(&a.tmo, dtype, p.out, p.dv, p.G, BH, kBM)) ? 1 : 0;
+    if (!encode_3d(&a.tmq, dtype, p.q, p.d, p.G, BH, geo.q_rows)) return cudaErrorInvalidValue;
+    // (the output tile is staged in the Q tile's buffer: a 64-row buffer is too small)
+    a.tma_out = (out_fits && geo.q_rows == kBM && encode_3d(&a.tmo, dtype, p.out, p.dv, p.G, BH, kBM)) ? 1 : 0;
   }
   a.n_rt = (int)geo.n_rt;
   a.n_it = (int)geo.n_it;
@@ -1283,8 +1311,7 @@ cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, b
   }
   const int64_t grid = geo.grid;
   // (two CTAs per SM: the ring and Q alone; otherwise at least 120 KB, one CTA per SM)
-  const size_t smem = (geo.tmem_cols == 256 ? smem_need(p.d, p.dv, bn, nq, stg)
-                                            : prefill_tc_smem_bytes(p.d, p.dv, bn, nq, stg)) + am_extra;
+  const size_t smem = (geo.tmem_cols == 256 ? need : prefill_tc_smem_bytes(p.d, p.dv, bn, nq, stg)) + am_extra;
   if (dtype == 1) return launch_tc_cfg<__half>(bn, nq, stg, a, smem, grid, st);
   return launch_tc_cfg<__nv_bfloat16>(bn, nq, stg, a, smem, grid, st);
 }
