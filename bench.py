@@ -285,25 +285,31 @@ def dist_env():
     return ws, rank, local
 
 
+def n_sets(touched_bytes):
+    """Device copies of a workload's inputs to rotate over, so that L2 holds nothing of a
+    call's inputs from an earlier call: at least six, and four times the L2 in all (the
+    keys and values of a decode are loaded with an evict-first L2 policy, and with only
+    two copies some lines of one survive the other's stream)."""
+    return max(6, math.ceil(4 * L2_BYTES / touched_bytes) + 1)
+
+
 def time_calls(torch, call, sets, steps, warmup, stream):
-    """Warm-up, then EXACTLY `steps` calls timed with CUDA events on `stream`; the
-    inputs rotate over `sets` so that L2 cannot hold a step's inputs from the last."""
+    """Warm-up, then EXACTLY `steps` calls back to back, timed by one pair of CUDA events on
+    `stream` around them (nothing else in the stream between calls, so each call's first
+    kernel may be placed while the previous call's last one drains, as in a serving loop);
+    the inputs rotate over `sets` so that L2 cannot hold a step's inputs from the last.
+    Returns (total ms, ms per call)."""
     for w in range(warmup):
         call(sets[w % len(sets)])
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
     for s in range(steps):
-        ev[s][0].record(stream)
         call(sets[s % len(sets)])
-        ev[s][1].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
     total_ms = start.elapsed_time(end)
-    launch_ms = [a.elapsed_time(b) for a, b in ev]
-    return total_ms, launch_ms
+    return total_ms, total_ms / steps
 
 
 def steady_ms(torch, call, sets, stream, windows=5, per_window=50):
@@ -385,14 +391,15 @@ def feature_lines(torch, nv, dev, stream, pk, pc, px, dc, dx, mc, mx, args):
             return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
-    def timed(call):
-        for _ in range(5):
-            call()
+    def timed(calls):
+        """ms per call: `calls` (one per input set) taken in turn, back to back."""
+        for i in range(5):
+            calls[i % len(calls)]()
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(steps):
-            call()
+        for i in range(steps):
+            calls[i % len(calls)]()
         b.record(stream)
         torch.cuda.synchronize()
         return a.elapsed_time(b) / steps
@@ -417,31 +424,39 @@ def feature_lines(torch, nv, dev, stream, pk, pc, px, dc, dx, mc, mx, args):
 
     out = {"steps": steps}
     q, k, v = (up(px[n], pc.dtype) for n in ("q", "k", "v"))
-    o = torch.empty((pc.B, pc.Hq, pc.Lq, pc.dv), dtype=q.dtype, device=dev)
+    pbytes = 2.0 * (q.numel() * 2 + k.numel() + v.numel())  # q, k, v read, out written
+    psets = [(q, k, v, torch.empty((pc.B, pc.Hq, pc.Lq, pc.dv), dtype=q.dtype, device=dev))]
+    psets += [tuple(t.clone() for t in psets[0]) for _ in range(n_sets(pbytes) - 1)]
+    out["input_sets"] = {"prefill": len(psets)}
     # causal sliding window on the 2x32/8 x 4096 prefill
     Wp = 1024
     fl = 2.0 * (pc.d + pc.dv) * pc.B * pc.Hq * window_pairs(pc.Lq, pc.Lk, Wp)
-    ms = timed(lambda: nv.sdpa(q, k, v, mask_kind="causal", scale=pc.scale_f32, window=Wp, out=o, want_lse=False))
+    ms = timed([lambda t=t: nv.sdpa(t[0], t[1], t[2], mask_kind="causal", scale=pc.scale_f32, window=Wp, out=t[3],
+                                    want_lse=False) for t in psets])
     out["window_prefill"] = tc_line(f"{pc.name}_window{Wp}", fl, ms)
     # every tensor a transposed [B, L, H, D] view (read and written in place)
     def tview(t):
         buf = torch.empty((t.shape[0], t.shape[2], t.shape[1], t.shape[3]), dtype=t.dtype, device=dev)
         buf.copy_(t.transpose(1, 2))
         return buf.transpose(1, 2)
-    qt, kt, vt, ot = tview(q), tview(k), tview(v), tview(o)
-    ms = timed(lambda: nv.sdpa(qt, kt, vt, mask_kind="causal", scale=pc.scale_f32, out=ot, want_lse=False))
+    psets = [tuple(tview(x) for x in t) for t in psets]
+    ms = timed([lambda t=t: nv.sdpa(t[0], t[1], t[2], mask_kind="causal", scale=pc.scale_f32, out=t[3],
+                                    want_lse=False) for t in psets])
     out["strided_prefill"] = tc_line(f"{pc.name}_bLhD_views", prefill_flops(pc), ms)
-    del q, k, v, o, qt, kt, vt, ot
+    del q, k, v, psets
     # additive mask [1, Hq, Lq, Lk] on the 16/2-head, 1024 x 1801, head-256 prefill
     mq, mk_, mv = (up(mx[n], mc.dtype) for n in ("q", "k", "v"))
     ms_ = up(mx["sinks"], mc.dtype)
     am = torch.randn((1, mc.Hq, mc.Lq, mc.Lk), dtype=mq.dtype, device=dev)
-    mo = torch.empty((mc.B, mc.Hq, mc.Lq, mc.dv), dtype=mq.dtype, device=dev)
-    ms = timed(lambda: nv.sdpa(mq, mk_, mv, mask_kind="add", scale=mc.scale_f32, add_mask=am, sinks=ms_,
-                               out=mo, want_lse=False))
+    asets = [(mq, mk_, mv, am, torch.empty((mc.B, mc.Hq, mc.Lq, mc.dv), dtype=mq.dtype, device=dev))]
+    abytes = 2.0 * (mq.numel() * 2 + mk_.numel() + mv.numel() + am.numel())
+    asets += [tuple(t.clone() for t in asets[0]) for _ in range(n_sets(abytes) - 1)]
+    out["input_sets"]["additive"] = len(asets)
+    ms = timed([lambda t=t: nv.sdpa(t[0], t[1], t[2], mask_kind="add", scale=mc.scale_f32, add_mask=t[3],
+                                    sinks=ms_, out=t[4], want_lse=False) for t in asets])
     out["additive_prefill"] = tc_line(mc.name.replace("bool", "additive"), prefill_flops(mc), ms,
                                       {"mask_bytes_per_call": am.numel() * 2})
-    del mq, mk_, mv, am, mo
+    del mq, mk_, mv, am, asets
     # decode with one sequence (the measured key split's case) and with 8 queries per sequence
     # and the pages' 256-wide decode shape (16/2 heads, one query over the same keys)
     for name, B1, Lq1, hd in (("decode_b1", 1, 1, None), ("decode_lq8", dc.B, 8, None),
@@ -451,21 +466,28 @@ def feature_lines(torch, nv, dev, stream, pk, pc, px, dc, dx, mc, mx, args):
             c1 = c1.with_(Hq=hd[0], Hkv=hd[1], d=hd[2], dv=hd[2])
         x1 = W.make_inputs(c1)
         q1, k1, v1, s1 = (up(x1[n], c1.dtype) for n in ("q", "k", "v", "sinks"))
-        o1 = torch.empty((c1.B, c1.Hq, c1.Lq, c1.dv), dtype=q1.dtype, device=dev)
-        ms = timed(lambda: nv.sdpa(q1, k1, v1, mask_kind="causal", scale=c1.scale_f32, sinks=s1, out=o1,
-                                   want_lse=False))
+        dsets = [(q1, k1, v1, torch.empty((c1.B, c1.Hq, c1.Lq, c1.dv), dtype=q1.dtype, device=dev))]
+        dsets += [tuple(t.clone() for t in dsets[0]) for _ in range(n_sets(kv_bytes(c1)) - 1)]
+        out["input_sets"][name] = len(dsets)
+        ms = timed([lambda t=t: nv.sdpa(t[0], t[1], t[2], mask_kind="causal", scale=c1.scale_f32, sinks=s1,
+                                        out=t[3], want_lse=False) for t in dsets])
         _, pl1 = nv.nv_sdpa_plan((c1.B, c1.Hq, c1.Hkv, c1.Lq, c1.Lk, c1.d, c1.dv), 1, 1, W.DTYPE_CODES[c1.dtype])
         out[name] = hbm_line(f"decode_f16_b{c1.B}_h{c1.Hq}x{c1.Hkv}_lq{c1.Lq}_lk32769_d{c1.d}_sinks", kv_bytes(c1), ms,
                              {"nblk": pl1["nblk"], "keys_per_blk": pl1["keys_per_blk"], "kernel": pl1["kernel"]})
-        del q1, k1, v1, o1
+        del q1, k1, v1, dsets
     # decode: a window of 4096 over the 32769 keys, and the keys in a paged cache
     dq, dk, dv_ = (up(dx[n], dc.dtype) for n in ("q", "k", "v"))
     dsk = up(dx["sinks"], dc.dtype)
     do = torch.empty((dc.B, dc.Hq, dc.Lq, dc.dv), dtype=dq.dtype, device=dev)
     Wd = 4096
-    ms = timed(lambda: nv.sdpa(dq, dk, dv_, mask_kind="causal", scale=dc.scale_f32, window=Wd, sinks=dsk, out=do,
-                               want_lse=False))
-    out["window_decode"] = hbm_line(f"{dc.name}_window{Wd}", dc.B * dc.Hkv * Wd * (dc.d + dc.dv) * 2.0, ms)
+    wbytes = dc.B * dc.Hkv * Wd * (dc.d + dc.dv) * 2.0
+    wsets = [(dq, dk, dv_, do)] + [(dq.clone(), dk.clone(), dv_.clone(), torch.empty_like(do))
+                                   for _ in range(n_sets(wbytes) - 1)]
+    out["input_sets"]["window_decode"] = len(wsets)
+    ms = timed([lambda t=t: nv.sdpa(t[0], t[1], t[2], mask_kind="causal", scale=dc.scale_f32, window=Wd, sinks=dsk,
+                                    out=t[3], want_lse=False) for t in wsets])
+    out["window_decode"] = hbm_line(f"{dc.name}_window{Wd}", wbytes, ms)
+    del wsets
     bs = 16
     per = -(-dc.Lk // bs)
     nblocks = dc.B * per + 7
@@ -482,13 +504,15 @@ def feature_lines(torch, nv, dev, stream, pk, pc, px, dc, dx, mc, mx, args):
     del dk, dv_
     table = order.view(dc.B, per).to(torch.int32).contiguous()
     lens = torch.full((dc.B,), dc.Lk, dtype=torch.int32, device=dev)
-    ms = timed(lambda: nv.sdpa_paged(dq, kc, vc, table, lens, mask_kind="causal", scale=dc.scale_f32, sinks=dsk,
-                                     out=do, want_lse=False))
+    gsets = [(kc, vc, do)] + [(kc.clone(), vc.clone(), torch.empty_like(do)) for _ in range(n_sets(kv_bytes(dc)) - 1)]
+    out["input_sets"]["paged_decode"] = len(gsets)
+    ms = timed([lambda t=t: nv.sdpa_paged(dq, t[0], t[1], table, lens, mask_kind="causal", scale=dc.scale_f32,
+                                          sinks=dsk, out=t[2], want_lse=False) for t in gsets])
     _, ppl = nv.nv_sdpa_paged_plan((dc.B, dc.Hq, dc.Hkv, 1, dc.d, dc.dv, nblocks, bs, per), 1, 0, 0, 1,
                                    W.DTYPE_CODES[dc.dtype])
     out["paged_decode"] = hbm_line(f"{dc.name}_paged_bs{bs}", kv_bytes(dc), ms,
-                                   {"block_size": bs, "nblk": ppl["nblk"], "loads": "16-byte cp.async per key row"})
-    del kc, vc, dq, do
+                                   {"block_size": bs, "nblk": ppl["nblk"], "loads": "TMA boxes of one block's rows"})
+    del kc, vc, dq, do, gsets
     torch.cuda.synchronize()
     return out
 
@@ -550,7 +574,7 @@ def run_ours(args):
         e = W.ELT_BYTES[case.dtype]
         return (n["q"] + n["k"] + n["v"] + n["out"]) * e + n["lse"] * 4
 
-    psets = device_sets(pc, px, max(2, math.ceil(2 * L2_BYTES / set_bytes(pc)) + 1))
+    psets = device_sets(pc, px, n_sets(set_bytes(pc)))
     st_, pplan = nv.nv_sdpa_plan((pc.B, pc.Hq, pc.Hkv, pc.Lq, pc.Lk, pc.d, pc.dv),
                                  W.MASK_CODES[pc.mask], 0, W.DTYPE_CODES[pc.dtype])
     pcall = caller(pc)
@@ -571,7 +595,7 @@ def run_ours(args):
     total_ms_max = max_over_ranks(torch, pg, total_ms, dev)
     flops_step = prefill_flops(pc)
     value = whole_job_rate(ws, flops_step, args.steps, total_ms_max / 1e3)
-    launch_avg = statistics.mean(launch_ms)
+    launch_avg = launch_ms
     p_steady = steady_ms(torch, pcall, psets, stream)
     peak_t = pk["bf16_tflops"]
     p_achieved = flops_step / (launch_avg / 1e3) / 1e12
@@ -580,23 +604,24 @@ def run_ours(args):
     # --------------------------------------------------------------- decode (secondary)
     dc = W.decode_f16_long_kv()
     dx = W.make_inputs(dc)
-    dsets = device_sets(dc, dx, 2)
+    dsets = device_sets(dc, dx, n_sets(set_bytes(dc)))
     _, dplan = nv.nv_sdpa_plan((dc.B, dc.Hq, dc.Hkv, dc.Lq, dc.Lk, dc.d, dc.dv),
                                W.MASK_CODES[dc.mask], 1, W.DTYPE_CODES[dc.dtype])
     dsteps = max(args.steps, 50)
     d_total, d_launch = time_calls(torch, caller(dc), dsets, dsteps, max(args.warmup, 3), stream)
     dbytes = kv_bytes(dc)
-    d_call_avg = statistics.mean(d_launch)
+    d_call_avg = d_launch
     d_gbs = dbytes / (d_call_avg / 1e3) / 1e9
     decode = {
         "workload": dc.name, "metric": "decode KV GB/s", "value": round(d_gbs, 1), "unit": "GB/s",
         "ms_per_call": round(d_call_avg, 5), "steps": dsteps, "kernel": dplan["kernel"],
+        "l2": f"inputs rotate over {len(dsets)} device copies",
         "nblk": dplan["nblk"], "launches_per_call": dplan["launches"],
         "roofline": {"bound": "hbm", "achieved": round(d_gbs, 1), "peak": pk["hbm_gbs"],
                      "unit": "GB/s", "frac": round(d_gbs / pk["hbm_gbs"], 4),
                      "peak_source": pk_src + " hbm_gbs (copy)",
                      "vs_nominal": vs_nominal(d_gbs, "hbm_gbs"),
-                     "timed": "whole call (pass 1 + merge) per CUDA-event pair",
+                     "timed": "whole calls (pass 1 + merge), back to back, CUDA events around the region",
                      "traffic": recorded_traffic("decode:" + dc.name)},
         "algorithmic_bytes_per_call": dbytes,
     }
@@ -604,13 +629,13 @@ def run_ours(args):
     # --------------------------------------------------------------- boolean mask + sinks, head 256
     mc = W.prefill_f16_boolmask_sinks()
     mx = W.make_inputs(mc)
-    msets = device_sets(mc, mx, max(2, math.ceil(2 * L2_BYTES / set_bytes(mc)) + 1))
+    msets = device_sets(mc, mx, n_sets(set_bytes(mc)))
     _, mplan = nv.nv_sdpa_plan((mc.B, mc.Hq, mc.Hkv, mc.Lq, mc.Lk, mc.d, mc.dv),
                                W.MASK_CODES[mc.mask], 1, W.DTYPE_CODES[mc.dtype])
     msteps = max(args.steps, 50)
     _, m_launch = time_calls(torch, caller(mc), msets, msteps, max(args.warmup, 3), stream)
     mflops = prefill_flops(mc)  # dense: a boolean mask is not halved
-    m_call_avg = statistics.mean(m_launch)
+    m_call_avg = m_launch
     m_tf = mflops / (m_call_avg / 1e3) / 1e12
     prefill_mask = {
         "workload": mc.name, "metric": "prefill attention TFLOP/s", "value": round(m_tf, 2),
@@ -622,7 +647,7 @@ def run_ours(args):
                      "unit": "TFLOP/s", "frac": round(m_tf / pk["bf16_tflops"], 4),
                      "peak_source": pk_src + " bf16_tflops (f16 runs at the bf16 rate)",
                      "vs_nominal": vs_nominal(m_tf, "bf16_tflops"),
-                     "timed": "whole call (mask packing + attention) per CUDA-event pair",
+                     "timed": "whole calls (mask packing + attention), back to back, CUDA events around the region",
                      "traffic": recorded_traffic("prefill:" + mc.name)},
     }
 
@@ -683,19 +708,21 @@ def run_ours(args):
                    "Lk": pc.Lk, "d": pc.d, "dv": pc.dv, "mask": pc.mask,
                    "flops_per_step": flops_step, "kernel": pkernel,
                    "l2": f"inputs rotate over {len(psets)} device copies "
-                         f"({len(psets) * set_bytes(pc) / 2**20:.0f} MiB > 2x the 129 MB L2)",
+                         f"({len(psets) * set_bytes(pc) / 2**20:.0f} MiB > 4x the 129 MB L2)",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU"},
         "roofline": {"bound": "tensor", "achieved": round(p_achieved, 2), "peak": peak_t,
                      "unit": "TFLOP/s", "frac": round(p_achieved / peak_t, 4),
                      "peak_source": pk_src + " bf16_tflops (burst, cuBLAS)",
                      "vs_nominal": vs_nominal(p_achieved, "bf16_tflops"),
                      "kernel_ms": round(launch_avg, 5),
+                     "timed": "one launch per step, back to back, CUDA events around the region",
                      "steady_ms_per_call": p_steady[0], "steady_windows_ms": p_steady[1],
                      "traffic": recorded_traffic("prefill:" + pc.name)},
         "decode": decode,
         "prefill_mask": prefill_mask,
         "features": features,
         "sweep": sweep,
+        "sweep_inputs": "one device copy per case: the small parity cases run from L2",
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "api": "nv_sdpa_host (pinned host buffers; copies, device alloc, sync inside)"},

@@ -126,7 +126,9 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + a.wpc * ST * stage_bytes);
   auto full = [&](int s) { return smem_addr(bars + warp * ST + s); };
 
-  // the merge pass may be scheduled once every CTA of this grid is running
+  // the stream's previous kernel has finished before any global access; the merge pass
+  // may be scheduled once every CTA of this grid is running
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.wpc * ST; ++i) mbar_init(smem_addr(bars + i), 1);
@@ -183,6 +185,7 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
   // tile i of the run into ring slot i % ST (called by every lane): by TMA from lane 0,
   // or (kKvPagedRows) by 16-byte copies of every lane, key row by key row through the page
   // table, rows outside [key_begin, key_end) and columns past the head zero-filled
+  const uint64_t l2_once = l2_policy_evict_first();  // each key and value is read once
   const T* kg = reinterpret_cast<const T*>(p.k);
   const T* vg = reinterpret_cast<const T*>(p.v);
   auto issue = [&](int i) {
@@ -192,10 +195,11 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
       if (lane == 0) {
         mbar_arrive_expect_tx(full(s), stage_bytes);
         for (int pn = 0; pn < a.dpanels; ++pn)
-          tma_load_4d(ring + s * stage_bytes + pn * kKT * 128, &a.tmk, full(s), pn * 64, (int)key0, (int)hkv, (int)b);
+          tma_load_4d_hint(ring + s * stage_bytes + pn * kKT * 128, &a.tmk, full(s), pn * 64, (int)key0, (int)hkv,
+                           (int)b, l2_once);
         for (int pn = 0; pn < a.dvpanels; ++pn)
-          tma_load_4d(ring + s * stage_bytes + k_bytes + pn * kKT * 128, &a.tmv, full(s), pn * 64, (int)key0,
-                      (int)hkv, (int)b);
+          tma_load_4d_hint(ring + s * stage_bytes + k_bytes + pn * kKT * 128, &a.tmv, full(s), pn * 64, (int)key0,
+                           (int)hkv, (int)b, l2_once);
       }
     } else if constexpr (KV == kKvPagedTma) {
       const int R = a.sub_rows;
@@ -206,11 +210,11 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
         const int pos = (int)(kk % p.page);
         if (lane == 0) {
           for (int pn = 0; pn < a.dpanels; ++pn)
-            tma_load_4d(ring + s * stage_bytes + pn * kKT * 128 + u * R * 128, &a.tmk, full(s), pn * 64, pos,
-                        (int)hkv, blk);
+            tma_load_4d_hint(ring + s * stage_bytes + pn * kKT * 128 + u * R * 128, &a.tmk, full(s), pn * 64, pos,
+                             (int)hkv, blk, l2_once);
           for (int pn = 0; pn < a.dvpanels; ++pn)
-            tma_load_4d(ring + s * stage_bytes + k_bytes + pn * kKT * 128 + u * R * 128, &a.tmv, full(s), pn * 64,
-                        pos, (int)hkv, blk);
+            tma_load_4d_hint(ring + s * stage_bytes + k_bytes + pn * kKT * 128 + u * R * 128, &a.tmv, full(s),
+                             pn * 64, pos, (int)hkv, blk, l2_once);
         }
       }
     } else {
@@ -634,8 +638,8 @@ cudaError_t launch_dec_t(const DecArgs& a, int64_t grid, cudaStream_t st) {
   if (a.wpc < 1 || a.wpc > Sh::WPC) return cudaErrorInvalidValue;
   constexpr int ST = Sh::ST;
   const int smem = a.wpc * ST * Sh::kStageBytes + 1024 + a.wpc * ST * 8 + 64;  // (Sh::kSmem at WPC warps)
-  sdpa_decode_mma<T, DMAX, DV, KV, SW><<<(unsigned)grid, a.wpc * 32, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_dependent(sdpa_decode_mma<T, DMAX, DV, KV, SW>, dim3((unsigned)grid), dim3(a.wpc * 32), (size_t)smem,
+                          st, a);
 }
 
 // (d, dv) buckets with a kernel: the smallest bucket covering the head is used; the

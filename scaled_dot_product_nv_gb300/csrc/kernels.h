@@ -27,6 +27,29 @@ bool encode_3d(CUtensorMap* m, int dtype, const void* ptr, int64_t inner, int64_
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per device (thread-safe bitmask).
 cudaError_t set_max_dynamic_smem_once(std::atomic<unsigned long long>& configured, const void* fn, int bytes);
 
+// Every kernel of the library is launched as the programmatic dependent of the stream's
+// previous kernel: its CTAs may be placed while that kernel's last CTAs run, once all of
+// them have signalled (griddepcontrol.launch_dependents), or have exited.  Each kernel
+// executes griddepcontrol.wait -- which returns once the previous grid has finished and
+// its writes are visible -- before it reads or writes global memory or takes TMEM, so
+// the order of the stream's results is that of plain launches; only the launch latency
+// and the CTAs' set-up overlap the previous kernel's tail.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // tiled_simt.cu
 size_t tiled_simt_smem_bytes(int64_t d, int64_t dv);
 int64_t tiled_simt_rows_per_cta();

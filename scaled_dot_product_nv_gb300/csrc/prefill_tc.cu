@@ -605,6 +605,13 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), (tc_ctas_per_sm<BN, NQ, MM>(
   for (int q = 0; q < NQ; ++q) n_max = n_q[q] > n_max ? n_q[q] : n_max;
 
   // ---- set-up: barriers, TMEM
+  // Launched as the programmatic dependent of the stream's previous kernel: nothing
+  // global is read or written, and no TMEM is taken, before that kernel has finished
+  // (an early CTA holding TMEM could starve one of the previous grid's on the same SM).
+  // With a boolean mask the previous kernel is the mask packing, which itself waited
+  // for everything before it: the copies of Q, K and V may start at once, and the
+  // softmax warps wait for the bits alone.
+  if constexpr (MM != kMmBits) asm volatile("griddepcontrol.wait;" ::: "memory");
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQ), 1);
     for (int s = 0; s < STG; ++s) {
@@ -630,6 +637,9 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), (tc_ctas_per_sm<BN, NQ, MM>(
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The next kernel of the stream (the merge pass, or the next call) may now place its
+  // CTAs as SMs free up; each waits there for this grid to finish.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
   const uint64_t limit = p.wait_limit;
   // TMEM columns: S slot b at b*BN (NQ = 1: the two buffers; NQ = 2: one per Q tile);
@@ -658,6 +668,9 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), (tc_ctas_per_sm<BN, NQ, MM>(
             else
               tma_load_3d(sQ + q * q_bytes + pn * a.q_rows * 128, &a.tmq, bar(kBarQ), pn * 64, (int)row0[q], (int)bh);
           }
+      // A split call reads each key block once, for every row it holds: its keys and
+      // values go first out of L2, before the partials the merge pass reads back.
+      const uint64_t l2_once = l2_policy_evict_first();
       // one ring slot: wait until its previous tile is released, then load tile t into it
       auto load = [&](int full, int empty, uint32_t ring, uint32_t bytes, const CUtensorMap* tm1, int panels1,
                       uint32_t ring2, const CUtensorMap* tm2, int panels2, int t) {
@@ -667,12 +680,20 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), (tc_ctas_per_sm<BN, NQ, MM>(
           return false;
         }
         mbar_arrive_expect_tx(bar(full + s), bytes);
-        for (int pn = 0; pn < panels1; ++pn)
-          tma_load_4d(ring + s * (panels1 * BN * 128) + pn * BN * 128, tm1, bar(full + s), pn * 64, (kt0 + t) * BN,
-                      (int)hkv, (int)bb);
-        for (int pn = 0; pn < panels2; ++pn)
-          tma_load_4d(ring2 + s * (panels2 * BN * 128) + pn * BN * 128, tm2, bar(full + s), pn * 64, (kt0 + t) * BN,
-                      (int)hkv, (int)bb);
+        for (int pn = 0; pn < panels1; ++pn) {
+          const uint32_t dst = ring + s * (panels1 * BN * 128) + pn * BN * 128;
+          if (a.split)
+            tma_load_4d_hint(dst, tm1, bar(full + s), pn * 64, (kt0 + t) * BN, (int)hkv, (int)bb, l2_once);
+          else
+            tma_load_4d(dst, tm1, bar(full + s), pn * 64, (kt0 + t) * BN, (int)hkv, (int)bb);
+        }
+        for (int pn = 0; pn < panels2; ++pn) {
+          const uint32_t dst = ring2 + s * (panels2 * BN * 128) + pn * BN * 128;
+          if (a.split)
+            tma_load_4d_hint(dst, tm2, bar(full + s), pn * 64, (kt0 + t) * BN, (int)hkv, (int)bb, l2_once);
+          else
+            tma_load_4d(dst, tm2, bar(full + s), pn * 64, (kt0 + t) * BN, (int)hkv, (int)bb);
+        }
         return true;
       };
       int k_issued = 0, v_issued = 0;
@@ -1072,6 +1093,10 @@ constexpr int kPackWarps = 8;
 __global__ void __launch_bounds__(kPackWarps * 32)
 sdpa_pack_mask_bits(const uint8_t* __restrict__ mask, int64_t Lq, int64_t Lk, int64_t words,
                     uint32_t* __restrict__ bits) {
+  // the stream's previous kernel has finished (and its writes are visible) before the
+  // mask is read and before the attention kernel may launch: that kernel copies Q, K
+  // and V without a wait of its own
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   const int lane = threadIdx.x & 31;
   const int64_t quads = words / 4;  // words per row is a multiple of 4
@@ -1098,26 +1123,11 @@ cudaError_t launch_tc_t(const TcArgs& a, size_t smem, int64_t grid, cudaStream_t
   cudaError_t e =
       set_max_dynamic_smem_once(configured, (const void*)sdpa_prefill_tc<T, BN, NQ, MM, STG>, (int)kTcMaxSmem);
   if (e != cudaSuccess) return e;
-  if constexpr (MM == kMmBits) {
-    // behind the mask packing, as its programmatic dependent: the prologue, the Q loads and
-    // the first products overlap the packing, and the softmax warps wait for its bits.
-    // (The packing itself was launched in stream order, so every earlier write of the
-    // stream -- q, k, v included -- is complete before this kernel can start.)
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(tc_threads<NQ>());
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, sdpa_prefill_tc<T, BN, NQ, MM, STG>, a);
-  } else {
-    sdpa_prefill_tc<T, BN, NQ, MM, STG><<<(unsigned)grid, tc_threads<NQ>(), smem, st>>>(a);
-    return cudaGetLastError();
-  }
+  // (with a boolean mask: behind the mask packing, whose grid waited for the stream's
+  // earlier work; the prologue, the Q loads and the first products overlap the packing,
+  // and the softmax warps wait for its bits)
+  return launch_dependent(sdpa_prefill_tc<T, BN, NQ, MM, STG>, dim3((unsigned)grid), dim3(tc_threads<NQ>()), smem,
+                          st, a);
 }
 
 template <typename T, int MM>
@@ -1304,9 +1314,8 @@ cudaError_t launch_prefill_tc(int dtype, const Params& p, uint32_t* mask_bits, b
     int64_t g = (n + kPackWarps - 1) / kPackWarps;
     const int64_t cap = (int64_t)device_sm_count() * 8;
     if (g > cap) g = cap;
-    sdpa_pack_mask_bits<<<(unsigned)(g > 0 ? g : 1), kPackWarps * 32, 0, st>>>(p.mask, p.Lq, p.Lk, a.mask_words,
-                                                                               mask_bits);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_dependent(sdpa_pack_mask_bits, dim3((unsigned)(g > 0 ? g : 1)), dim3(kPackWarps * 32), 0,
+                                     st, p.mask, p.Lq, p.Lk, a.mask_words, mask_bits);
     if (e != cudaSuccess) return e;
   }
   const int64_t grid = geo.grid;

@@ -132,6 +132,24 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* desc, uint
       "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
+// An L2 policy that marks the lines it touches as the first to evict: for data read
+// exactly once (a decode's keys and values), so that it does not push out lines written
+// for a later pass (the split-KV partials).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// The 4-D load with an L2 cache policy (from createpolicy).
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const void* desc, uint32_t bar, int c0,
+                                                 int c1, int c2, int c3, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(pol)
+      : "memory");
+}
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* desc, uint32_t bar, int c0,
                                             int c1, int c2, int c3, int c4) {
   asm volatile(

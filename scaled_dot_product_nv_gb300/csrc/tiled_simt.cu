@@ -39,7 +39,9 @@ sdpa_tiled_simt(const Params p) {
   float* red_sum = red_max + 4 * 32;          // [4][32]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // the merge pass may be scheduled once every CTA of this grid is running
+  // the stream's previous kernel has finished before any global access; the merge pass
+  // (or the next call) may be scheduled once every CTA of this grid is running
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   int64_t x = blockIdx.x;
   const int64_t rt = x % p.row_tiles; x /= p.row_tiles;
@@ -215,6 +217,7 @@ sdpa_merge_partials(const Params p) {
   __shared__ float red[kMergeWarps];
   __shared__ float part[kMergeWarps][256 + 1];  // per-warp partial sums of one row, + L
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");  // (the next call's set-up may overlap)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t row = blockIdx.x;
   const int64_t h = (row / p.Lq) % p.Hq;
@@ -294,6 +297,8 @@ sdpa_merge_partials(const Params p) {
 // Lk == 0: every row sees no key.  out = 0; lse = the sink, or -inf without sinks.
 template <typename T>
 __global__ void sdpa_fill_no_keys(const Params p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   const int64_t rows = p.B * p.Hq * p.Lq;
   const int64_t n = rows * p.dv;
   T* out = reinterpret_cast<T*>(p.out);
@@ -315,25 +320,14 @@ cudaError_t launch_simt_t(const Params& p, cudaStream_t st) {
                                             (int)tiled_simt_smem_bytes(256, 256));
   if (e != cudaSuccess) return e;
   const int64_t grid = p.B * p.Hkv * p.nblk * p.row_tiles;
-  sdpa_tiled_simt<T><<<(unsigned)grid, kThreads, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(sdpa_tiled_simt<T>, dim3((unsigned)grid), dim3(kThreads), smem, st, p);
 }
 
 template <typename T>
 cudaError_t launch_merge_t(const Params& p, cudaStream_t st) {
   const int64_t rows = p.B * p.Hq * p.Lq;
-  // programmatic dependent launch: the merge grid is set up while pass 1 drains
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)rows);
-  cfg.blockDim = dim3(kMergeWarps * 32);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, sdpa_merge_partials<T>, p);
+  // (its grid is set up while pass 1 drains)
+  return launch_dependent(sdpa_merge_partials<T>, dim3((unsigned)rows), dim3(kMergeWarps * 32), 0, st, p);
 }
 
 template <typename T>
@@ -343,8 +337,7 @@ cudaError_t launch_fill_t(const Params& p, cudaStream_t st) {
   const int64_t cap = (int64_t)device_sm_count() * 16;
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
-  sdpa_fill_no_keys<T><<<(unsigned)grid, 256, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(sdpa_fill_no_keys<T>, dim3((unsigned)grid), dim3(256), 0, st, p);
 }
 
 }  // namespace
