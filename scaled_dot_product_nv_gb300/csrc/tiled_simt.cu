@@ -294,6 +294,76 @@ sdpa_merge_partials(const Params p) {
   if (threadIdx.x == 0 && p.lse) p.lse[row] = (M + log2f(Lt)) * kLn2;
 }
 
+// Pass 2 for few key blocks (nblk <= kWarpMergeMax): one warp per query row, eight rows
+// per CTA, the same sums as above.  Lane k (< nblk) loads block k's (m, l); every lane
+// loads its four columns of each 128-column group from every block; all of these loads
+// are in flight together, so a row costs one trip to memory, and no CTA barrier is
+// needed.
+constexpr int kWarpMergeMax = 16;
+
+template <typename T>
+__global__ void __launch_bounds__(kMergeWarps * 32)
+sdpa_merge_partials_warp(const Params p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");  // (the next call's set-up may overlap)
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = p.B * p.Hq * p.Lq;
+  const int64_t row = (int64_t)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int64_t h = (row / p.Lq) % p.Hq;
+  const int nb = (int)p.nblk;
+  const int dv = (int)p.dv;
+  const float* ml = p.part_ml + row * p.nblk * 2;
+  const float* po = p.part_o + row * p.nblk * p.dv;
+  const float mk = lane < nb ? ml[2 * lane] : -INFINITY;
+  const float lk = lane < nb ? ml[2 * lane + 1] : 0.f;
+  float4 o[2][kWarpMergeMax];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int c0 = j * 128 + lane * 4;
+#pragma unroll
+    for (int k = 0; k < kWarpMergeMax; ++k)
+      o[j][k] = (k < nb && c0 < dv) ? *reinterpret_cast<const float4*>(po + (int64_t)k * p.dv + c0)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  const float sk = sink_log2<T>(p, h);
+  float M = fmaxf(mk, sk);
+#pragma unroll
+  for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  T* orow = reinterpret_cast<T*>(p.out) + o_offset(p, row / (p.Lq * p.Hq), h, row % p.Lq);
+  if (M == -INFINITY) {
+    for (int c = lane; c < dv; c += 32) orow[c] = from_f32<T>(0.f);
+    if (lane == 0 && p.lse) p.lse[row] = -INFINITY;
+    return;
+  }
+  const float w = (mk == -INFINITY) ? 0.f : ex2(mk - M);  // block lane's weight
+  float L = lk * w;
+#pragma unroll
+  for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  L += ex2(sk - M);
+  const float inv = 1.f / L;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kWarpMergeMax; ++k) {
+      const float wk = __shfl_sync(0xffffffffu, w, k);  // 0 past nblk
+      acc.x = fmaf(o[j][k].x, wk, acc.x);
+      acc.y = fmaf(o[j][k].y, wk, acc.y);
+      acc.z = fmaf(o[j][k].z, wk, acc.z);
+      acc.w = fmaf(o[j][k].w, wk, acc.w);
+    }
+    const int c0 = j * 128 + lane * 4;
+    if (c0 < dv) {
+      orow[c0] = from_f32<T>(acc.x * inv);
+      orow[c0 + 1] = from_f32<T>(acc.y * inv);
+      orow[c0 + 2] = from_f32<T>(acc.z * inv);
+      orow[c0 + 3] = from_f32<T>(acc.w * inv);
+    }
+  }
+  if (lane == 0 && p.lse) p.lse[row] = (M + log2f(L)) * kLn2;
+}
+
 // Lk == 0: every row sees no key.  out = 0; lse = the sink, or -inf without sinks.
 template <typename T>
 __global__ void sdpa_fill_no_keys(const Params p) {
@@ -327,6 +397,9 @@ template <typename T>
 cudaError_t launch_merge_t(const Params& p, cudaStream_t st) {
   const int64_t rows = p.B * p.Hq * p.Lq;
   // (its grid is set up while pass 1 drains)
+  if (p.nblk <= kWarpMergeMax && p.dv <= 256)
+    return launch_dependent(sdpa_merge_partials_warp<T>, dim3((unsigned)((rows + kMergeWarps - 1) / kMergeWarps)),
+                            dim3(kMergeWarps * 32), 0, st, p);
   return launch_dependent(sdpa_merge_partials<T>, dim3((unsigned)rows), dim3(kMergeWarps * 32), 0, st, p);
 }
 
