@@ -18,7 +18,11 @@
  * All entry points are plain C.  Device pointers are CUDA device addresses of the
  * current device; `stream` is a cudaStream_t (NULL = the legacy default stream).
  * Every call is asynchronous with respect to the host, like a kernel launch, unless
- * stated otherwise.  No entry point ever falls back to the CPU.
+ * stated otherwise.  No entry point ever falls back to the CPU.  A call's kernels are
+ * launched as programmatic dependents of the stream's previous kernel: their CTAs may
+ * be placed while that kernel finishes, but each waits for it to complete (its writes
+ * visible) before reading or writing any of the call's buffers, so stream order holds
+ * as for plain launches.
  *
  * Layouts (all contiguous, row-major, element type = `dtype`):
  *   q    [B, Hq,  Lq, d ]        k [B, Hkv, Lk, d]        v [B, Hkv, Lk, dv]
