@@ -176,12 +176,14 @@ __host__ __device__ constexpr int av_words() { return MM == kMmAdd ? BN / 2 : 1;
 // tO: TMEM addresses (lane base included) of this tile's S columns and of O; the row
 // sees keys [first_key, last_key]; mrow: its mask row (MM = kMmBits: bit-packed words,
 // kMmAdd: unused; the tile's additive values are in av), unused otherwise.  PF: the tile's
-// words were loaded ahead by the caller into mw.  Returns false if a wait gave up.
+// words were loaded ahead by the caller into mw.  wait_pv: O may still be receiving
+// P_{t-1} V_{t-1} (the one-tile variant), so a rescale waits for it on pv_bar; last: the
+// walk's last tile, which waits in any case.  Returns false if a wait gave up.
 template <typename T, int BN, int NQ, int MM, bool PF>
 __device__ __forceinline__ bool softmax_tile(const TcArgs& a, int t, int kt, uint32_t tS, uint32_t tO,
                                              bool row_ok, int first_key, int last_key, const void* mrow_any,
                                              const uint32_t (&mw)[BN / 32], const uint32_t (&av)[av_words<BN, MM>()],
-                                             float& m_run, float& l_run, uint32_t pv_bar, bool wait_pv,
+                                             float& m_run, float& l_run, uint32_t pv_bar, bool wait_pv, bool last,
                                              uint64_t limit, volatile int* abort) {
   const Params& p = a.p;
   const uint32_t* mrow = static_cast<const uint32_t*>(mrow_any);
@@ -311,15 +313,18 @@ __device__ __forceinline__ bool softmax_tile(const TcArgs& a, int t, int kt, uin
     else masked_tile(std::false_type{});
   }
   tmem_st_wait();
-  if (t > 0 && wait_pv) {
-    // Wait for P_{t-1} V_{t-1} on every tile, rescale or not.  The wait tests a phase
-    // parity, so this thread must never fall two phases behind pv_done: here the newest
-    // completed phase is at most t-1 (P_t is not released yet) and, because tile t-1
-    // waited for phase t-2, at least t-2.  O is then stable for the rescale.
+  const bool rescale = t > 0 && __any_sync(0xffffffffu, need);
+  if (t > 0 && wait_pv && (rescale || last)) {
+    // O is rescaled only once P_{t-1} V_{t-1} has landed in it.  The wait tests a phase
+    // parity, which is exact while the newest completed phase of pv_done is t-2 or t-1:
+    // it is at most t-1 (P_t is not released yet), and at least t-2 because S_t, whose
+    // completion this thread has seen, was issued after P_{t-2} V_{t-2} and its commit
+    // tracks every earlier MMA -- so tiles that need no rescale skip the wait.  The last
+    // tile waits all the same: the epilogue's wait for the last P V is then exact too.
     if (!__all_sync(0xffffffffu, mbar_wait(pv_bar, (t - 1) & 1, limit, abort))) return false;
     tc_fence_after();
   }
-  if (t > 0 && __any_sync(0xffffffffu, need)) {
+  if (rescale) {
     for (int c = 0; c < (a.n_pv + 31) / 32; ++c) {
       uint32_t o[32];
       tmem_ld32_sync(tO + c * 32, o);
@@ -901,7 +906,7 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), (tc_ctas_per_sm<BN, NQ, MM>(
         uint32_t no_add[av_words<BN, MM>()];  // (additive masks take the one-tile variant)
         ok = softmax_tile<T, BN, NQ, MM, false>(a, t, kt0 + t, tmem + lane_base + tS_col(q), tO, row_ok, first_key,
                                             last_key, mrow_any, no_words, no_add, m_run, l_run, bar(kBarPvDone + q),
-                                            false, limit, abort);
+                                            false, false, limit, abort);
         if (!ok) {
           fail(p, abort, kStatTimeoutMma);
           break;
@@ -1002,7 +1007,7 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), (tc_ctas_per_sm<BN, NQ, MM>(
         // S_t was issued before P_{t-1} V_{t-1}: the softmax waits for that product
         ok = softmax_tile<T, BN, NQ, MM, true>(a, t, kt0 + t, tmem + lane_base + tS_col(slot), tO, row_ok, first_key,
                                            last_key, mrow_any, mw, av, m_run, l_run, bar(kBarPvDone + q), true,
-                                           limit, abort);
+                                           t + 1 == n_tiles, limit, abort);
         if (!ok) {
           fail(p, abort, kStatTimeoutMma);
           break;
