@@ -815,10 +815,12 @@ NV_SDPA_API int nv_sdpa_host(const void* q, const void* k, const void* v, const 
   if (use_mask) h2d(om, bool_mask, nm);
   if (use_sinks) h2d(os, sinks, ns);
   const int64_t g = x.Hq / x.Hkv;
-  // Enqueue order: in(c), attention(c), out(c - 2), ...  A copy here can hold the host
+  // Enqueue order: in(c), attention(c), out(c), ...  A copy here can hold the host
   // until it is done (measured: queueing every copy in first left the first run's
-  // attention waiting for the last copy in), so each run's attention is queued right
-  // behind its inputs, and its copies out two runs later, while later copies proceed.
+  // attention waiting for the last copy in), so each run's attention and copies out are
+  // queued right behind its inputs; the copies out then overlap the next runs' copies in
+  // (queued two runs later they had started late and left three runs' outputs to drain
+  // after the last attention: 0.857 -> 0.787 ms for the 2x32/8x4096x128 prefill).
   auto do_in = [&](size_t c) {
     const size_t u0 = unit0(chunks[c]), nu = units(chunks[c]);
     h2d(oq + u0 * uq, static_cast<const char*>(q) + u0 * uq, nu * uq);
@@ -846,9 +848,8 @@ NV_SDPA_API int nv_sdpa_host(const void* q, const void* k, const void* v, const 
   for (size_t c = 0; c < chunks.size(); ++c) {
     do_in(c);
     do_attn(c);
-    if (c >= 2) do_out(c - 2);
+    do_out(c);
   }
-  for (size_t c = chunks.size() >= 2 ? chunks.size() - 2 : 0; c < chunks.size(); ++c) do_out(c);
   if (piped) {
     if (ce == cudaSuccess) record_wait(ev[1], cps.d2h, cs);
     if (ce != cudaSuccess || st != NV_SDPA_OK) {

@@ -235,11 +235,13 @@ def test_host_buffer_entry_point_matches_device_entry_point():
     np.testing.assert_array_equal(lse, l_dev.cpu().numpy())
 
 
-@pytest.mark.parametrize("mask,sinks", [("causal", False), ("bool", True)])
-def test_large_host_buffer_call_gives_the_device_call_bits(mask, sinks):
+@pytest.mark.parametrize("mask,sinks,out_pinned", [("causal", False, True), ("bool", True, True),
+                                                   ("causal", False, False)])
+def test_large_host_buffer_call_gives_the_device_call_bits(mask, sinks, out_pinned):
     """A large host-buffer call from pinned memory runs as a pipeline over runs of
     (batch item, KV head) units (48 MiB of inputs: 2 batch items x 2 runs of 4 KV heads)
-    and gives every output and lse bit of the single device call."""
+    and gives every output and lse bit of the single device call, with the outputs in
+    page-locked or in pageable memory."""
     import torch
     nv = ensure_built()
     c = W.Case(2, 32, 8, 2048, 2048, 128, 128, "bf16", mask, sinks, None, "n0.5", seed=31)
@@ -250,8 +252,10 @@ def test_large_host_buffer_call_gives_the_device_call_bits(mask, sinks):
     torch.cuda.synchronize()
     pin = {n: torch.from_numpy(np.ascontiguousarray(x[n]).view(np.int16)).pin_memory()
            for n in ("q", "k", "v")}
-    hout = torch.empty((c.B, c.Hq, c.Lq, c.dv), dtype=torch.int16).pin_memory()
-    hlse = torch.empty((c.B, c.Hq, c.Lq), dtype=torch.float32).pin_memory()
+    hout = torch.empty((c.B, c.Hq, c.Lq, c.dv), dtype=torch.int16)
+    hlse = torch.empty((c.B, c.Hq, c.Lq), dtype=torch.float32)
+    if out_pinned:
+        hout, hlse = hout.pin_memory(), hlse.pin_memory()
     st = nv.nv_sdpa_host(pin["q"].data_ptr(), pin["k"].data_ptr(), pin["v"].data_ptr(),
                          (c.B, c.Hq, c.Hkv, c.Lq, c.Lk, c.d, c.dv), nv.MASKS[mask],
                          x["mask"].ctypes.data if mask == "bool" else None,
