@@ -8,6 +8,10 @@ d=128, sinks) in GB/s of K+V read, the end-to-end rate through the host-buffer e
 point, each dominant kernel's roofline fraction, clocks sampled during the timed
 region, and the f64 CPU oracle timed on a bounded sample.
 
+Every line times its calls back to back on one stream, with a pair of CUDA events around
+the timed region only, and rotates over device copies of its inputs (at least six, four
+L2 sizes in all), so that no call finds an earlier call's inputs in L2.
+
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Under torchrun (N > 1) every rank runs its own copy of the workload (weak scaling,
