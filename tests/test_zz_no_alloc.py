@@ -73,3 +73,52 @@ def test_noalloc_rejects_a_plan_beyond_the_static_scratch():
     fake = 1 << 20  # never dereferenced: the size check comes first and launches nothing
     assert nv.nv_sdpa_noalloc(fake, fake, fake, dims, 1, 0, fake, 0.1, fake, 0, 1, 0) == \
         nv.ERR_UNSUPPORTED
+
+
+def test_noalloc_calls_replay_from_a_cuda_graph():
+    """Captured in a CUDA graph -- the kernels' programmatic dependent launches become
+    the graph's programmatic edges -- a boolean-mask prefill (packing + attention) and
+    a split-KV decode (pass 1 + merge), replayed three times with new inputs copied into
+    the captured buffers each time, give the bits of direct nv_sdpa calls."""
+    import torch
+    nv = ensure_built()
+    cases = [W.Case(1, 8, 2, 200, 700, 128, 128, "f16", "bool", True, None, "n0.5", seed=61, name="g_bool"),
+             W.Case(2, 16, 4, 1, 9000, 128, 128, "bf16", "causal", True, None, "n0.5", seed=62, name="g_decode")]
+    from helpers import torch_dtype
+    devs, outs, lses = [], [], []
+    for c in cases:
+        devs.append(upload(c, W.make_inputs(c)))
+        outs.append(torch.empty((c.B, c.Hq, c.Lq, c.dv), dtype=torch_dtype(c.dtype), device="cuda"))
+        lses.append(torch.empty((c.B, c.Hq, c.Lq), dtype=torch.float32, device="cuda"))
+
+    def launch_all():
+        for c, dev, o, l in zip(cases, devs, outs, lses):
+            st = nv.nv_sdpa_noalloc(dev["q"].data_ptr(), dev["k"].data_ptr(), dev["v"].data_ptr(),
+                                    (c.B, c.Hq, c.Hkv, c.Lq, c.Lk, c.d, c.dv), W.MASK_CODES[c.mask],
+                                    dev["mask"].data_ptr() if dev["mask"] is not None else 0,
+                                    dev["sinks"].data_ptr() if dev["sinks"] is not None else 0, c.scale_f32,
+                                    o.data_ptr(), l.data_ptr(), W.DTYPE_CODES[c.dtype],
+                                    torch.cuda.current_stream().cuda_stream)
+            assert st == nv.OK
+    launch_all()  # outside the capture first (the static array's address is looked up)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        launch_all()
+    torch.cuda.synchronize()
+    for rep in range(3):
+        for i, c in enumerate(cases):
+            x = W.make_inputs(c.with_(seed=c.seed + 100 * (rep + 1)))
+            fresh = upload(c, x)
+            for n in ("q", "k", "v"):
+                devs[i][n].copy_(fresh[n])
+        graph.replay()
+        torch.cuda.synchronize()
+        for c, dev, o, l in zip(cases, devs, outs, lses):
+            want, wl = nv.sdpa(dev["q"], dev["k"], dev["v"], mask_kind=c.mask, scale=c.scale_f32,
+                               bool_mask=dev["mask"], sinks=dev["sinks"])
+            torch.cuda.synchronize()
+            bits = torch.int16 if c.dtype != "f32" else torch.int32
+            assert torch.equal(o.view(bits), want.view(bits)), (c.name, rep)
+            assert torch.equal(l, wl), (c.name, rep)
+        assert nv.nv_sdpa_device_status(0) == (nv.OK, 0)
