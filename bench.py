@@ -591,7 +591,7 @@ def run_ours(args):
     if pg:
         pg.barrier()
     sampler.mark()
-    total_ms, launch_ms = time_calls(torch, pcall, psets, args.steps, 0, stream)
+    total_ms, per_call_ms = time_calls(torch, pcall, psets, args.steps, 0, stream)
     sampler.mark()
     if pg:
         pg.barrier()
@@ -599,7 +599,7 @@ def run_ours(args):
     total_ms_max = max_over_ranks(torch, pg, total_ms, dev)
     flops_step = prefill_flops(pc)
     value = whole_job_rate(ws, flops_step, args.steps, total_ms_max / 1e3)
-    launch_avg = launch_ms
+    launch_avg = per_call_ms  # one launch per step
     p_steady = steady_ms(torch, pcall, psets, stream)
     peak_t = pk["bf16_tflops"]
     p_achieved = flops_step / (launch_avg / 1e3) / 1e12
