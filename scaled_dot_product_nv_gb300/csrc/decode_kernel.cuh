@@ -170,8 +170,21 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
   // take their block from it by a shuffle, refilled 32 pages at a time.
   int64_t ebase = -(int64_t(1) << 40);
   int ent = 0;
+  // (keys and pages in 32 bits when the table's capacity fits: a 64-bit division per tile
+  // costs more than the tile's other integer work)
+  const bool cap32 = p.max_pages * p.page <= 0x7fffffff;
+  auto page_of = [&](int64_t key, int& pos) -> int64_t {  // page index and position in it
+    if (cap32) {
+      const uint32_t k32 = (uint32_t)key, pg32 = k32 / (uint32_t)p.page;
+      pos = (int)(k32 - pg32 * (uint32_t)p.page);
+      return pg32;
+    }
+    pos = (int)(key % p.page);
+    return key / p.page;
+  };
   auto page_entry = [&](int64_t key) -> int {  // every lane, the same key
-    int64_t pg = key / p.page;
+    int pos_unused;
+    int64_t pg = page_of(key, pos_unused);
     if (pg >= p.max_pages) pg = p.max_pages - 1;  // only past the sequence's end
     if (pg < ebase || pg >= ebase + 32) {
       ebase = pg;
@@ -207,7 +220,8 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
       for (int u = 0; u * R < kKT; ++u) {
         const int64_t kk = key0 + u * R;
         const int blk = page_entry(kk);
-        const int pos = (int)(kk % p.page);
+        int pos;
+        page_of(kk, pos);
         if (lane == 0) {
           for (int pn = 0; pn < a.dpanels; ++pn)
             tma_load_4d_hint(ring + s * stage_bytes + pn * kKT * 128 + u * R * 128, &a.tmk, full(s), pn * 64, pos,
