@@ -444,6 +444,16 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
   }
 
   bool ok = true;
+  // this tile's key block (c_begin + blk_rel) and the block's last key + 1.  The paged
+  // forms count them along (a division per tile slowed their streams, 5,043 -> 5,564
+  // GB/s); the strided form divides (counting along measured 1.5 % slower there).
+  int blk_rel = 0, in_blk = 0;
+  int j_end = 0;
+  auto block_end = [&](int rel) {
+    const int64_t jb_end = u_lo + (c_begin + rel + 1) * p.keys_per_blk;
+    return (int)(jb_end < key_end ? jb_end : key_end);
+  };
+  if (KV != kKvTma && n_tiles > 0) j_end = block_end(0);
   for (int gt = 0; gt < n_tiles; ++gt) {
     const int s = gt % ST;
     if constexpr (KV == kKvPagedRows) cp_async_wait<ST - 1>();
@@ -453,9 +463,11 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
       break;
     }
     consumed = gt + 1;
-    const int64_t c = c_begin + gt / tpb;  // key block of this tile
-    const int64_t jb_end = u_lo + (c + 1) * p.keys_per_blk;
-    const int j_end = (int)(jb_end < key_end ? jb_end : key_end);
+    if constexpr (KV == kKvTma) {
+      blk_rel = gt / tpb;
+      j_end = block_end(blk_rel);
+    }
+    const int64_t c = c_begin + blk_rel;  // key block of this tile
     const uint32_t kst = ring + s * stage_bytes, vst = kst + k_bytes;
     if constexpr (SW) {
       // ---- S^T = K Q^T: per 16 keys one m16 (keys) x n8 (query rows) tile; sc[e] holds
@@ -627,7 +639,14 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
     if constexpr (KV == kKvPagedRows) cp_async_commit();
 
     // ---- end of a key block: write its partial (or the output when it is the only one)
-    if ((gt + 1) % tpb == 0 || gt + 1 == n_tiles) flush(c);
+    if constexpr (KV == kKvTma) {
+      if ((gt + 1) % tpb == 0 || gt + 1 == n_tiles) flush(c);
+    } else if (++in_blk == tpb || gt + 1 == n_tiles) {
+      flush(c);
+      in_blk = 0;
+      ++blk_rel;
+      j_end = block_end(blk_rel);
+    }
   }
   if (ok) {
     // key blocks of this run that hold no key of this tile's rows (past a sequence's
