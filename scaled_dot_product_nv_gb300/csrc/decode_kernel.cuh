@@ -182,9 +182,9 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
     pos = (int)(key % p.page);
     return key / p.page;
   };
-  auto page_entry = [&](int64_t key) -> int {  // every lane, the same key
-    int pos_unused;
-    int64_t pg = page_of(key, pos_unused);
+  int64_t next_key = -1, next_pg = 0;  // the next tile's first key, its page and position
+  int next_pos = 0;
+  auto page_entry = [&](int64_t pg) -> int {  // every lane, the same page
     if (pg >= p.max_pages) pg = p.max_pages - 1;  // only past the sequence's end
     if (pg < ebase || pg >= ebase + 32) {
       ebase = pg;
@@ -217,11 +217,13 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
     } else if constexpr (KV == kKvPagedTma) {
       const int R = a.sub_rows;
       if (lane == 0) mbar_arrive_expect_tx(full(s), stage_bytes);
+      // the page and position of key0: carried over from the previous tile (tiles are
+      // issued in order, kKT keys apart), divided out only for the run's first
+      if (key0 != next_key) next_pg = page_of(key0, next_pos);
+      int64_t pg = next_pg;
+      int pos = next_pos;
       for (int u = 0; u * R < kKT; ++u) {
-        const int64_t kk = key0 + u * R;
-        const int blk = page_entry(kk);
-        int pos;
-        page_of(kk, pos);
+        const int blk = page_entry(pg);
         if (lane == 0) {
           for (int pn = 0; pn < a.dpanels; ++pn)
             tma_load_4d_hint(ring + s * stage_bytes + pn * kKT * 128 + u * R * 128, &a.tmk, full(s), pn * 64, pos,
@@ -230,7 +232,16 @@ sdpa_decode_mma(const __grid_constant__ DecArgs a) {
             tma_load_4d_hint(ring + s * stage_bytes + k_bytes + pn * kKT * 128 + u * R * 128, &a.tmv, full(s),
                              pn * 64, pos, (int)hkv, blk, l2_once);
         }
+        // (a box never crosses a page: R divides the page size)
+        pos += R;
+        if (pos >= (int)p.page) {
+          pos -= (int)p.page;
+          ++pg;
+        }
       }
+      next_key = key0 + kKT;
+      next_pg = pg;
+      next_pos = pos;
     } else {
       const int ck = (int)(p.d / 8), cv = (int)(p.dv / 8);  // 16-byte chunks of a K / V row
       const int pk = a.dpanels * 8, pv = a.dvpanels * 8;    // chunks of a panelled smem row
