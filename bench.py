@@ -613,12 +613,15 @@ def run_ours(args):
                                W.MASK_CODES[dc.mask], 1, W.DTYPE_CODES[dc.dtype])
     dsteps = max(args.steps, 50)
     d_total, d_launch = time_calls(torch, caller(dc), dsets, dsteps, max(args.warmup, 3), stream)
+    d_steady = steady_ms(torch, caller(dc), dsets, stream)
     dbytes = kv_bytes(dc)
     d_call_avg = d_launch
     d_gbs = dbytes / (d_call_avg / 1e3) / 1e9
     decode = {
         "workload": dc.name, "metric": "decode KV GB/s", "value": round(d_gbs, 1), "unit": "GB/s",
         "ms_per_call": round(d_call_avg, 5), "steps": dsteps, "kernel": dplan["kernel"],
+        "steady_ms_per_call": d_steady[0], "steady_windows_ms": d_steady[1],
+        "steady_gbs": round(dbytes / (d_steady[0] / 1e3) / 1e9, 1),
         "l2": f"inputs rotate over {len(dsets)} device copies",
         "nblk": dplan["nblk"], "launches_per_call": dplan["launches"],
         "roofline": {"bound": "hbm", "achieved": round(d_gbs, 1), "peak": pk["hbm_gbs"],
@@ -638,12 +641,15 @@ def run_ours(args):
                                W.MASK_CODES[mc.mask], 1, W.DTYPE_CODES[mc.dtype])
     msteps = max(args.steps, 50)
     _, m_launch = time_calls(torch, caller(mc), msets, msteps, max(args.warmup, 3), stream)
+    m_steady = steady_ms(torch, caller(mc), msets, stream)
     mflops = prefill_flops(mc)  # dense: a boolean mask is not halved
     m_call_avg = m_launch
     m_tf = mflops / (m_call_avg / 1e3) / 1e12
     prefill_mask = {
         "workload": mc.name, "metric": "prefill attention TFLOP/s", "value": round(m_tf, 2),
         "unit": "TFLOP/s", "ms_per_call": round(m_call_avg, 5), "steps": msteps,
+        "steady_ms_per_call": m_steady[0], "steady_windows_ms": m_steady[1],
+        "steady_tflops": round(mflops / (m_steady[0] / 1e3) / 1e12, 2),
         "kernel": mplan["kernel"], "launches_per_call": mplan["launches"],
         "flops_per_call": mflops,
         "l2": f"inputs rotate over {len(msets)} device copies",
