@@ -247,12 +247,35 @@ def nv_sdpa_abi_version() -> int:
 
 # ----------------------------------------------------------------------------- torch
 
+_TORCH_DTYPE_CODES = None
+_RAW_STREAM = None
+
+
 def _torch_dtype_code(t):
-    import torch
-    m = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
-    if t.dtype not in m:
+    global _TORCH_DTYPE_CODES
+    if _TORCH_DTYPE_CODES is None:
+        import torch
+        _TORCH_DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+    code = _TORCH_DTYPE_CODES.get(t.dtype)
+    if code is None:
         raise TypeError(f"unsupported dtype {t.dtype}")
-    return m[t.dtype]
+    return code
+
+
+def _stream_handle(stream, t):
+    """The cudaStream_t to launch on: `stream` (a torch.cuda.Stream) if given, else torch's
+    current stream on t's device (read without building a Stream object where torch
+    exposes the raw handle: the lookup is part of every call's host time)."""
+    global _RAW_STREAM
+    if stream is not None:
+        return stream.cuda_stream
+    if _RAW_STREAM is None:
+        import torch
+        _RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", False)
+    if _RAW_STREAM:
+        return _RAW_STREAM(t.get_device())
+    import torch
+    return torch.cuda.current_stream(t.device).cuda_stream
 
 
 def _bhl_strides(t):
@@ -260,6 +283,11 @@ def _bhl_strides(t):
     if t.stride(3) != 1 and t.shape[3] > 1:
         raise ValueError("the head dimension must be contiguous")
     return tuple(int(x) for x in t.stride()[:3])
+
+
+def _strides_or_none(t, contiguous):
+    """None (zero strides: the contiguous layout) for a contiguous tensor, else its strides."""
+    return None if contiguous else _bhl_strides(t)
 
 
 def sdpa(q, k, v, *, mask_kind: str = "none", scale: Optional[float] = None, bool_mask=None,
@@ -294,9 +322,9 @@ def sdpa(q, k, v, *, mask_kind: str = "none", scale: Optional[float] = None, boo
     mk = MASKS[mask_kind] if isinstance(mask_kind, str) else int(mask_kind)
     if bool_mask is not None and bool_mask.dtype != torch.uint8:
         bool_mask = bool_mask.to(torch.uint8)
-    st = (stream or torch.cuda.current_stream(q.device)).cuda_stream
-    plain = (all(t.is_contiguous() for t in (q, k, v, out)) and window is None and add_mask is None
-             and mk != MASKS["add"])
+    st = _stream_handle(stream, q)
+    cq, ck, cv, co = q.is_contiguous(), k.is_contiguous(), v.is_contiguous(), out.is_contiguous()
+    plain = cq and ck and cv and co and window is None and add_mask is None and mk != MASKS["add"]
     if plain:
         status = nv_sdpa(q.data_ptr(), k.data_ptr(), v.data_ptr(), (B, Hq, Hkv, Lq, Lk, d, dv), mk,
                          bool_mask.data_ptr() if (bool_mask is not None and mk == 2) else 0,
@@ -310,8 +338,8 @@ def sdpa(q, k, v, *, mask_kind: str = "none", scale: Optional[float] = None, boo
                 raise ValueError("add_mask must be a contiguous [1|B, 1|Hq, Lq, Lk] tensor")
             am, mb, mh = add_mask.data_ptr(), add_mask.shape[0], add_mask.shape[1]
         opts = make_options(window=window, add_mask=am, add_mask_b=mb, add_mask_h=mh,
-                            q_strides=_bhl_strides(q), k_strides=_bhl_strides(k),
-                            v_strides=_bhl_strides(v), out_strides=_bhl_strides(out))
+                            q_strides=_strides_or_none(q, cq), k_strides=_strides_or_none(k, ck),
+                            v_strides=_strides_or_none(v, cv), out_strides=_strides_or_none(out, co))
         status = nv_sdpa_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), (B, Hq, Hkv, Lq, Lk, d, dv), mk,
                             bool_mask.data_ptr() if (bool_mask is not None and mk == 2) else 0,
                             sinks.data_ptr() if sinks is not None else 0, float(scale), opts,
@@ -344,7 +372,7 @@ def sdpa_paged(q, k_cache, v_cache, block_table, seq_lens, *, mask_kind: str = "
     if lse is None and want_lse:
         lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
     mk = MASKS[mask_kind] if isinstance(mask_kind, str) else int(mask_kind)
-    st = (stream or torch.cuda.current_stream(q.device)).cuda_stream
+    st = _stream_handle(stream, q)
     status = nv_sdpa_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
                            seq_lens.data_ptr(), (B, Hq, Hkv, Lq, d, dv, nb, bs, block_table.shape[1]),
                            mk, window is not None, int(window or 0),
