@@ -130,6 +130,10 @@ typedef struct {
  * (cudaMallocFromPoolAsync on `stream`) and frees it with cudaFreeAsync on the same
  * stream; the pool keeps freed blocks for later calls (at most the largest call's
  * scratch at a time).  Nothing else is allocated, nothing synchronises.
+ * Graphs: while `stream` is being captured, the scratch comes from cudaMallocAsync and
+ * is freed in the same capture, so the graph holds its own allocation and free nodes;
+ * each replay computes what the captured call would have.  Make one call outside the
+ * capture first: it sets the kernels' attributes and looks up the device status word.
  * Returns NV_SDPA_OK or an nv_sdpa_status; on error nothing was launched (INVALID,
  * UNSUPPORTED) or a launch failed (CUDA). */
 int nv_sdpa(const void* q, const void* k, const void* v, const nv_sdpa_dims* dims,

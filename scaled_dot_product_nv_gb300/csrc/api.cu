@@ -557,12 +557,21 @@ cudaError_t launch_plan(int dtype, const nv_sdpa_plan_t& pl, Params& p, void* sc
 
 namespace nvsdpa {
 namespace {
-// Runs a prepared call with its scratch from the library's pool on `stream`.
+// Runs a prepared call with its scratch from the library's pool on `stream`.  While the
+// stream is being captured into a CUDA graph the scratch comes from cudaMallocAsync
+// instead, which capture records as the graph's own allocation and free nodes (the
+// library's pool is not one a graph can allocate from).
 int run_pooled(int dtype, const nv_sdpa_plan_t& pl, Params& p, void* stream) {
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   void* scratch = nullptr;
-  if (pl.scratch_bytes && pool_alloc(&scratch, (size_t)pl.scratch_bytes, cs) != cudaSuccess)
-    return NV_SDPA_ERR_CUDA;
+  if (pl.scratch_bytes) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(cs, &cap) != cudaSuccess) return NV_SDPA_ERR_CUDA;
+    const cudaError_t ae = cap == cudaStreamCaptureStatusActive
+                               ? cudaMallocAsync(&scratch, (size_t)pl.scratch_bytes, cs)
+                               : pool_alloc(&scratch, (size_t)pl.scratch_bytes, cs);
+    if (ae != cudaSuccess) return NV_SDPA_ERR_CUDA;
+  }
   cudaError_t ce = launch_plan(dtype, pl, p, scratch, cs);
   if (scratch) {
     cudaError_t fe = cudaFreeAsync(scratch, cs);
