@@ -931,6 +931,13 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), (tc_ctas_per_sm<BN, NQ, MM>(
       const int64_t am_row_off =
           MM == kMmAdd ? (int64_t)(reinterpret_cast<const T*>(mrow_any) - reinterpret_cast<const T*>(p.amask)) : 0;
       const int am_m = (int)(am_row_off & 7);  // (the tensor starts on a 16-byte boundary)
+      // this row's slot in the staging buffers.  A slot's pitch is 4 words past a multiple
+      // of 32 banks, and a row's tile starts (am_m >> 1) words into it; with the rows in
+      // slot order a warp's 32-bit reads of its 32 rows met 4 to a bank.  Slot 8 j + 2 q + e
+      // holds lane 8 q + 2 j + e: the four lanes sharing a bank group (same q and e) then
+      // start at four different word phases whenever Lk is odd (consecutive queries of one
+      // row tile), and the reads are free of conflicts
+      const int am_slot = q4 * 32 + 8 * ((lane & 7) >> 1) + 2 * (lane >> 3) + (lane & 1);
       // this row's copy of chunk c (key tiles [kAmTiles c, kAmTiles c + kAmTiles) of the walk)
       // into buffer c & 1: [a0, a0 + row bytes) from the 8-element boundary at or below its
       // first column, clipped to the tensor's last 16-byte boundary; every softmax thread
@@ -949,7 +956,7 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), (tc_ctas_per_sm<BN, NQ, MM>(
           // (the buffer's previous contents were read by this thread alone, by generic loads)
           fence_proxy_async_smem();
           mbar_arrive_expect_tx(fb, n);
-          if (n) bulk_load(sM + b * (kBM * am_row_bytes<BN>()) + row * am_row_bytes<BN>(),
+          if (n) bulk_load(sM + b * (kBM * am_row_bytes<BN>()) + am_slot * am_row_bytes<BN>(),
                            reinterpret_cast<const T*>(p.amask) + a0, n, fb);
         }
       };
@@ -971,7 +978,7 @@ __global__ void __launch_bounds__(tc_threads<NQ>(), (tc_ctas_per_sm<BN, NQ, MM>(
             chunks_seen = c + 1;
           }
           const int e0 = am_m + (t % kAmTiles) * BN;
-          const uint32_t rs = sM + b * (kBM * am_row_bytes<BN>()) + row * am_row_bytes<BN>() + (e0 >> 1) * 4;
+          const uint32_t rs = sM + b * (kBM * am_row_bytes<BN>()) + am_slot * am_row_bytes<BN>() + (e0 >> 1) * 4;
           uint32_t w[BN / 2 + 1];
 #pragma unroll
           for (int k = 0; k < BN / 2 + 1; ++k)
