@@ -208,3 +208,28 @@ def test_package_never_imports_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 src = open(os.path.join(dp, f)).read()
                 assert not re.search(r"\boracle\b", src.replace("oracle is", "")), f
+
+
+def test_wrapper_passes_zero_strides_for_contiguous_tensors(nv):
+    """The torch wrapper hands the options struct strides only for tensors that are not
+    contiguous: zero strides are the header's contiguous layout, and skipping them keeps
+    a windowed call's host time down."""
+    import torch
+    t = torch.empty(2, 3, 5, 8)
+    assert nv._strides_or_none(t, t.is_contiguous()) is None
+    v = torch.empty(2, 5, 3, 8).transpose(1, 2)  # a [B, L, H, D] buffer viewed as [B, H, L, D]
+    assert not v.is_contiguous()
+    assert nv._strides_or_none(v, False) == (5 * 3 * 8, 8, 3 * 8)
+    o = nv.make_options(window=7, q_strides=None, k_strides=nv._strides_or_none(v, False))
+    assert (o.has_window, o.window) == (1, 7)
+    assert list(o.q_strides) == [0, 0, 0] and list(o.k_strides) == [120, 8, 24]
+    assert list(o.v_strides) == [0, 0, 0] and list(o.out_strides) == [0, 0, 0]
+    with pytest.raises(ValueError):
+        nv._bhl_strides(torch.empty(2, 3, 8, 5).transpose(2, 3))  # head dimension not contiguous
+
+
+def test_wrapper_launches_on_a_given_stream(nv):
+    """An explicit stream object's handle is used as is (no current-stream lookup)."""
+    class FakeStream:
+        cuda_stream = 0x1234
+    assert nv._stream_handle(FakeStream(), None) == 0x1234
